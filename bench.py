@@ -1,0 +1,380 @@
+"""Benchmark: one decode step of load-balanced split-KV GQA attention.
+
+A step is the whole path over one synthetic batch: Task Assign (hpa_plan),
+split-KV attention (hpa_decode_attn) and the combine (hpa_combine), on one
+stream.  Default workload: the mixed-length batch (40 requests log-uniform
+in [1K, 128K] + one each of 1K/4K/16K/64K/128K; 64/8 heads, d=128; bf16 KV
+in 64-token pages with shuffled page ids; tile 512; one partition per
+resident attention CTA).  Its KV (about 7 GB) is far larger than L2, so no
+flush is needed between steps.
+
+  python bench.py [--gpus N --steps K --warmup W] [--config 1..5] [--impl reference]
+
+Prints one JSON line (rank 0).  Under torchrun each rank runs its own batch
+(seeded by rank) on its own GPU -- data-parallel replicas with no collective
+on the data path -- and the timing is the max over ranks.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import tempfile
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+
+import workloads as W  # noqa: E402
+
+METRIC = "mixed-length decode attention: µs/batch, KV-read HBM GB/s and % of peak"
+UNIT = "us/batch"
+
+# DRAM traffic of one decode_attn_kernel launch from an ncu capture, valid only
+# for the kernel source it was taken on (sha256 of decode_attn.cu); else null.
+TRAFFIC_PROFILE = {"source_sha256": None, "bytes_per_kv_byte": None, "workload": None}
+
+
+def peaks():
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        d = json.load(open(p))
+        return float(d["hbm_gbs"]), "measured"
+    return 6800.0, "fallback"
+
+
+def kernel_sha():
+    src = os.path.join(ROOT, "load_balanced_split_gb300", "csrc", "decode_attn.cu")
+    return hashlib.sha256(open(src, "rb").read()).hexdigest()
+
+
+# ----------------------------------------------------------------------------- clocks
+class ClockSampler:
+    """nvidia-smi clocks / throttle reasons sampled every 200 ms while running."""
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, device_index):
+        self.dev = device_index
+        self.proc = None
+        self.f = None
+
+    def __enter__(self):
+        try:
+            self.f = tempfile.TemporaryFile(mode="w+")
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "--query-gpu=" + self.FIELDS, "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.dev)], stdout=self.f, stderr=subprocess.DEVNULL)
+            time.sleep(0.3)
+        except Exception:
+            self.proc = None
+        return self
+
+    def __exit__(self, *a):
+        if self.proc is not None:
+            time.sleep(0.25)
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except Exception:
+                self.proc.kill()
+
+    def summary(self):
+        if self.proc is None or self.f is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        self.f.seek(0)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.f.read().splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None, "samples": len(sm),
+                "reasons": sorted(reasons)}
+
+
+# ----------------------------------------------------------------------------- our arm
+def run_ours(args, rank, world, local_rank):
+    import torch
+    import load_balanced_split_gb300 as hpa
+
+    torch.cuda.set_device(local_rank)
+    dev = torch.device("cuda", local_rank)
+    b = W.make_config(args.config, seed=args.seed + rank)
+    kv = hpa.KV_BF16 if b.kv_dtype == "bf16" else hpa.KV_E4M3
+    C = b.num_ctas or hpa.hpa_default_num_ctas(b.Hkv, b.q_len, kv)
+    q = b.q.to(dev)
+    k, v = b.k_pool.to(dev), b.v_pool.to(dev)
+    ks = vs = None
+    if kv == hpa.KV_E4M3:
+        ks = torch.from_numpy(b.k_scale).to(dev)
+        vs = torch.from_numpy(b.v_scale).to(dev)
+    lens = torch.from_numpy(b.seq_lens).to(dev)
+    indptr = torch.from_numpy(b.page_indptr).to(dev)
+    indices = torch.from_numpy(b.page_indices).to(dev)
+    ws = hpa.Workspace(b.B, b.q_len, b.Hq, b.d, num_ctas=C, device=dev)
+    out = torch.empty((b.B, b.q_len, b.Hq, b.d), dtype=torch.bfloat16, device=dev)
+    out_lse = torch.empty((b.B, b.q_len, b.Hq), dtype=torch.float32, device=dev)
+    stream = torch.cuda.Stream(device=dev)
+
+    def step(w=ws, ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        w.plan(lens, b.tile, stream)
+        if ev is not None:
+            ev[1].record(stream)
+        hpa.hpa_decode_attn(q, k, v, indptr, indices, w.taskmap, w.num_ctas, w.partial_o,
+                            w.partial_lse, ks, vs, stream=stream)
+        if ev is not None:
+            ev[2].record(stream)
+        hpa.hpa_combine(w.partial_o, w.partial_lse, w.taskmap, w.num_ctas, out, out_lse, stream)
+        if ev is not None:
+            ev[3].record(stream)
+
+    def barrier():
+        if world > 1:
+            import torch.distributed as dist
+            dist.barrier()
+
+    def timed(fn, steps, warmup, sampler=None):
+        for _ in range(warmup):
+            fn()
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        torch.cuda.synchronize(dev)
+        barrier()
+        torch.cuda.synchronize(dev)
+        for i in range(steps):
+            fn(ev=evs[i])
+        torch.cuda.synchronize(dev)
+        barrier()
+        total = evs[0][0].elapsed_time(evs[-1][3])
+        attn = [e[1].elapsed_time(e[2]) for e in evs]
+        plan = [e[0].elapsed_time(e[1]) for e in evs]
+        comb = [e[2].elapsed_time(e[3]) for e in evs]
+        return total / steps, attn, plan, comb
+
+    with ClockSampler(local_rank) as clk:
+        ms, attn, plan_ms, comb_ms = timed(step, args.steps, args.warmup)
+    clocks = clk.summary()
+    torch.cuda.synchronize(dev)
+    status = ws.status()
+    if status != 0:
+        raise RuntimeError("task map status %d after the timed steps" % status)
+
+    # max over ranks of the per-step time
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        ms = float(t.item())
+
+    # static split-KV comparators through the same kernels (heuristic and best of a sweep)
+    comparator = None
+    if not args.no_static and rank == 0:
+        max_tiles = int((b.seq_lens.max() + b.tile - 1) // b.tile)
+        heur = max(1, min(max_tiles, math.ceil(C / b.B)))
+        sweep = sorted(set([heur] + [s for s in (1, 2, 4, 8, 16, 32, 64, 128) if s <= max_tiles]))
+        res = {}
+        for s in sweep:
+            wss = hpa.Workspace(b.B, b.q_len, b.Hq, b.d, splits=s, device=dev)
+            res[s] = timed(lambda ev=None, w=wss: step(w, ev), max(3, args.steps // 2), 2)[0]
+        best = min(res, key=res.get)
+        comparator = {
+            "static_heuristic": {"splits": heur, "us_per_batch": round(res[heur] * 1e3, 2)},
+            "static_best": {"splits": best, "us_per_batch": round(res[best] * 1e3, 2)},
+            "sweep_us": {str(s): round(t * 1e3, 2) for s, t in res.items()},
+            "speedup_vs_static_heuristic": round(res[heur] / ms, 3),
+            "speedup_vs_static_best": round(res[best] / ms, 3),
+        }
+
+    # end to end through the public API with host buffers
+    pin = lambda t: t.pin_memory()
+    q_h, lens_h, indptr_h, indices_h = (pin(b.q), pin(torch.from_numpy(b.seq_lens)),
+                                        pin(torch.from_numpy(b.page_indptr)),
+                                        pin(torch.from_numpy(b.page_indices)))
+    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
+    lse_h = torch.empty(out_lse.shape, dtype=out_lse.dtype).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (q_h, lens_h, indptr_h, indices_h))
+    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+
+    def e2e_step(ev=None):
+        if ev is not None:
+            ev[0].record(stream)
+        with torch.cuda.stream(stream):
+            q.copy_(q_h, non_blocking=True)
+            lens.copy_(lens_h, non_blocking=True)
+            indptr.copy_(indptr_h, non_blocking=True)
+            indices.copy_(indices_h, non_blocking=True)
+        hpa.decode_step(ws, q, k, v, lens, indptr, indices, out, out_lse, ks, vs, tile=b.tile,
+                        stream=stream)
+        with torch.cuda.stream(stream):
+            out_h.copy_(out, non_blocking=True)
+            lse_h.copy_(out_lse, non_blocking=True)
+        if ev is not None:
+            for e in ev[1:]:
+                e.record(stream)
+
+    e2e_ms = timed(e2e_step, args.steps, args.warmup)[0]
+    if world > 1:
+        import torch.distributed as dist
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+
+    return dict(b=b, C=C, ms=ms, attn=attn, plan=plan_ms, comb=comb_ms, clocks=clocks,
+                comparator=comparator, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
+
+
+# ----------------------------------------------------------------------------- CPU oracle
+def oracle_sample(b, target_s):
+    """Time the oracle on a prefix of the batch's requests (about target_s seconds).
+
+    Returns (seconds per batch extrapolated by token count, threads, description)."""
+    import oracle
+    threads = os.cpu_count() or 1
+    order = list(range(b.B))
+    # calibrate on the first request, then take a prefix worth ~target_s
+    t0 = time.perf_counter()
+    oracle.attention(b, items=[(0, 0, int(b.seq_lens[0]))], n_threads=threads)
+    t1 = time.perf_counter() - t0
+    rate = int(b.seq_lens[0]) / max(t1, 1e-6)                # tokens per second
+    want = max(int(rate * target_s), 1)
+    items, tok = [], 0
+    for r in order:
+        if tok >= want:
+            break
+        items.append((r, 0, int(b.seq_lens[r])))
+        tok += int(b.seq_lens[r])
+    t0 = time.perf_counter()
+    oracle.attention(b, items=items, n_threads=threads)
+    dt = time.perf_counter() - t0
+    total = int(b.seq_lens.astype(np.int64).sum())
+    per_batch = dt * total / tok
+    desc = ("fp64 C oracle, unsplit attention of the first %d of %d requests (%d of %d tokens, "
+            "all %d heads), scaled to the batch by token count" % (len(items), b.B, tok, total,
+                                                                   b.Hq))
+    return per_batch, threads, desc
+
+
+def run_reference(args, rank, world):
+    if rank != 0:
+        return None
+    b = W.make_config(args.config, seed=args.seed)
+    for _ in range(args.warmup):
+        oracle_sample(b, 1.0)
+    secs, threads, desc = [], 0, ""
+    t_begin = time.perf_counter()
+    per_step_s = max(2.0, min(20.0, 120.0 / max(1, args.steps)))
+    for _ in range(args.steps):
+        s, threads, desc = oracle_sample(b, per_step_s)
+        secs.append(s)
+    wall = time.perf_counter() - t_begin
+    us = statistics.mean(secs) * 1e6
+    return {"impl": "reference", "metric": METRIC, "value": round(us, 1), "unit": UNIT,
+            "n_gpus": world, "steps": args.steps, "warmup": args.warmup,
+            "ms_per_step": round(us / 1e3, 3), "higher_is_better": False, "scaling": "weak",
+            "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": W.CONFIGS[args.config], "batch": int(b.B),
+                       "kv_tokens": int(b.seq_lens.sum()), "q_len": b.q_len,
+                       "heads": "64q/8kv", "head_dim": 128, "kv_dtype": b.kv_dtype,
+                       "seed": args.seed},
+            "cpu_baseline": {"value": round(us, 1), "unit": UNIT, "cores": threads,
+                             "kind": "oracle", "sample": desc},
+            "e2e": {"value": round(us, 1), "unit": UNIT, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0},
+            "wall_s": round(wall, 1)}
+
+
+# ----------------------------------------------------------------------------- main
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=20)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--no-static", action="store_true", help="skip the static comparators")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local_rank = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1 and args.impl == "ours":
+        import torch.distributed as dist
+        dist.init_process_group("nccl")
+
+    if args.impl == "reference":
+        line = run_reference(args, rank, world)
+        if line is not None:
+            print(json.dumps(line), flush=True)
+        return
+
+    r = run_ours(args, rank, world, local_rank)
+    if rank != 0:
+        return
+    b = r["b"]
+    kv_bytes = b.kv_bytes
+    peak, peak_kind = peaks()
+    attn_ms = statistics.mean(r["attn"])
+    achieved = kv_bytes / (attn_ms * 1e-3) / 1e9
+    us_batch = r["ms"] * 1e3 / world
+    traffic = None
+    if TRAFFIC_PROFILE["source_sha256"] == kernel_sha() and TRAFFIC_PROFILE["bytes_per_kv_byte"]:
+        traffic = int(TRAFFIC_PROFILE["bytes_per_kv_byte"] * kv_bytes)
+    cpu = None
+    if not args.no_cpu_baseline:
+        s, threads, desc = oracle_sample(b, 15.0)
+        cpu = {"value": round(s * 1e6, 1), "unit": UNIT, "cores": threads, "kind": "oracle",
+               "sample": desc}
+    line = {
+        "metric": METRIC, "value": round(us_batch, 2), "unit": UNIT, "n_gpus": world,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms"], 4),
+        "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
+        "dtype": b.kv_dtype, "data": "synthetic",
+        "config": {"workload": W.CONFIGS[args.config], "batch": int(b.B),
+                   "kv_tokens": int(b.seq_lens.sum()), "q_len": b.q_len, "heads": "64q/8kv",
+                   "head_dim": 128, "page": 64, "tile": b.tile, "num_ctas": int(r["C"]),
+                   "kv_dtype": b.kv_dtype, "kv_bytes": int(kv_bytes),
+                   "l2": "inputs larger than L2 (%.2f GB KV), no flush" % (kv_bytes / 1e9),
+                   "parallelism": "dp%d replicas" % world, "seed": args.seed},
+        "kv_gbs": round(kv_bytes / (r["ms"] * 1e-3) / 1e9, 1),
+        "pct_of_hbm_peak": round(100.0 * kv_bytes / (r["ms"] * 1e-3) / 1e9 / peak, 1),
+        "breakdown_us": {"plan": round(statistics.mean(r["plan"]) * 1e3, 2),
+                         "attention": round(attn_ms * 1e3, 2),
+                         "combine": round(statistics.mean(r["comb"]) * 1e3, 2)},
+        "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
+                     "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
+                     "kernel": "decode_attn_kernel", "peak_kind": peak_kind + " (hbm_gbs)"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": round(r["e2e_ms"] * 1e3 / world, 2), "unit": UNIT,
+                "h2d_bytes_per_step": int(r["h2d"]), "d2h_bytes_per_step": int(r["d2h"])},
+        "gpu_launches": 3 * args.steps,
+        "clocks": r["clocks"],
+        "comparator": r["comparator"],
+    }
+    print(json.dumps(line), flush=True)
+
+
+if __name__ == "__main__":
+    main()

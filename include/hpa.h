@@ -1,0 +1,185 @@
+/*
+ * hpa.h -- load-balanced split-KV GQA decode attention for NVIDIA GB300 (sm_103a).
+ *
+ * C ABI.  Every pointer argument named *_dev is a device pointer allocated by
+ * the caller; the library never allocates or frees memory and never
+ * synchronises a stream.  All work is enqueued on the caller's stream in
+ * stream order, so the three calls below can be captured in a CUDA graph.
+ *
+ * The method (sources are web pages, cited by title and section):
+ *   [Notes §3.1]  "Hy3 Preview AI Infra 推理优化精读笔记", §3.1 "Attention：动态切分和
+ *                 负载均衡" -- cut every request's KV into uniform tiles, join all
+ *                 tiles into one stream, give each CTA an equal (or +1) budget of
+ *                 it, build a task map before the step, have the attention
+ *                 kernel take its tiles from the map, merge split results in a
+ *                 combine kernel.  Worked example: lengths 1024/5120/2048, tile
+ *                 512 -> 2/10/4 tiles, 4 CTAs x 4 tiles, the long request spans
+ *                 CTAs.
+ *   [HPC-Ops §二.1] "腾讯混元AI Infra进化：HPC-Ops推理核心算子全面升级", §二.1
+ *                 "Attention：动态调度负载均衡" -- a Task Assign module builds the
+ *                 map once per inference step; the attention kernel of every
+ *                 layer reads it; a Combine kernel merges the split-KV results.
+ *   [Stack §二.1]  "大模型推理性能优化新范式：Hy3架构下的全栈优化技术拆解", §二.1 --
+ *                 budget base = T / C, the first T % C CTAs get one more tile.
+ *   [Notes §2]    same notes page, §2 -- 64 query heads, 8 KV heads, head dim 128.
+ *
+ * Units used below: B requests; L_r the KV length of request r (counting its
+ * q_len new tokens); T the total number of tiles; C = num_ctas, the number of
+ * partitions of the tile stream; each partition runs once per KV head, so
+ * the attention grid has C x Hkv CTAs.
+ *
+ * Error behaviour: every call validates its host-visible arguments first and
+ * returns a negative HPA_ERR_* code without launching anything when one is
+ * wrong.  Problems only the device can see (sequence lengths, page ids, a
+ * task map built for another shape, a pipeline wait that ran past its time
+ * bound) set bits in the task map's status word (int32 word 6 of the map,
+ * HPA_STATUS_*); the attention kernel then does no work and the combine
+ * kernel writes NaN to every output element, so a bad step cannot pass
+ * silently.  Asynchronous CUDA faults surface at the caller's next sync.
+ */
+#ifndef HPA_H
+#define HPA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* A cudaStream_t (the runtime's stream handle); NULL is the legacy default stream. */
+typedef struct CUstream_st *hpa_stream_t;
+
+/* ---- return codes (host) ---- */
+#define HPA_OK 0
+#define HPA_ERR_INVALID (-1)     /* NULL pointer or out-of-range size; nothing launched */
+#define HPA_ERR_UNSUPPORTED (-2) /* a shape these kernels do not implement */
+#define HPA_ERR_WORKSPACE (-3)   /* task map buffer smaller than required */
+#define HPA_ERR_ALIGN (-4)       /* a pointer lacks the alignment stated below */
+#define HPA_ERR_CUDA (-5)        /* a CUDA runtime call or launch failed */
+
+/* ---- status bits written by the kernels into task map word 6 ---- */
+#define HPA_STATUS_BAD_SEQLEN 1 /* some L_r < 1 (plan) or L_r < q_len (attention) */
+#define HPA_STATUS_MISMATCH 2   /* map built for another B / num_ctas / tile */
+#define HPA_STATUS_BAD_PAGE 4   /* a page id outside [0, num_pages); page 0 was read instead */
+#define HPA_STATUS_TIMEOUT 8    /* a shared-memory pipeline wait exceeded ~2 s; CTA gave up */
+#define HPA_STATUS_OVERFLOW 16  /* total tile count does not fit int32 */
+
+/* ---- KV element types ---- */
+#define HPA_KV_BF16 0 /* bfloat16 */
+#define HPA_KV_E4M3 1 /* OCP FP8 E4M3 code; value = code * scale[kv head] */
+
+/*
+ * Task map: an opaque int32 blob in device memory, written by hpa_plan or
+ * hpa_plan_static and read by hpa_decode_attn and hpa_combine.  One map
+ * serves every layer of a decode step ([HPC-Ops §二.1]).  Layout (int32 words):
+ *   [0,16)  header: T, base, rem, C, B, S (segments), status, tile, kind
+ *           (0 dynamic / 1 static), splits, S_cap, 0...
+ *   lens[B]            copy of the sequence lengths
+ *   cu_tiles[B+1]      exclusive running sum of tiles per request
+ *   cta_begin[C+1]     first stream tile of each partition
+ *   cta_seg[C+1]       first segment of each partition
+ *   seg_off[B+1]       first segment of each request
+ *   (padding to a multiple of 4 words)
+ *   seg[S_cap][4]      {request, tile_lo, tile_hi, partition}; tiles are
+ *                      request-local, [tile_lo, tile_hi); unused rows are -1.
+ * A segment is the part of one request that one partition owns.
+ */
+
+/* Bytes of the dynamic task map for B requests over num_ctas partitions
+ * (segment capacity B + num_ctas - 1).  0 if an argument is out of range. */
+size_t hpa_taskmap_bytes(int32_t B, int32_t num_ctas);
+
+/* Segment capacity of the dynamic map: B + num_ctas - 1 (0 if out of range).
+ * partial_o needs capacity * q_len * Hq * d floats, partial_lse capacity *
+ * q_len * Hq floats. */
+int32_t hpa_max_segments(int32_t B, int32_t num_ctas);
+
+/* Static comparator: num_ctas = B * splits partitions, capacity B * splits. */
+int32_t hpa_static_num_ctas(int32_t B, int32_t splits);
+size_t hpa_static_taskmap_bytes(int32_t B, int32_t splits);
+
+/* Partitions per KV head that fill the current device once: SMs x resident
+ * attention CTAs per SM / Hkv (at least 1).  Returns <= 0 on a CUDA error or
+ * an unsupported (q_len, kv_dtype). */
+int32_t hpa_default_num_ctas(int32_t Hkv, int32_t q_len, int32_t kv_dtype);
+
+/*
+ * hpa_plan -- the Task Assign step ([Notes §3.1] steps 1-4, [HPC-Ops §二.1],
+ * [Stack §二.1]).  One device kernel:
+ *   n_r = ceil(L_r / tile); cu_tiles = exclusive scan of n_r; T = cu_tiles[B];
+ *   base = T / C, rem = T % C; partition c owns stream tiles
+ *   [c*base + min(c, rem), (c+1)*base + min(c+1, rem)); its range is split at
+ *   request boundaries into segments.
+ * seq_lens_dev: int32[B] device, L_r >= 1.  tile: a positive multiple of 64
+ * (the page size).  num_ctas >= 1 (more partitions than tiles leaves the
+ * surplus empty).  taskmap_dev: >= hpa_taskmap_bytes(B, num_ctas) bytes,
+ * 16-byte aligned.
+ */
+int hpa_plan(const int32_t *seq_lens_dev, int32_t B, int32_t tile, int32_t num_ctas,
+             void *taskmap_dev, size_t taskmap_bytes, hpa_stream_t stream);
+
+/*
+ * hpa_plan_static -- the static split-KV comparator the pages contrast the
+ * method with ([Notes §3.1] 问题): request r is cut into min(splits, n_r)
+ * contiguous chunks of near-equal tile counts (the first n_r % chunks get
+ * one more); partition r * splits + s owns chunk s, or nothing.  Same map
+ * format, so the same attention and combine kernels run it.
+ * taskmap_dev: >= hpa_static_taskmap_bytes(B, splits) bytes.
+ */
+int hpa_plan_static(const int32_t *seq_lens_dev, int32_t B, int32_t tile, int32_t splits,
+                    void *taskmap_dev, size_t taskmap_bytes, hpa_stream_t stream);
+
+/*
+ * hpa_decode_attn -- the split-KV attention kernel ([Notes §3.1] steps 4-5).
+ * Grid num_ctas x Hkv; the CTA of (partition c, KV head h) walks c's
+ * segments in order and, for each, computes over the segment's keys
+ *   s = sm_scale * q . k,  m = max s,  l = sum exp(s - m),  o = sum exp(s - m) v / l
+ * for the G = Hq / Hkv query heads of h and every query token j (token j
+ * of the q_len new ones sees keys [0, L_r - q_len + 1 + j)), and writes
+ *   partial_o[seg][j][head][d] = o,  partial_lse[seg][j][head] = m + ln l
+ * (natural log; -inf and o = 0 for a row that sees no key of the segment).
+ *
+ * q_dev:        bf16 [B][q_len][Hq][d], 4-byte aligned.
+ * k_pool_dev, v_pool_dev: [num_pages][Hkv][page_size][d] of bf16 or E4M3
+ *               bytes, 16-byte aligned (read with TMA tensor copies).
+ * k_scale_dev, v_scale_dev: fp32 [Hkv] for HPA_KV_E4M3, ignored for bf16.
+ * page_indptr_dev: int32 [B+1]; page_indices_dev: int32; key i of request r
+ *               is slot i % page_size of page page_indices[page_indptr[r] + i / page_size].
+ * Supported: d == 128, page_size == 64, Hq % Hkv == 0, (Hq / Hkv) * q_len <= 16,
+ *               num_pages * Hkv < 2^31.
+ * taskmap_dev:  a map from hpa_plan / hpa_plan_static for these B and num_ctas.
+ * partial_o_dev: fp32, >= (B + num_ctas - 1) * q_len * Hq * d, 16-byte aligned (one
+ *               row per segment; no map has more than B + num_ctas - 1 segments);
+ * partial_lse_dev: fp32, >= (B + num_ctas - 1) * q_len * Hq.
+ */
+int hpa_decode_attn(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
+                    int32_t kv_dtype, const float *k_scale_dev, const float *v_scale_dev,
+                    int64_t num_pages, const int32_t *page_indptr_dev,
+                    const int32_t *page_indices_dev, int32_t page_size, int32_t B,
+                    int32_t q_len, int32_t Hq, int32_t Hkv, int32_t d, float sm_scale,
+                    void *taskmap_dev, int32_t num_ctas, float *partial_o_dev,
+                    float *partial_lse_dev, hpa_stream_t stream);
+
+/*
+ * hpa_combine -- the Combine kernel ([Notes §3.1] step 5, [HPC-Ops §二.1]).
+ * For every (request r, token j, head g) over r's segments s:
+ *   M = max_s lse_s,  w_s = exp(lse_s - M),
+ *   out = sum_s w_s o_s / sum_s w_s  (rounded to bf16),  out_lse = M + ln sum_s w_s.
+ * out_dev: bf16 [B][q_len][Hq][d], 8-byte aligned; out_lse_dev: fp32
+ * [B][q_len][Hq] or NULL.  d == 128.
+ */
+int hpa_combine(const float *partial_o_dev, const float *partial_lse_dev, void *taskmap_dev,
+                int32_t B, int32_t num_ctas, int32_t q_len, int32_t Hq, int32_t d,
+                void *out_dev, float *out_lse_dev, hpa_stream_t stream);
+
+/* Static description of a return code. */
+const char *hpa_error_string(int code);
+
+/* The last CUDA error the library saw on this thread (cudaError_t value), 0 if none. */
+int hpa_last_cuda_error(void);
+
+#ifdef __cplusplus
+}
+#endif
+#endif /* HPA_H */

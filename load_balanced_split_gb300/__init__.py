@@ -1,0 +1,9 @@
+"""Load-balanced split-KV GQA decode attention for GB300 (sm_103a).
+
+The compute path is the C-ABI library libhpa (include/hpa.h, sources in
+csrc/); `hpa` is its ctypes binding.  Nothing here computes on the CPU.
+"""
+from .hpa import (KV_BF16, KV_E4M3, HpaError, Workspace, decode_step, hpa_combine,  # noqa: F401
+                  hpa_decode_attn, hpa_default_num_ctas, hpa_max_segments, hpa_plan,
+                  hpa_plan_static, hpa_static_num_ctas, hpa_static_taskmap_bytes,
+                  hpa_taskmap_bytes, lib)

@@ -1,0 +1,563 @@
+// Split-KV GQA decode attention over a paged KV cache, driven by a task map.
+//
+// "Hy3 Preview AI Infra 推理优化精读笔记", §3.1 方案 steps 4-5: every attention CTA
+// takes the tiles the task map gives it and writes split-KV partial results
+// for a later combine.  Here one CTA is (partition c, KV head h): it walks the
+// segments of partition c and, per segment, reduces the segment's keys for
+// the G query heads of h and every new query token (rows = G * q_len <= 16).
+//
+// GB300 design:
+//  * one warp of TMA producer + four consumer warps, 2 CTAs per SM;
+//  * a page of one KV head (64 tokens x 128 dims; 16 KB bf16 / 8 KB E4M3 for K
+//    and again for V) is one pipeline stage, fetched with 3-D tiled TMA copies
+//    in 128-byte-swizzled form so the consumers' shared-memory reads are free
+//    of bank conflicts; completion is tracked with mbarriers;
+//  * each consumer warp owns 16 of the page's 64 keys: S = Q K^T and O += P V
+//    run as m16n8k16 tensor-core MMAs with the query rows as M (16 rows: the
+//    8 heads of the group x up to 2 tokens), keys as N / K;
+//  * FP32 online softmax in base 2 (scores pre-multiplied by sm_scale*log2 e),
+//    per-warp running (m, l, O) merged across the 4 warps at each segment end;
+//  * E4M3 pages are widened to f16 in registers (exact), with a consistent
+//    permutation of the head dimension between Q and K and of the output
+//    columns for V, so every shared-memory read is a 16-byte vector load;
+//  * every wait is bounded in time; a CTA that gives up flags the task map's
+//    status word, waits for its own copies in flight and returns.
+#include <math_constants.h>
+
+#include "hpa_internal.cuh"
+
+namespace hpa {
+namespace {
+
+constexpr int kConsumerWarps = 4;
+constexpr int kThreads = (kConsumerWarps + 1) * 32;
+constexpr uint32_t kFull = 0xffffffffu;
+
+template <int KV>
+struct Cfg;
+template <>
+struct Cfg<HPA_KV_BF16> {
+  static constexpr int kKBytes = 16384;  // one page-head of K: 64 x 128 bf16
+  static constexpr int kStages = 3;
+};
+template <>
+struct Cfg<HPA_KV_E4M3> {
+  static constexpr int kKBytes = 8192;  // 64 x 128 bytes
+  static constexpr int kStages = 6;
+};
+
+template <int KV>
+struct Smem {
+  static constexpr int kStageBytes = 2 * Cfg<KV>::kKBytes;
+  static constexpr int kStages = Cfg<KV>::kStages;
+  static constexpr int kMerge = kStages * kStageBytes;     // float[16][128]
+  static constexpr int kStats = kMerge + MAX_ROWS * HEAD_DIM * 4;  // m[4][16], l[4][16]
+  static constexpr int kBars = kStats + 2 * kConsumerWarps * MAX_ROWS * 4;
+  static constexpr int kFlag = kBars + 2 * kStages * 8;
+  static constexpr int kBytes = kFlag + 16;
+  static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 B
+};
+
+struct SegInfo {
+  int r, L, klo, khi, pg0, pg1;
+};
+
+__device__ __forceinline__ SegInfo seg_info(const AttnParams &p, int s, int tile) {
+  const int4 sg = reinterpret_cast<const int4 *>(p.tm + p.lay.segs)[s];
+  SegInfo f;
+  f.r = sg.x;
+  f.L = p.tm[p.lay.lens + sg.x];
+  f.klo = sg.y * tile;
+  f.khi = min(sg.z * tile, f.L);
+  f.pg0 = f.klo / PAGE;
+  f.pg1 = (f.khi + PAGE - 1) / PAGE;
+  return f;
+}
+
+// ----------------------------------------------------------------------------- producer
+template <int KV>
+__device__ void producer(const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv,
+                         uint8_t *smem, int s_begin, int s_end, int tile, int h) {
+  using S = Smem<KV>;
+  const int lane = threadIdx.x & 31;
+  const uint32_t base = smem_u32(smem);
+  const uint32_t full0 = base + S::kBars, empty0 = full0 + 8 * S::kStages;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kFlag);
+  uint64_t pol = 0;
+  if (lane == 0) {
+    pol = l2_policy_evict_first();
+    prefetch_tmap(tmk);
+    prefetch_tmap(tmv);
+  }
+  int stage = 0;
+  uint32_t phase = 0, issued = 0, parity_bits = 0;
+  bool ok = true;
+  for (int s = s_begin; s < s_end && ok; ++s) {
+    const SegInfo f = seg_info(p, s, tile);
+    const int pstart = p.page_indptr[f.r];
+    const int pcount = p.page_indptr[f.r + 1] - pstart;  // pages listed for request r
+    const int32_t *pidx = p.page_indices + pstart;
+    for (int pb = f.pg0; pb < f.pg1 && ok; pb += 32) {
+      const int cnt = min(32, f.pg1 - pb);
+      int id = 0;
+      if (lane < cnt) {
+        id = pb + lane < pcount ? pidx[pb + lane] : -1;
+        if (id < 0 || id >= p.num_pages) {  // bad id or too short a page list
+          status_or(p.tm, HPA_STATUS_BAD_PAGE);
+          id = 0;
+        }
+      }
+      for (int i = 0; i < cnt; ++i) {
+        const int pid = __shfl_sync(kFull, id, i);
+        int good = 1;
+        if (lane == 0) {
+          if (*abort_flag || !mbar_wait_bounded(empty0 + 8 * stage, phase ^ 1)) {
+            good = 0;
+          } else {
+            const uint32_t fb = full0 + 8 * stage;
+            const uint32_t dst = base + stage * S::kStageBytes;
+            const int z = pid * p.Hkv + h;
+            mbar_arrive_expect_tx(fb, S::kStageBytes);
+            if (KV == HPA_KV_BF16) {
+              tma_load_3d(dst, tmk, fb, 0, 0, z, pol);
+              tma_load_3d(dst + 8192, tmk, fb, 64, 0, z, pol);
+              tma_load_3d(dst + 16384, tmv, fb, 0, 0, z, pol);
+              tma_load_3d(dst + 24576, tmv, fb, 64, 0, z, pol);
+            } else {
+              tma_load_3d(dst, tmk, fb, 0, 0, z, pol);
+              tma_load_3d(dst + 8192, tmv, fb, 0, 0, z, pol);
+            }
+            issued |= 1u << stage;
+            parity_bits = (parity_bits & ~(1u << stage)) | (phase << stage);
+          }
+        }
+        ok = __shfl_sync(kFull, good, 0) != 0;
+        if (!ok) break;
+        if (++stage == S::kStages) {
+          stage = 0;
+          phase ^= 1;
+        }
+      }
+    }
+  }
+  if (!ok && lane == 0) {
+    status_or(p.tm, HPA_STATUS_TIMEOUT);
+    *abort_flag = 1;
+    // never leave the CTA with copies still landing in its shared memory
+    for (int st = 0; st < S::kStages; ++st)
+      if (issued & (1u << st))
+        mbar_wait_bounded(full0 + 8 * st, (parity_bits >> st) & 1u, 1000000000ull);
+  }
+}
+
+// ----------------------------------------------------------------------------- consumer helpers
+// Zero the V rows (keys >= L) this warp reads from a page that ends past L.
+template <int KV>
+__device__ __forceinline__ void zero_tail_rows(uint8_t *vtile, int w, int wk, int L, int lane) {
+  const int4 z = make_int4(0, 0, 0, 0);
+  if (KV == HPA_KV_BF16) {
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int id = lane + 32 * i, rr = id >> 4, hf = (id >> 3) & 1, ch = id & 7;
+      if (wk + rr >= L)
+        *reinterpret_cast<int4 *>(vtile + hf * 8192 + (16 * w + rr) * 128 + ch * 16) = z;
+    }
+  } else {
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int id = lane + 32 * i, rr = id >> 3, ch = id & 7;
+      if (wk + rr >= L) *reinterpret_cast<int4 *>(vtile + (16 * w + rr) * 128 + ch * 16) = z;
+    }
+  }
+}
+
+// S[16 rows x 16 keys] = Q K^T for the warp's keys of the page in `kt`.
+template <int KV>
+__device__ __forceinline__ void qk(float (&s)[2][4], const uint32_t (&qa)[8][4], uint32_t kt,
+                                   int w, int lane) {
+#pragma unroll
+  for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+    for (int e = 0; e < 4; ++e) s[nt][e] = 0.f;
+  if (KV == HPA_KV_BF16) {
+    const int mi = lane >> 3, key = 16 * w + (mi >> 1) * 8 + (lane & 7);
+    const uint32_t row = kt + key * 128;
+#pragma unroll
+    for (int ks = 0; ks < 8; ++ks) {
+      const int chunk = (ks & 3) * 2 + (mi & 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4(row + (ks >> 2) * 8192 + ((chunk ^ (lane & 7)) << 4), b0, b1, b2, b3);
+      mma_bf16(s[0], qa[ks], b0, b1);
+      mma_bf16(s[1], qa[ks], b2, b3);
+    }
+  } else {
+    const int r8 = lane >> 2, qd = lane & 3;
+#pragma unroll
+    for (int nt = 0; nt < 2; ++nt) {
+      const uint32_t row = kt + (16 * w + 8 * nt + r8) * 128;
+      uint32_t u[8];
+      lds128(row + (((2 * qd) ^ r8) << 4), u[0], u[1], u[2], u[3]);
+      lds128(row + (((2 * qd + 1) ^ r8) << 4), u[4], u[5], u[6], u[7]);
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        const uint32_t b0 = e4m3x2_to_f16x2(static_cast<uint16_t>(u[ks] & 0xffffu));
+        const uint32_t b1 = e4m3x2_to_f16x2(static_cast<uint16_t>(u[ks] >> 16));
+        mma_f16(s[nt], qa[ks], b0, b1);
+      }
+    }
+  }
+}
+
+// O[16 rows x 128] += P[16 x 16 keys] V for the warp's keys of the page in `vt`.
+template <int KV>
+__device__ __forceinline__ void pv(float (&o)[16][4], const uint32_t (&pa)[4], uint32_t vt,
+                                   int w, int lane) {
+  if (KV == HPA_KV_BF16) {
+    const int mi = lane >> 3, key = 16 * w + (mi & 1) * 8 + (lane & 7);
+    const uint32_t row = vt + key * 128;
+#pragma unroll
+    for (int np = 0; np < 8; ++np) {
+      const int chunk = (np & 3) * 2 + (mi >> 1);
+      uint32_t b0, b1, b2, b3;
+      ldsm_x4_t(row + (np >> 2) * 8192 + ((chunk ^ (lane & 7)) << 4), b0, b1, b2, b3);
+      mma_bf16(o[2 * np], pa, b0, b1);
+      mma_bf16(o[2 * np + 1], pa, b2, b3);
+    }
+  } else {
+    // thread (r8 = c, qd) reads dims [16c, 16c+16) of keys 2qd, 2qd+1, 2qd+8, 2qd+9;
+    // output column n of n-tile i is head dim 16 n + i.
+    const int c = lane >> 2, qd = lane & 3;
+    uint32_t R[4][4];
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const int key = 16 * w + 2 * qd + (k & 1) + (k >> 1) * 8;
+      lds128(vt + key * 128 + ((c ^ (key & 7)) << 4), R[k][0], R[k][1], R[k][2], R[k][3]);
+    }
+#pragma unroll
+    for (int wd = 0; wd < 4; ++wd) {
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {  // byte pairs (0,1) and (2,3) of the word
+        // bytes [k0.b, k1.b, k0.b+1, k1.b+1] for b = 2*hb
+        const uint32_t sel = hb ? 0x7362u : 0x5140u;
+        const uint32_t lo01 = __byte_perm(R[0][wd], R[1][wd], sel);
+        const uint32_t lo23 = __byte_perm(R[2][wd], R[3][wd], sel);
+        const int i = 4 * wd + 2 * hb;
+        mma_f16(o[i], pa, e4m3x2_to_f16x2(static_cast<uint16_t>(lo01 & 0xffffu)),
+                e4m3x2_to_f16x2(static_cast<uint16_t>(lo23 & 0xffffu)));
+        mma_f16(o[i + 1], pa, e4m3x2_to_f16x2(static_cast<uint16_t>(lo01 >> 16)),
+                e4m3x2_to_f16x2(static_cast<uint16_t>(lo23 >> 16)));
+      }
+    }
+  }
+}
+
+// Head-dim index of accumulator o[i][e] (row pair aside) for this lane.
+template <int KV>
+__device__ __forceinline__ int out_dim(int i, int e, int lane) {
+  const int qd = lane & 3;
+  if (KV == HPA_KV_BF16) return 8 * i + 2 * qd + e;
+  return 16 * (2 * qd + e) + i;
+}
+
+// ----------------------------------------------------------------------------- consumer
+template <int KV>
+__device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_end, int tile,
+                         int h) {
+  using S = Smem<KV>;
+  const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r8 = lane >> 2, qd = lane & 3;
+  const uint32_t base = smem_u32(smem);
+  const uint32_t full0 = base + S::kBars, empty0 = full0 + 8 * S::kStages;
+  float *mbuf = reinterpret_cast<float *>(smem + S::kMerge);
+  float *sm_m = reinterpret_cast<float *>(smem + S::kStats);
+  float *sm_l = sm_m + kConsumerWarps * MAX_ROWS;
+  volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kFlag);
+
+  float sl2 = p.scale_log2, vsc = 1.f;
+  if (KV == HPA_KV_E4M3) {
+    sl2 *= p.k_scale[h];
+    vsc = p.v_scale[h];
+  }
+  const int G = p.G, rows = p.rows, q_len = p.q_len;
+  const int row0 = r8, row1 = r8 + 8;
+  const bool v0 = row0 < rows, v1 = row1 < rows;
+  const int j0 = row0 / G, g0 = row0 % G, j1 = row1 / G, g1 = row1 % G;
+
+  int stage = 0;
+  uint32_t phase = 0;
+  for (int s = s_begin; s < s_end; ++s) {
+    const SegInfo f = seg_info(p, s, tile);
+    if (f.L < q_len && w == 0 && lane == 0) status_or(p.tm, HPA_STATUS_BAD_SEQLEN);
+    const int lim_min = f.L - q_len + 1;  // first key hidden from some row
+    const int lim0 = v0 ? f.L - q_len + 1 + j0 : f.L;
+    const int lim1 = v1 ? f.L - q_len + 1 + j1 : f.L;
+
+    // query fragments (A operand, 16 rows x 128)
+    uint32_t qa[8][4];
+    {
+      const __nv_bfloat16 *q0 =
+          p.q + ((static_cast<int64_t>(f.r) * q_len + j0) * p.Hq + h * G + g0) * HEAD_DIM;
+      const __nv_bfloat16 *q1 =
+          p.q + ((static_cast<int64_t>(f.r) * q_len + j1) * p.Hq + h * G + g1) * HEAD_DIM;
+#pragma unroll
+      for (int ks = 0; ks < 8; ++ks) {
+        if (KV == HPA_KV_BF16) {
+          const int d0 = 16 * ks + 2 * qd;
+          qa[ks][0] = v0 ? *reinterpret_cast<const uint32_t *>(q0 + d0) : 0u;
+          qa[ks][1] = v1 ? *reinterpret_cast<const uint32_t *>(q1 + d0) : 0u;
+          qa[ks][2] = v0 ? *reinterpret_cast<const uint32_t *>(q0 + d0 + 8) : 0u;
+          qa[ks][3] = v1 ? *reinterpret_cast<const uint32_t *>(q1 + d0 + 8) : 0u;
+        } else {
+          const int d0 = 32 * qd + 4 * ks;
+          auto h2 = [](const __nv_bfloat16 *x) {
+            const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(x));
+            return pack_f16(t.x, t.y);
+          };
+          qa[ks][0] = v0 ? h2(q0 + d0) : 0u;
+          qa[ks][1] = v1 ? h2(q1 + d0) : 0u;
+          qa[ks][2] = v0 ? h2(q0 + d0 + 2) : 0u;
+          qa[ks][3] = v1 ? h2(q1 + d0 + 2) : 0u;
+        }
+      }
+    }
+
+    float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
+    float o[16][4];
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+#pragma unroll
+      for (int e = 0; e < 4; ++e) o[i][e] = 0.f;
+
+    bool ok = true;
+    for (int pg = f.pg0; pg < f.pg1; ++pg) {
+      const bool got = !(*abort_flag) && mbar_wait_bounded(full0 + 8 * stage, phase);
+      if (!__all_sync(kFull, got)) {
+        ok = false;  // the rest of this CTA's work is abandoned (see below)
+        break;
+      }
+      uint8_t *kt = smem + stage * S::kStageBytes;
+      uint8_t *vt = kt + Cfg<KV>::kKBytes;
+      const int key0 = pg * PAGE, wk = key0 + 16 * w;
+      const bool tail = wk + 16 > f.L;
+      if (tail) {
+        zero_tail_rows<KV>(vt, w, wk, f.L, lane);
+        __syncwarp();
+      }
+
+      float sc[2][4];
+      qk<KV>(sc, qa, smem_u32(kt), w, lane);
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+        for (int e = 0; e < 4; ++e) sc[nt][e] *= sl2;
+      if (wk + 16 > lim_min) {
+#pragma unroll
+        for (int nt = 0; nt < 2; ++nt)
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const int key = wk + 8 * nt + 2 * qd + (e & 1);
+            if (key >= (e < 2 ? lim0 : lim1)) sc[nt][e] = -CUDART_INF_F;
+          }
+      }
+      // online softmax, rows row0 (e = 0,1) and row1 (e = 2,3)
+      float mx0 = fmaxf(fmaxf(sc[0][0], sc[0][1]), fmaxf(sc[1][0], sc[1][1]));
+      float mx1 = fmaxf(fmaxf(sc[0][2], sc[0][3]), fmaxf(sc[1][2], sc[1][3]));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 1));
+      mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 2));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 1));
+      mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 2));
+      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      const float b0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
+      const float b1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
+      const float a0 = exp2f(m0 - b0), a1 = exp2f(m1 - b1);
+      m0 = mn0;
+      m1 = mn1;
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        sc[nt][0] = exp2f(sc[nt][0] - b0);
+        sc[nt][1] = exp2f(sc[nt][1] - b0);
+        sc[nt][2] = exp2f(sc[nt][2] - b1);
+        sc[nt][3] = exp2f(sc[nt][3] - b1);
+      }
+      l0 = l0 * a0 + (sc[0][0] + sc[0][1] + sc[1][0] + sc[1][1]);
+      l1 = l1 * a1 + (sc[0][2] + sc[0][3] + sc[1][2] + sc[1][3]);
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        o[i][0] *= a0;
+        o[i][1] *= a0;
+        o[i][2] *= a1;
+        o[i][3] *= a1;
+      }
+      uint32_t pa[4];
+      if (KV == HPA_KV_BF16) {
+        pa[0] = pack_bf16(sc[0][0], sc[0][1]);
+        pa[1] = pack_bf16(sc[0][2], sc[0][3]);
+        pa[2] = pack_bf16(sc[1][0], sc[1][1]);
+        pa[3] = pack_bf16(sc[1][2], sc[1][3]);
+      } else {
+        pa[0] = pack_f16(sc[0][0], sc[0][1]);
+        pa[1] = pack_f16(sc[0][2], sc[0][3]);
+        pa[2] = pack_f16(sc[1][0], sc[1][1]);
+        pa[3] = pack_f16(sc[1][2], sc[1][3]);
+      }
+      pv<KV>(o, pa, smem_u32(vt), w, lane);
+      __syncwarp();
+      if (tail) fence_proxy_async_smem();  // generic writes before the next TMA fill
+      if (lane == 0) mbar_arrive(empty0 + 8 * stage);
+      if (++stage == S::kStages) {
+        stage = 0;
+        phase ^= 1;
+      }
+    }
+    // A timed-out warp flags the map and raises the CTA's abort flag; it still
+    // takes part in the epilogue's named barriers below so that no other
+    // consumer warp waits on it.  Later waits see the flag and fail at once.
+    if (!ok && lane == 0) {
+      status_or(p.tm, HPA_STATUS_TIMEOUT);
+      *abort_flag = 1;
+    }
+
+    // ---- segment end: merge the four warps' (m, l, O) and store the partial
+    l0 += __shfl_xor_sync(kFull, l0, 1);
+    l0 += __shfl_xor_sync(kFull, l0, 2);
+    l1 += __shfl_xor_sync(kFull, l1, 1);
+    l1 += __shfl_xor_sync(kFull, l1, 2);
+    if (qd == 0) {
+      sm_m[w * MAX_ROWS + row0] = m0;
+      sm_l[w * MAX_ROWS + row0] = l0;
+      sm_m[w * MAX_ROWS + row1] = m1;
+      sm_l[w * MAX_ROWS + row1] = l1;
+    }
+    named_barrier(1, kConsumerWarps * 32);
+    auto row_stats = [&](int row, float &M, float &Lsum) {
+      M = -CUDART_INF_F;
+#pragma unroll
+      for (int x = 0; x < kConsumerWarps; ++x) M = fmaxf(M, sm_m[x * MAX_ROWS + row]);
+      const float Mb = M == -CUDART_INF_F ? 0.f : M;
+      Lsum = 0.f;
+#pragma unroll
+      for (int x = 0; x < kConsumerWarps; ++x)
+        Lsum += sm_l[x * MAX_ROWS + row] * exp2f(sm_m[x * MAX_ROWS + row] - Mb);
+      M = Mb;
+    };
+    float M0, L0, M1, L1;
+    row_stats(row0, M0, L0);
+    row_stats(row1, M1, L1);
+    const float f0 = L0 > 0.f ? exp2f(m0 - M0) / L0 * vsc : 0.f;
+    const float f1 = L1 > 0.f ? exp2f(m1 - M1) / L1 * vsc : 0.f;
+#pragma unroll
+    for (int i = 0; i < 16; ++i)
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const int dd = out_dim<KV>(i, e, lane);
+        if (v0) atomicAdd(&mbuf[row0 * HEAD_DIM + dd], o[i][e] * f0);
+        if (v1) atomicAdd(&mbuf[row1 * HEAD_DIM + dd], o[i][2 + e] * f1);
+      }
+    named_barrier(1, kConsumerWarps * 32);
+    const int tid = threadIdx.x;
+    float4 *mb4 = reinterpret_cast<float4 *>(mbuf);
+    for (int v = tid; v < rows * (HEAD_DIM / 4); v += kConsumerWarps * 32) {
+      const int row = v / (HEAD_DIM / 4), c4 = v % (HEAD_DIM / 4);
+      const int j = row / G, g = row % G;
+      const int64_t dst = ((static_cast<int64_t>(s) * q_len + j) * p.Hq + h * G + g) * HEAD_DIM;
+      reinterpret_cast<float4 *>(p.partial_o + dst)[c4] = mb4[v];
+      mb4[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+    }
+    if (tid < rows) {
+      float M, Lsum;
+      row_stats(tid, M, Lsum);
+      const int j = tid / G, g = tid % G;
+      p.partial_lse[(static_cast<int64_t>(s) * q_len + j) * p.Hq + h * G + g] =
+          Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -CUDART_INF_F;
+    }
+    named_barrier(1, kConsumerWarps * 32);
+  }
+}
+
+// ----------------------------------------------------------------------------- kernel
+template <int KV>
+__global__ void __launch_bounds__(kThreads, 2)
+    decode_attn_kernel(const __grid_constant__ CUtensorMap tmk,
+                       const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
+  using S = Smem<KV>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int c = blockIdx.x, h = blockIdx.y;
+  __shared__ int hdr[4];  // go, tile, s_begin, s_end -- read once, used by all threads
+  const uint32_t base = smem_u32(smem);
+  if (threadIdx.x == 0) {
+    const int32_t *tm = p.tm;
+    const int tile = tm[TM_TILE];
+    int go = tm[TM_STATUS] == 0;
+    if (go && (tm[TM_B] != p.B || tm[TM_C] != p.C || tile <= 0 || tile % PAGE != 0)) {
+      if (c == 0 && h == 0) status_or(p.tm, HPA_STATUS_MISMATCH);
+      go = 0;
+    }
+    hdr[1] = tile;
+    hdr[2] = go ? tm[p.lay.cta_seg + c] : 0;
+    hdr[3] = go ? tm[p.lay.cta_seg + c + 1] : 0;
+    hdr[0] = go && hdr[2] < hdr[3];
+    for (int st = 0; st < S::kStages; ++st) {
+      mbar_init(base + S::kBars + 8 * st, 1);
+      mbar_init(base + S::kBars + 8 * (S::kStages + st), kConsumerWarps);
+    }
+    *reinterpret_cast<int *>(smem + S::kFlag) = 0;
+    fence_barrier_init();
+  }
+  float4 *mb4 = reinterpret_cast<float4 *>(smem + S::kMerge);
+  for (int v = threadIdx.x; v < MAX_ROWS * HEAD_DIM / 4; v += kThreads)
+    mb4[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+  __syncthreads();
+  if (!hdr[0]) return;  // bad map, or a partition with no tiles
+  const int tile = hdr[1], s_begin = hdr[2], s_end = hdr[3];
+
+  if (threadIdx.x >= kConsumerWarps * 32)
+    producer<KV>(p, &tmk, &tmv, smem, s_begin, s_end, tile, h);
+  else
+    consumer<KV>(p, smem, s_begin, s_end, tile, h);
+}
+
+template <int KV>
+cudaError_t launch(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                   cudaStream_t s) {
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(decode_attn_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                             Smem<KV>::kAlloc);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  dim3 grid(p.C, p.Hkv);
+  decode_attn_kernel<KV><<<grid, kThreads, Smem<KV>::kAlloc, s>>>(tmk, tmv, p);
+  return cudaGetLastError();
+}
+
+template <int KV>
+int occupancy(int *ctas) {
+  cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<KV>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Smem<KV>::kAlloc);
+  if (e != cudaSuccess) return -1;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, decode_attn_kernel<KV>, kThreads,
+                                                    Smem<KV>::kAlloc);
+  return e == cudaSuccess ? 0 : -1;
+}
+
+}  // namespace
+
+cudaError_t launch_decode_attn(const AttnParams &p, const CUtensorMap &tmk,
+                               const CUtensorMap &tmv, int kv_dtype, cudaStream_t s) {
+  return kv_dtype == HPA_KV_BF16 ? launch<HPA_KV_BF16>(p, tmk, tmv, s)
+                                 : launch<HPA_KV_E4M3>(p, tmk, tmv, s);
+}
+
+int attn_ctas_per_sm(int kv_dtype, int q_len, int *ctas) {
+  (void)q_len;
+  return kv_dtype == HPA_KV_BF16 ? occupancy<HPA_KV_BF16>(ctas) : occupancy<HPA_KV_E4M3>(ctas);
+}
+
+}  // namespace hpa

@@ -1,0 +1,251 @@
+// C ABI of libhpa: argument checks, task map sizing, TMA descriptor set-up
+// and kernel launches.  See include/hpa.h for the contract of every call.
+#include <cudaTypedefs.h>
+
+#include <climits>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "hpa_internal.cuh"
+
+namespace {
+
+thread_local int g_last_cuda_error = 0;
+
+int cuda_fail(cudaError_t e) {
+  g_last_cuda_error = static_cast<int>(e);
+  return HPA_ERR_CUDA;
+}
+
+bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+constexpr int32_t kMaxB = 1 << 24;
+constexpr int32_t kMaxC = 1 << 20;
+
+int64_t taskmap_words(int64_t B, int64_t C, int64_t s_cap) {
+  return hpa::TaskMapLayout::make(B, C).words(s_cap);
+}
+
+// ---- TMA descriptors for a KV pool: 3-D view (d, token-in-page, page*Hkv + head)
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void *p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+struct MapKey {
+  const void *ptr;
+  int64_t rows;
+  int kv_dtype;
+  bool operator==(const MapKey &o) const {
+    return ptr == o.ptr && rows == o.rows && kv_dtype == o.kv_dtype;
+  }
+};
+
+std::mutex g_map_mu;
+constexpr int kMapCache = 8;
+MapKey g_map_keys[kMapCache];
+CUtensorMap g_maps[kMapCache];
+int g_map_next = 0, g_map_used = 0;
+
+int pool_map(const void *pool, int64_t num_pages, int Hkv, int kv_dtype, CUtensorMap *out) {
+  const int64_t zdim = num_pages * Hkv;
+  const MapKey key{pool, zdim, kv_dtype};
+  {
+    std::lock_guard<std::mutex> lk(g_map_mu);
+    for (int i = 0; i < g_map_used; ++i)
+      if (g_map_keys[i] == key) {
+        *out = g_maps[i];
+        return HPA_OK;
+      }
+  }
+  auto fn = encode_fn();
+  if (!fn) return cuda_fail(cudaErrorNotSupported);
+  const int es = kv_dtype == HPA_KV_BF16 ? 2 : 1;
+  const cuuint64_t dims[3] = {static_cast<cuuint64_t>(hpa::HEAD_DIM),
+                              static_cast<cuuint64_t>(hpa::PAGE), static_cast<cuuint64_t>(zdim)};
+  const cuuint64_t strides[2] = {static_cast<cuuint64_t>(hpa::HEAD_DIM * es),
+                                 static_cast<cuuint64_t>(hpa::HEAD_DIM * es * hpa::PAGE)};
+  const cuuint32_t box[3] = {static_cast<cuuint32_t>(128 / es), static_cast<cuuint32_t>(hpa::PAGE),
+                             1u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  CUtensorMap m;
+  CUresult r = fn(&m,
+                  kv_dtype == HPA_KV_BF16 ? CU_TENSOR_MAP_DATA_TYPE_BFLOAT16
+                                          : CU_TENSOR_MAP_DATA_TYPE_UINT8,
+                  3, const_cast<void *>(pool), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  if (r != CUDA_SUCCESS) return HPA_ERR_INVALID;
+  std::lock_guard<std::mutex> lk(g_map_mu);
+  g_map_keys[g_map_next] = key;
+  g_maps[g_map_next] = m;
+  g_map_next = (g_map_next + 1) % kMapCache;
+  if (g_map_used < kMapCache) ++g_map_used;
+  *out = m;
+  return HPA_OK;
+}
+
+int check_plan_args(const int32_t *seq_lens, int32_t B, int32_t tile, int64_t C,
+                    const void *tm, size_t bytes, int64_t s_cap) {
+  if (!seq_lens || !tm) return HPA_ERR_INVALID;
+  if (B < 1 || B > kMaxB || C < 1 || C > kMaxC) return HPA_ERR_INVALID;
+  if (tile < hpa::PAGE || tile % hpa::PAGE != 0) return HPA_ERR_INVALID;
+  if (!aligned(tm, 16)) return HPA_ERR_ALIGN;
+  if (bytes < static_cast<size_t>(taskmap_words(B, C, s_cap)) * 4) return HPA_ERR_WORKSPACE;
+  return HPA_OK;
+}
+
+}  // namespace
+
+extern "C" {
+
+size_t hpa_taskmap_bytes(int32_t B, int32_t num_ctas) {
+  if (B < 1 || B > kMaxB || num_ctas < 1 || num_ctas > kMaxC) return 0;
+  return static_cast<size_t>(taskmap_words(B, num_ctas, int64_t(B) + num_ctas - 1)) * 4;
+}
+
+int32_t hpa_max_segments(int32_t B, int32_t num_ctas) {
+  if (B < 1 || B > kMaxB || num_ctas < 1 || num_ctas > kMaxC) return 0;
+  return B + num_ctas - 1;
+}
+
+int32_t hpa_static_num_ctas(int32_t B, int32_t splits) {
+  if (B < 1 || B > kMaxB || splits < 1 || int64_t(B) * splits > kMaxC) return 0;
+  return B * splits;
+}
+
+size_t hpa_static_taskmap_bytes(int32_t B, int32_t splits) {
+  const int32_t C = hpa_static_num_ctas(B, splits);
+  if (C == 0) return 0;
+  return static_cast<size_t>(taskmap_words(B, C, C)) * 4;
+}
+
+int32_t hpa_default_num_ctas(int32_t Hkv, int32_t q_len, int32_t kv_dtype) {
+  if (Hkv < 1 || q_len < 1 || (kv_dtype != HPA_KV_BF16 && kv_dtype != HPA_KV_E4M3)) return -1;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    g_last_cuda_error = static_cast<int>(e);
+    return -1;
+  }
+  if (hpa::attn_ctas_per_sm(kv_dtype, q_len, &per_sm) != 0 || per_sm < 1) return -1;
+  const int c = sms * per_sm / Hkv;
+  return c < 1 ? 1 : c;
+}
+
+int hpa_plan(const int32_t *seq_lens_dev, int32_t B, int32_t tile, int32_t num_ctas,
+             void *taskmap_dev, size_t taskmap_bytes, hpa_stream_t stream) {
+  const int64_t s_cap = int64_t(B) + num_ctas - 1;
+  int rc = check_plan_args(seq_lens_dev, B, tile, num_ctas, taskmap_dev, taskmap_bytes, s_cap);
+  if (rc != HPA_OK) return rc;
+  cudaError_t e = hpa::launch_plan(seq_lens_dev, B, tile, num_ctas, 0, 0,
+                                   static_cast<int32_t *>(taskmap_dev), s_cap,
+                                   reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? HPA_OK : cuda_fail(e);
+}
+
+int hpa_plan_static(const int32_t *seq_lens_dev, int32_t B, int32_t tile, int32_t splits,
+                    void *taskmap_dev, size_t taskmap_bytes, hpa_stream_t stream) {
+  const int32_t C = hpa_static_num_ctas(B, splits);
+  if (C == 0) return HPA_ERR_INVALID;
+  int rc = check_plan_args(seq_lens_dev, B, tile, C, taskmap_dev, taskmap_bytes, C);
+  if (rc != HPA_OK) return rc;
+  cudaError_t e = hpa::launch_plan(seq_lens_dev, B, tile, C, 1, splits,
+                                   static_cast<int32_t *>(taskmap_dev), C,
+                                   reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? HPA_OK : cuda_fail(e);
+}
+
+int hpa_decode_attn(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
+                    int32_t kv_dtype, const float *k_scale_dev, const float *v_scale_dev,
+                    int64_t num_pages, const int32_t *page_indptr_dev,
+                    const int32_t *page_indices_dev, int32_t page_size, int32_t B,
+                    int32_t q_len, int32_t Hq, int32_t Hkv, int32_t d, float sm_scale,
+                    void *taskmap_dev, int32_t num_ctas, float *partial_o_dev,
+                    float *partial_lse_dev, hpa_stream_t stream) {
+  if (!q_dev || !k_pool_dev || !v_pool_dev || !page_indptr_dev || !page_indices_dev ||
+      !taskmap_dev || !partial_o_dev || !partial_lse_dev)
+    return HPA_ERR_INVALID;
+  if (kv_dtype != HPA_KV_BF16 && kv_dtype != HPA_KV_E4M3) return HPA_ERR_INVALID;
+  if (kv_dtype == HPA_KV_E4M3 && (!k_scale_dev || !v_scale_dev)) return HPA_ERR_INVALID;
+  if (B < 1 || B > kMaxB || num_ctas < 1 || num_ctas > kMaxC || q_len < 1 || Hq < 1 ||
+      Hkv < 1 || Hkv > 65535 || num_pages < 1 || !std::isfinite(sm_scale))
+    return HPA_ERR_INVALID;
+  if (d != hpa::HEAD_DIM || page_size != hpa::PAGE || Hq % Hkv != 0 ||
+      (Hq / Hkv) * q_len > hpa::MAX_ROWS)
+    return HPA_ERR_UNSUPPORTED;
+  if (num_pages * Hkv > INT_MAX) return HPA_ERR_UNSUPPORTED;
+  if (!aligned(q_dev, 4) || !aligned(k_pool_dev, 16) || !aligned(v_pool_dev, 16) ||
+      !aligned(taskmap_dev, 16) || !aligned(partial_o_dev, 16) || !aligned(partial_lse_dev, 4))
+    return HPA_ERR_ALIGN;
+  CUtensorMap tmk, tmv;
+  int rc = pool_map(k_pool_dev, num_pages, Hkv, kv_dtype, &tmk);
+  if (rc == HPA_OK) rc = pool_map(v_pool_dev, num_pages, Hkv, kv_dtype, &tmv);
+  if (rc != HPA_OK) return rc;
+  hpa::AttnParams p;
+  p.q = static_cast<const __nv_bfloat16 *>(q_dev);
+  p.tm = static_cast<int32_t *>(taskmap_dev);
+  p.page_indptr = page_indptr_dev;
+  p.page_indices = page_indices_dev;
+  p.k_scale = k_scale_dev;
+  p.v_scale = v_scale_dev;
+  p.partial_o = partial_o_dev;
+  p.partial_lse = partial_lse_dev;
+  p.num_pages = num_pages;
+  p.lay = hpa::TaskMapLayout::make(B, num_ctas);
+  p.B = B;
+  p.C = num_ctas;
+  p.q_len = q_len;
+  p.Hq = Hq;
+  p.Hkv = Hkv;
+  p.G = Hq / Hkv;
+  p.rows = p.G * q_len;
+  p.scale_log2 = sm_scale * 1.4426950408889634f;
+  cudaError_t e = hpa::launch_decode_attn(p, tmk, tmv, kv_dtype,
+                                          reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? HPA_OK : cuda_fail(e);
+}
+
+int hpa_combine(const float *partial_o_dev, const float *partial_lse_dev, void *taskmap_dev,
+                int32_t B, int32_t num_ctas, int32_t q_len, int32_t Hq, int32_t d,
+                void *out_dev, float *out_lse_dev, hpa_stream_t stream) {
+  if (!partial_o_dev || !partial_lse_dev || !taskmap_dev || !out_dev) return HPA_ERR_INVALID;
+  if (B < 1 || B > kMaxB || num_ctas < 1 || num_ctas > kMaxC || q_len < 1 || Hq < 1)
+    return HPA_ERR_INVALID;
+  if (d != hpa::HEAD_DIM) return HPA_ERR_UNSUPPORTED;
+  if (int64_t(B) * q_len * Hq > (int64_t(1) << 34)) return HPA_ERR_UNSUPPORTED;
+  if (!aligned(partial_o_dev, 16) || !aligned(out_dev, 8) || !aligned(taskmap_dev, 16))
+    return HPA_ERR_ALIGN;
+  cudaError_t e = hpa::launch_combine(partial_o_dev, partial_lse_dev,
+                                      static_cast<int32_t *>(taskmap_dev), B, num_ctas, q_len,
+                                      Hq, static_cast<__nv_bfloat16 *>(out_dev), out_lse_dev,
+                                      reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? HPA_OK : cuda_fail(e);
+}
+
+const char *hpa_error_string(int code) {
+  switch (code) {
+    case HPA_OK: return "ok";
+    case HPA_ERR_INVALID: return "invalid argument";
+    case HPA_ERR_UNSUPPORTED: return "unsupported shape";
+    case HPA_ERR_WORKSPACE: return "task map buffer too small";
+    case HPA_ERR_ALIGN: return "misaligned pointer";
+    case HPA_ERR_CUDA: return "CUDA runtime error";
+    default: return "unknown error";
+  }
+}
+
+int hpa_last_cuda_error(void) { return g_last_cuda_error; }
+
+}  // extern "C"

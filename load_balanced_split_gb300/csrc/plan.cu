@@ -1,0 +1,194 @@
+// Task Assign: builds the split-KV task map on the device with one CTA.
+//
+// Dynamic map ("Hy3 Preview AI Infra 推理优化精读笔记", §3.1 方案 steps 1-4;
+// "大模型推理性能优化新范式：Hy3架构下的全栈优化技术拆解", §二.1 budget rule):
+//   n_r = ceil(L_r / tile), cu_tiles = exclusive scan of n_r, T = cu_tiles[B],
+//   base = T / C, rem = T % C, partition c owns stream tiles
+//   [c*base + min(c, rem), (c+1)*base + min(c+1, rem)) -- a greedy fill of
+//   equal budgets along the request-major tile stream -- and its range is
+//   cut at request boundaries into segments.
+// Static map (the fixed split-KV the same §3.1 contrasts it with): request r
+//   is cut into min(splits, n_r) near-equal chunks, partition r*splits+s owns
+//   chunk s.
+#include <climits>
+
+#include "hpa_internal.cuh"
+
+namespace hpa {
+namespace {
+
+constexpr int kPlanThreads = 1024;
+
+// Inclusive scan over the block; `total` receives the block-wide sum.
+__device__ long long block_scan(long long v, long long *wbuf, long long &total) {
+  const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
+  for (int o = 1; o < 32; o <<= 1) {
+    long long n = __shfl_up_sync(0xffffffffu, v, o);
+    if (lane >= o) v += n;
+  }
+  if (lane == 31) wbuf[wid] = v;
+  __syncthreads();
+  if (wid == 0) {
+    long long w = (lane < kPlanThreads / 32) ? wbuf[lane] : 0;
+    for (int o = 1; o < 32; o <<= 1) {
+      long long n = __shfl_up_sync(0xffffffffu, w, o);
+      if (lane >= o) w += n;
+    }
+    wbuf[lane] = w;
+  }
+  __syncthreads();
+  if (wid > 0) v += wbuf[wid - 1];
+  total = wbuf[kPlanThreads / 32 - 1];
+  __syncthreads();
+  return v;
+}
+
+// First index i in [0, n) with a[i] > x (n if none).
+__device__ int upper_bound(const int32_t *a, int n, long long x) {
+  int lo = 0, hi = n;
+  while (lo < hi) {
+    int mid = (lo + hi) >> 1;
+    if (a[mid] > x) hi = mid;
+    else lo = mid + 1;
+  }
+  return lo;
+}
+
+__global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__restrict__ lens_in,
+                                                            int B, int tile, int C, int kind,
+                                                            int splits, int32_t *tm,
+                                                            long long s_cap) {
+  const TaskMapLayout lay = TaskMapLayout::make(B, C);
+  int32_t *lens = tm + lay.lens, *cu = tm + lay.cu_tiles, *cb = tm + lay.cta_begin;
+  int32_t *cs = tm + lay.cta_seg, *so = tm + lay.seg_off;
+  int4 *seg = reinterpret_cast<int4 *>(tm + lay.segs);
+  __shared__ long long wbuf[kPlanThreads / 32];
+  __shared__ int s_bad;
+  const int tid = threadIdx.x;
+  if (tid == 0) s_bad = 0;
+  __syncthreads();
+
+  // a1 + a2: tile counts and their running sum
+  long long carry = 0, total;
+  for (int base = 0; base < B; base += kPlanThreads) {
+    const int i = base + tid;
+    long long n = 0;
+    if (i < B) {
+      const int L = lens_in[i];
+      lens[i] = L;
+      if (L < 1) atomicOr(&s_bad, HPA_STATUS_BAD_SEQLEN);
+      else n = (L - 1) / tile + 1;
+    }
+    const long long incl = block_scan(n, wbuf, total);
+    if (i < B) cu[i + 1] = static_cast<int32_t>(carry + incl);
+    carry += total;
+  }
+  if (tid == 0) cu[0] = 0;
+  if (carry > INT_MAX && tid == 0) atomicOr(&s_bad, HPA_STATUS_OVERFLOW);
+  __syncthreads();
+  const long long T = carry;
+  const int bad = s_bad;
+  if (bad) {
+    if (tid == 0) {
+      for (int w = 0; w < TM_HEADER_WORDS; ++w) tm[w] = 0;
+      tm[TM_C] = C;
+      tm[TM_B] = B;
+      tm[TM_TILE] = tile;
+      tm[TM_KIND] = kind;
+      tm[TM_SPLITS] = splits;
+      tm[TM_SCAP] = static_cast<int32_t>(s_cap);
+      tm[TM_STATUS] = bad;
+    }
+    return;
+  }
+
+  // a3: partition ranges over the stream
+  const long long tbase = T / C, trem = T % C;
+  for (int c = tid; c < C; c += kPlanThreads) {
+    long long begin;
+    if (kind == 0) {
+      begin = c * tbase + (c < trem ? c : trem);
+    } else {
+      const int r = c / splits, s = c % splits;
+      const int n = cu[r + 1] - cu[r];
+      const int k = n < splits ? n : splits;
+      if (s < k) {
+        const int b = n / k, rm = n % k;
+        begin = cu[r] + s * b + (s < rm ? s : rm);
+      } else {
+        begin = cu[r + 1];
+      }
+    }
+    cb[c] = static_cast<int32_t>(begin);
+  }
+  if (tid == 0) cb[C] = static_cast<int32_t>(T);
+  __syncthreads();
+
+  // a4: segments per partition, their running sum, then the segment rows
+  carry = 0;
+  for (int base = 0; base < C; base += kPlanThreads) {
+    const int c = base + tid;
+    long long cnt = 0;
+    if (c < C) {
+      const int b = cb[c], e = cb[c + 1];
+      if (e > b) {
+        const int rf = upper_bound(cu, B + 1, b) - 1;
+        const int rl = upper_bound(cu, B + 1, e - 1) - 1;
+        cnt = rl - rf + 1;
+      }
+    }
+    const long long incl = block_scan(cnt, wbuf, total);
+    if (c < C) cs[c] = static_cast<int32_t>(carry + incl - cnt);
+    carry += total;
+  }
+  const long long S = carry;
+  if (tid == 0) cs[C] = static_cast<int32_t>(S);
+  if (S > s_cap) {  // cannot happen for maps sized by the library's own queries
+    if (tid == 0) tm[TM_STATUS] = HPA_STATUS_OVERFLOW;
+    return;
+  }
+  __syncthreads();
+  for (int c = tid; c < C; c += kPlanThreads) {
+    const int b = cb[c], e = cb[c + 1];
+    if (e <= b) continue;
+    const int rf = upper_bound(cu, B + 1, b) - 1;
+    const int rl = upper_bound(cu, B + 1, e - 1) - 1;
+    int out = cs[c];
+    for (int r = rf; r <= rl; ++r, ++out) {
+      const int lo = (b > cu[r] ? b : cu[r]) - cu[r];
+      const int hi = (e < cu[r + 1] ? e : cu[r + 1]) - cu[r];
+      seg[out] = make_int4(r, lo, hi, c);
+    }
+  }
+  for (long long s = S + tid; s < s_cap; s += kPlanThreads) seg[s] = make_int4(-1, -1, -1, -1);
+  __syncthreads();
+  for (long long s = tid; s < S; s += kPlanThreads) {
+    const int r = seg[s].x;
+    if (s == 0 || seg[s - 1].x != r) so[r] = static_cast<int32_t>(s);
+  }
+  if (tid == 0) {
+    so[B] = static_cast<int32_t>(S);
+    for (int w = TM_SCAP + 1; w < TM_HEADER_WORDS; ++w) tm[w] = 0;
+    tm[TM_T] = static_cast<int32_t>(T);
+    tm[TM_BASE] = kind == 0 ? static_cast<int32_t>(tbase) : -1;
+    tm[TM_REM] = kind == 0 ? static_cast<int32_t>(trem) : -1;
+    tm[TM_C] = C;
+    tm[TM_B] = B;
+    tm[TM_S] = static_cast<int32_t>(S);
+    tm[TM_STATUS] = 0;
+    tm[TM_TILE] = tile;
+    tm[TM_KIND] = kind;
+    tm[TM_SPLITS] = splits;
+    tm[TM_SCAP] = static_cast<int32_t>(s_cap);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_plan(const int32_t *seq_lens, int B, int tile, int C, int kind, int splits,
+                        int32_t *tm, int64_t s_cap, cudaStream_t s) {
+  plan_kernel<<<1, kPlanThreads, 0, s>>>(seq_lens, B, tile, C, kind, splits, tm, s_cap);
+  return cudaGetLastError();
+}
+
+}  // namespace hpa

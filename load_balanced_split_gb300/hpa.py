@@ -1,0 +1,230 @@
+"""Python binding of libhpa (ctypes): the C entry points under the same names.
+
+Argument marshalling only -- every step of the path runs in the library's
+CUDA kernels.  Tensors are torch CUDA tensors; shapes are taken from them and
+checked by the library, which returns an error code (raised here as
+HpaError) before launching anything on bad input.  There is no CPU path: if
+the shared library is missing or cannot be loaded, every call raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import math
+import os
+import threading
+
+import torch
+
+from . import build as _build
+
+KV_BF16, KV_E4M3 = 0, 1
+STATUS_BITS = {1: "BAD_SEQLEN", 2: "MISMATCH", 4: "BAD_PAGE", 8: "TIMEOUT", 16: "OVERFLOW"}
+HEADER_WORDS = 16
+
+_lock = threading.Lock()
+_lib = None
+
+
+class HpaError(RuntimeError):
+    pass
+
+
+def lib():
+    """Load libhpa.so (building it first if it is missing or older than its sources)."""
+    global _lib
+    with _lock:
+        if _lib is None:
+            path = _build.LIB
+            if _build._stale():
+                try:
+                    path = _build.build()
+                except Exception as e:  # no nvcc, or a compile error: fail loudly
+                    raise HpaError("libhpa.so is not built and cannot be built: %s" % e)
+            L = ctypes.CDLL(path)
+            P, I32, I64, SZ, F = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64,
+                                  ctypes.c_size_t, ctypes.c_float)
+            sig = {
+                "hpa_taskmap_bytes": ([I32, I32], SZ),
+                "hpa_max_segments": ([I32, I32], I32),
+                "hpa_static_num_ctas": ([I32, I32], I32),
+                "hpa_static_taskmap_bytes": ([I32, I32], SZ),
+                "hpa_default_num_ctas": ([I32, I32, I32], I32),
+                "hpa_plan": ([P, I32, I32, I32, P, SZ, P], ctypes.c_int),
+                "hpa_plan_static": ([P, I32, I32, I32, P, SZ, P], ctypes.c_int),
+                "hpa_decode_attn": ([P, P, P, I32, P, P, I64, P, P, I32, I32, I32, I32, I32,
+                                     I32, F, P, I32, P, P, P], ctypes.c_int),
+                "hpa_combine": ([P, P, P, I32, I32, I32, I32, I32, P, P, P], ctypes.c_int),
+                "hpa_error_string": ([ctypes.c_int], ctypes.c_char_p),
+                "hpa_last_cuda_error": ([], ctypes.c_int),
+            }
+            for name, (args, res) in sig.items():
+                fn = getattr(L, name)
+                fn.argtypes = args
+                fn.restype = res
+            _lib = L
+    return _lib
+
+
+def _check(rc: int, what: str):
+    if rc != 0:
+        L = lib()
+        msg = L.hpa_error_string(rc).decode()
+        if rc == -5:
+            msg += " (cudaError %d)" % L.hpa_last_cuda_error()
+        raise HpaError("%s failed: %s (%d)" % (what, msg, rc))
+
+
+def _stream(stream):
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream if hasattr(stream, "cuda_stream") else stream)
+
+
+def _ptr(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _dev(t, name, dtype=None):
+    if not (isinstance(t, torch.Tensor) and t.is_cuda and t.is_contiguous()):
+        raise HpaError("%s must be a contiguous CUDA tensor" % name)
+    if dtype is not None and t.dtype != dtype:
+        raise HpaError("%s must be %s, got %s" % (name, dtype, t.dtype))
+    return t
+
+
+# ----------------------------------------------------------------------------- sizes
+def hpa_taskmap_bytes(B: int, num_ctas: int) -> int:
+    return int(lib().hpa_taskmap_bytes(B, num_ctas))
+
+
+def hpa_max_segments(B: int, num_ctas: int) -> int:
+    return int(lib().hpa_max_segments(B, num_ctas))
+
+
+def hpa_static_num_ctas(B: int, splits: int) -> int:
+    return int(lib().hpa_static_num_ctas(B, splits))
+
+
+def hpa_static_taskmap_bytes(B: int, splits: int) -> int:
+    return int(lib().hpa_static_taskmap_bytes(B, splits))
+
+
+def hpa_default_num_ctas(Hkv: int, q_len: int, kv_dtype: int) -> int:
+    c = int(lib().hpa_default_num_ctas(Hkv, q_len, kv_dtype))
+    if c <= 0:
+        raise HpaError("hpa_default_num_ctas failed (cudaError %d)" % lib().hpa_last_cuda_error())
+    return c
+
+
+# ----------------------------------------------------------------------------- the three calls
+def hpa_plan(seq_lens, tile: int, num_ctas: int, taskmap, stream=None):
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(taskmap, "taskmap")
+    _check(lib().hpa_plan(_ptr(seq_lens), seq_lens.numel(), tile, num_ctas, _ptr(taskmap),
+                          taskmap.numel() * taskmap.element_size(), _stream(stream)), "hpa_plan")
+
+
+def hpa_plan_static(seq_lens, tile: int, splits: int, taskmap, stream=None):
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(taskmap, "taskmap")
+    _check(lib().hpa_plan_static(_ptr(seq_lens), seq_lens.numel(), tile, splits, _ptr(taskmap),
+                                 taskmap.numel() * taskmap.element_size(), _stream(stream)),
+           "hpa_plan_static")
+
+
+def hpa_decode_attn(q, k_pool, v_pool, page_indptr, page_indices, taskmap, num_ctas: int,
+                    partial_o, partial_lse, k_scale=None, v_scale=None,
+                    sm_scale: float | None = None, stream=None):
+    """q bf16 [B][q_len][Hq][d]; k/v pools bf16 or uint8 (E4M3) [P][Hkv][page][d]."""
+    _dev(q, "q", torch.bfloat16)
+    _dev(k_pool, "k_pool")
+    _dev(v_pool, "v_pool")
+    if k_pool.dtype == torch.bfloat16:
+        kv = KV_BF16
+    elif k_pool.dtype in (torch.uint8, torch.float8_e4m3fn):
+        kv = KV_E4M3
+        _dev(k_scale, "k_scale", torch.float32)
+        _dev(v_scale, "v_scale", torch.float32)
+    else:
+        raise HpaError("unsupported KV dtype %s" % k_pool.dtype)
+    if v_pool.dtype != k_pool.dtype or v_pool.shape != k_pool.shape:
+        raise HpaError("k_pool and v_pool must match")
+    for t, n in ((page_indptr, "page_indptr"), (page_indices, "page_indices")):
+        _dev(t, n, torch.int32)
+    _dev(taskmap, "taskmap")
+    _dev(partial_o, "partial_o", torch.float32)
+    _dev(partial_lse, "partial_lse", torch.float32)
+    B, q_len, Hq, d = q.shape
+    P, Hkv, page, d2 = k_pool.shape
+    if d2 != d:
+        raise HpaError("head dim mismatch")
+    need = hpa_max_segments(B, num_ctas) * q_len * Hq
+    if partial_lse.numel() < need or partial_o.numel() < need * d:
+        raise HpaError("partial buffers too small: need (B + num_ctas - 1) segments")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d)
+    _check(lib().hpa_decode_attn(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), kv, _ptr(k_scale), _ptr(v_scale), P,
+        _ptr(page_indptr), _ptr(page_indices), page, B, q_len, Hq, Hkv, d, float(sm_scale),
+        _ptr(taskmap), num_ctas, _ptr(partial_o), _ptr(partial_lse), _stream(stream)),
+        "hpa_decode_attn")
+
+
+def hpa_combine(partial_o, partial_lse, taskmap, num_ctas: int, out, out_lse=None, stream=None):
+    """out bf16 [B][q_len][Hq][d]; out_lse fp32 [B][q_len][Hq] or None."""
+    _dev(partial_o, "partial_o", torch.float32)
+    _dev(partial_lse, "partial_lse", torch.float32)
+    _dev(taskmap, "taskmap")
+    _dev(out, "out", torch.bfloat16)
+    if out_lse is not None:
+        _dev(out_lse, "out_lse", torch.float32)
+    B, q_len, Hq, d = out.shape
+    _check(lib().hpa_combine(_ptr(partial_o), _ptr(partial_lse), _ptr(taskmap), B, num_ctas,
+                             q_len, Hq, d, _ptr(out), _ptr(out_lse), _stream(stream)),
+           "hpa_combine")
+
+
+# ----------------------------------------------------------------------------- workspace helper
+class Workspace:
+    """Device buffers for one decode step: task map and split partials.
+
+    Sized once for (B, num_ctas, q_len, Hq, d) -- dynamic map by default, or
+    the static comparator with `splits`.  Allocation is done with torch; the
+    library itself never allocates.
+    """
+
+    def __init__(self, B, q_len, Hq, d, num_ctas=None, splits=None, device="cuda"):
+        if splits is not None:
+            self.num_ctas = hpa_static_num_ctas(B, splits)
+            nbytes = hpa_static_taskmap_bytes(B, splits)
+        else:
+            self.num_ctas = num_ctas
+            nbytes = hpa_taskmap_bytes(B, num_ctas)
+        cap = hpa_max_segments(B, self.num_ctas)   # partial rows, valid for either map
+        if nbytes == 0 or cap == 0:
+            raise HpaError("workspace size query failed")
+        self.splits = splits
+        self.capacity = cap
+        self.taskmap = torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device=device)
+        self.partial_o = torch.empty(cap * q_len * Hq * d, dtype=torch.float32, device=device)
+        self.partial_lse = torch.empty(cap * q_len * Hq, dtype=torch.float32, device=device)
+
+    def plan(self, seq_lens, tile=512, stream=None):
+        if self.splits is not None:
+            hpa_plan_static(seq_lens, tile, self.splits, self.taskmap, stream)
+        else:
+            hpa_plan(seq_lens, tile, self.num_ctas, self.taskmap, stream)
+
+    def status(self) -> int:
+        """Status word of the map (synchronises the current stream)."""
+        return int(self.taskmap[6].item())
+
+
+def decode_step(ws: Workspace, q, k_pool, v_pool, seq_lens, page_indptr, page_indices, out,
+                out_lse=None, k_scale=None, v_scale=None, tile=512, plan=True, stream=None):
+    """plan (optional) -> split-KV attention -> combine, all enqueued on one stream."""
+    if plan:
+        ws.plan(seq_lens, tile, stream)
+    hpa_decode_attn(q, k_pool, v_pool, page_indptr, page_indices, ws.taskmap, ws.num_ctas,
+                    ws.partial_o, ws.partial_lse, k_scale, v_scale, stream=stream)
+    hpa_combine(ws.partial_o, ws.partial_lse, ws.taskmap, ws.num_ctas, out, out_lse, stream)

@@ -1,0 +1,155 @@
+"""Split-KV attention and combine on the GPU against the fp64 oracle.
+
+Every case checks (i) the task map bit-exactly, (ii) every segment's partial
+(o, lse) against the oracle's attention over that segment's keys, and (iii)
+the combined output and lse against the oracle's unsplit attention."""
+import math
+
+import numpy as np
+import pytest
+import torch
+
+import load_balanced_split_gb300 as hpa
+import oracle
+import workloads as W
+from gpu_helpers import (DeviceBatch, assert_close, assert_lse_close, expect_taskmap_equal,
+                         run_gpu)
+
+pytestmark = pytest.mark.gpu
+
+
+def check(b, num_ctas=None, splits=None, tile=512, db=None, check_partials=True):
+    g = run_gpu(b, num_ctas=num_ctas, splits=splits, tile=tile, db=db)
+    if splits is None:
+        ref_plan = oracle.plan(b.seq_lens, tile, g["num_ctas"])
+    else:
+        ref_plan = oracle.plan_static(b.seq_lens, tile, splits)
+    expect_taskmap_equal(g["tm"], ref_plan, g["capacity"])
+    if check_partials:
+        po, pl = oracle.split_attention(b, ref_plan)
+        assert_close(g["po"], po, b.kv_dtype, "partial_o")
+        assert_lse_close(g["pl"], pl, "partial_lse")
+    out, lse = oracle.attention(b)
+    err = assert_close(g["out"], out, b.kv_dtype, "out")
+    assert_lse_close(g["lse"], lse, "out_lse")
+    return g, err
+
+
+def test_worked_example():
+    b = W.make_config(1)
+    g, _ = check(b)
+    assert list(np.diff(g["tm"]["cta_begin"])) == [4, 4, 4, 4]
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+@pytest.mark.parametrize("q_len", [1, 2])
+@pytest.mark.parametrize("C", [1, 5, 23])
+def test_ragged_batch(kv, q_len, C):
+    lens = [2, 63, 64, 65, 511, 512, 513, 1000, 3333, 4096 + 17]
+    b = W.make_batch(lens, q_len=q_len, kv_dtype=kv, seed=11 + C)
+    check(b, num_ctas=C)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_more_partitions_than_tiles(kv):
+    b = W.make_batch([100, 700, 30], kv_dtype=kv, seed=2)
+    check(b, num_ctas=40)
+
+
+@pytest.mark.parametrize("L,q_len", [(1, 1), (2, 2), (64, 1), (65, 2), (512, 1), (513, 2)])
+def test_tiny_requests(L, q_len):
+    b = W.make_batch([L], q_len=q_len, seed=L)
+    check(b, num_ctas=3)
+
+
+@pytest.mark.parametrize("tile", [64, 128, 1024])
+def test_tile_sizes(tile):
+    b = W.make_batch([100, 2000, 9000, 64 * 7], q_len=2, seed=tile)
+    check(b, num_ctas=9, tile=tile)
+
+
+@pytest.mark.parametrize("splits", [1, 3, 16])
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_static_plan_same_kernels(splits, kv):
+    b = W.make_batch([100, 2000, 9000, 1], kv_dtype=kv, seed=splits)
+    check(b, splits=splits)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+@pytest.mark.parametrize("q_len", [1, 2])
+def test_poisoned_tail_slots_are_ignored(kv, q_len):
+    """Pool slots past each request's length hold NaN; they must not reach the output."""
+    lens = [70, 130, 1000, 5]
+    b = W.make_batch(lens, q_len=q_len, kv_dtype=kv, seed=5)
+    nan_code = 0x7FC0 if kv == "bf16" else 0x7F
+    for r, L in enumerate(lens):
+        last = b.page_indices[b.page_indptr[r + 1] - 1]
+        used = L - (len(range(b.page_indptr[r], b.page_indptr[r + 1])) - 1) * b.page_size
+        for pool in (b.k_pool, b.v_pool):
+            raw = pool.view(torch.int16) if kv == "bf16" else pool
+            raw[last, :, used:, :] = nan_code
+    check(b, num_ctas=6)
+
+
+def test_gqa_groups_of_four():
+    b = W.make_batch([300, 1500], q_len=4, Hq=16, Hkv=4, seed=3)   # 4 heads x 4 tokens = 16 rows
+    check(b, num_ctas=5)
+
+
+def test_map_reused_across_layers():
+    b = W.make_batch([3000, 40, 12000], seed=4)
+    db = DeviceBatch(b)
+    C = 7
+    ws = hpa.Workspace(b.B, 1, 64, 128, num_ctas=C)
+    ws.plan(db.lens)
+    outs = []
+    for layer in range(3):
+        out = torch.empty((b.B, 1, 64, 128), dtype=torch.bfloat16, device="cuda")
+        hpa.decode_step(ws, db.q, db.k, db.v, db.lens, db.indptr, db.indices, out, plan=False)
+        outs.append(out.float().cpu().numpy())
+    ref, _ = oracle.attention(b)
+    for o in outs:
+        assert_close(o, ref, "bf16")
+
+
+def test_bad_page_id_is_flagged():
+    b = W.make_batch([200, 300], seed=6)
+    b.page_indices = b.page_indices.copy()
+    b.page_indices[2] = b.num_pages + 5
+    db = DeviceBatch(b)
+    ws = hpa.Workspace(b.B, 1, 64, 128, num_ctas=4)
+    out = torch.empty((2, 1, 64, 128), dtype=torch.bfloat16, device="cuda")
+    hpa.decode_step(ws, db.q, db.k, db.v, db.lens, db.indptr, db.indices, out)
+    torch.cuda.synchronize()
+    assert ws.status() & 4
+    assert torch.isnan(out.float()).all()
+
+
+def test_mismatched_partition_count_is_flagged():
+    b = W.make_batch([200, 3000], seed=7)
+    db = DeviceBatch(b)
+    ws = hpa.Workspace(b.B, 1, 64, 128, num_ctas=4)
+    ws.plan(db.lens)
+    big = hpa.Workspace(b.B, 1, 64, 128, num_ctas=9)
+    out = torch.empty((2, 1, 64, 128), dtype=torch.bfloat16, device="cuda")
+    hpa.hpa_decode_attn(db.q, db.k, db.v, db.indptr, db.indices, ws.taskmap, 9, big.partial_o,
+                        big.partial_lse)
+    hpa.hpa_combine(big.partial_o, big.partial_lse, ws.taskmap, 9, out)
+    torch.cuda.synchronize()
+    assert ws.status() & 2
+    assert torch.isnan(out.float()).all()
+
+
+def test_sm_scale_argument():
+    b = W.make_batch([900], seed=8)
+    db = DeviceBatch(b)
+    ws = hpa.Workspace(1, 1, 64, 128, num_ctas=3)
+    ws.plan(db.lens)
+    out = torch.empty((1, 1, 64, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((1, 1, 64), dtype=torch.float32, device="cuda")
+    hpa.hpa_decode_attn(db.q, db.k, db.v, db.indptr, db.indices, ws.taskmap, 3, ws.partial_o,
+                        ws.partial_lse, sm_scale=0.05)
+    hpa.hpa_combine(ws.partial_o, ws.partial_lse, ws.taskmap, 3, out, lse)
+    ref, ref_lse = oracle.attention(b, sm_scale=0.05)
+    assert_close(out.float().cpu().numpy(), ref, "bf16")
+    assert_lse_close(lse.cpu().numpy(), ref_lse)
