@@ -110,6 +110,24 @@ class ClockSampler:
                 "reasons": sorted(reasons)}
 
 
+# ----------------------------------------------------------------------------- ranks
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """Max of a per-rank float over all ranks (identity for one rank)."""
+    if world <= 1:
+        return float(x)
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64,
+                     device=device if dist.get_backend() == "nccl" else "cpu")
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def per_batch_us(ms_per_step: float, world: int) -> float:
+    """Whole-job µs per batch: every rank processes one batch per step."""
+    return ms_per_step * 1e3 / world
+
+
 # ----------------------------------------------------------------------------- our arm
 def run_ours(args, rank, world, local_rank):
     import torch
@@ -178,12 +196,7 @@ def run_ours(args, rank, world, local_rank):
     if status != 0:
         raise RuntimeError("task map status %d after the timed steps" % status)
 
-    # max over ranks of the per-step time
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        ms = float(t.item())
+    ms = max_over_ranks(ms, world, dev)       # the slowest rank sets the step time
 
     # static split-KV comparators through the same kernels (heuristic and best of a sweep)
     comparator = None
@@ -231,12 +244,7 @@ def run_ours(args, rank, world, local_rank):
             for e in ev[1:]:
                 e.record(stream)
 
-    e2e_ms = timed(e2e_step, args.steps, args.warmup)[0]
-    if world > 1:
-        import torch.distributed as dist
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device=dev)
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(timed(e2e_step, args.steps, args.warmup)[0], world, dev)
 
     return dict(b=b, C=C, ms=ms, attn=attn, plan=plan_ms, comb=comb_ms, clocks=clocks,
                 comparator=comparator, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
@@ -338,7 +346,7 @@ def main():
     peak, peak_kind = peaks()
     attn_ms = statistics.mean(r["attn"])
     achieved = kv_bytes / (attn_ms * 1e-3) / 1e9
-    us_batch = r["ms"] * 1e3 / world
+    us_batch = per_batch_us(r["ms"], world)
     traffic = None
     if TRAFFIC_PROFILE["source_sha256"] == kernel_sha() and TRAFFIC_PROFILE["bytes_per_kv_byte"]:
         traffic = int(TRAFFIC_PROFILE["bytes_per_kv_byte"] * kv_bytes)
@@ -367,7 +375,7 @@ def main():
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "decode_attn_kernel", "peak_kind": peak_kind + " (hbm_gbs)"},
         "cpu_baseline": cpu,
-        "e2e": {"value": round(r["e2e_ms"] * 1e3 / world, 2), "unit": UNIT,
+        "e2e": {"value": round(per_batch_us(r["e2e_ms"], world), 2), "unit": UNIT,
                 "h2d_bytes_per_step": int(r["h2d"]), "d2h_bytes_per_step": int(r["d2h"])},
         "gpu_launches": 3 * args.steps,
         "clocks": r["clocks"],

@@ -173,6 +173,16 @@ int hpa_combine(const float *partial_o_dev, const float *partial_lse_dev, void *
                 int32_t B, int32_t num_ctas, int32_t q_len, int32_t Hq, int32_t d,
                 void *out_dev, float *out_lse_dev, hpa_stream_t stream);
 
+/*
+ * hpa_selftest_wait_timeout -- diagnostic for the failure path of the
+ * attention pipeline (no counterpart on the pages).  One thread waits on an
+ * mbarrier phase that nothing completes, using the same time-bounded wait
+ * as hpa_decode_attn, for limit_ns nanoseconds (1e3 .. 5e9); on expiry it ORs
+ * HPA_STATUS_TIMEOUT into status_dev[0] and returns, leaving the context
+ * usable.  status_dev: one int32 in device memory, 4-byte aligned.
+ */
+int hpa_selftest_wait_timeout(int32_t *status_dev, int64_t limit_ns, hpa_stream_t stream);
+
 /* Static description of a return code. */
 const char *hpa_error_string(int code);
 

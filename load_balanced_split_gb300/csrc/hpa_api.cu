@@ -234,6 +234,15 @@ int hpa_combine(const float *partial_o_dev, const float *partial_lse_dev, void *
   return e == cudaSuccess ? HPA_OK : cuda_fail(e);
 }
 
+int hpa_selftest_wait_timeout(int32_t *status_dev, int64_t limit_ns, hpa_stream_t stream) {
+  if (!status_dev) return HPA_ERR_INVALID;
+  if (limit_ns < 1000 || limit_ns > 5000000000ll) return HPA_ERR_INVALID;
+  if (!aligned(status_dev, 4)) return HPA_ERR_ALIGN;
+  cudaError_t e = hpa::launch_selftest_wait(status_dev, limit_ns,
+                                            reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? HPA_OK : cuda_fail(e);
+}
+
 const char *hpa_error_string(int code) {
   switch (code) {
     case HPA_OK: return "ok";

@@ -60,6 +60,7 @@ cudaError_t launch_combine(const float *po, const float *plse, int32_t *tm, int 
 cudaError_t launch_decode_attn(const AttnParams &p, const CUtensorMap &tmk,
                                const CUtensorMap &tmv, int kv_dtype, cudaStream_t s);
 int attn_ctas_per_sm(int kv_dtype, int q_len, int *ctas);  // occupancy query (host)
+cudaError_t launch_selftest_wait(int32_t *status, long long limit_ns, cudaStream_t s);
 
 // ----------------------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {

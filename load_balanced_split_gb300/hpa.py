@@ -54,6 +54,7 @@ def lib():
                 "hpa_decode_attn": ([P, P, P, I32, P, P, I64, P, P, I32, I32, I32, I32, I32,
                                      I32, F, P, I32, P, P, P], ctypes.c_int),
                 "hpa_combine": ([P, P, P, I32, I32, I32, I32, I32, P, P, P], ctypes.c_int),
+                "hpa_selftest_wait_timeout": ([P, I64, P], ctypes.c_int),
                 "hpa_error_string": ([ctypes.c_int], ctypes.c_char_p),
                 "hpa_last_cuda_error": ([], ctypes.c_int),
             }
@@ -182,6 +183,13 @@ def hpa_combine(partial_o, partial_lse, taskmap, num_ctas: int, out, out_lse=Non
     _check(lib().hpa_combine(_ptr(partial_o), _ptr(partial_lse), _ptr(taskmap), B, num_ctas,
                              q_len, Hq, d, _ptr(out), _ptr(out_lse), _stream(stream)),
            "hpa_combine")
+
+
+def hpa_selftest_wait_timeout(status, limit_ns: int, stream=None):
+    """Run the bounded-wait diagnostic; status: int32 CUDA tensor of >= 1 element."""
+    _dev(status, "status", torch.int32)
+    _check(lib().hpa_selftest_wait_timeout(_ptr(status), int(limit_ns), _stream(stream)),
+           "hpa_selftest_wait_timeout")
 
 
 # ----------------------------------------------------------------------------- workspace helper

@@ -113,3 +113,10 @@ def test_error_strings():
     L = hpa.lib()
     for c in (0, -1, -2, -3, -4, -5, 99):
         assert L.hpa_error_string(c)
+
+
+def test_selftest_argument_checks():
+    L = hpa.lib()
+    assert L.hpa_selftest_wait_timeout(None, 10**6, None) == -1
+    assert L.hpa_selftest_wait_timeout(FAKE, 10, None) == -1
+    assert L.hpa_selftest_wait_timeout(FAKE + 2, 10**6, None) == -4
