@@ -114,7 +114,7 @@ def assert_close(got, ref, kv, what="out"):
         i = np.unravel_index(np.argmax(d / np.maximum(floor, 1e-30)), d.shape)
         raise AssertionError("%s: %d of %d elements out of tolerance; worst at %s: got %r ref %r"
                              % (what, int(bad.sum()), bad.size, i, got[i], ref[i]))
-    return float(d.max()), float((d / floor).max())
+    return float(d.max()), float((d / np.maximum(floor, 1e-30)).max())
 
 
 def assert_lse_close(got, ref, what="lse"):
