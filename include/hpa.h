@@ -57,6 +57,7 @@ typedef struct CUstream_st *hpa_stream_t;
 #define HPA_ERR_WORKSPACE (-3)   /* task map buffer smaller than required */
 #define HPA_ERR_ALIGN (-4)       /* a pointer lacks the alignment stated below */
 #define HPA_ERR_CUDA (-5)        /* a CUDA runtime call or launch failed */
+#define HPA_ERR_NOALLOC_CAPACITY (-6) /* the problem needs more than the fixed no-alloc scratch */
 
 /* ---- status bits written by the kernels into task map word 6 ---- */
 #define HPA_STATUS_BAD_SEQLEN 1 /* some L_r < 1 (plan) or L_r < q_len (attention) */
@@ -182,6 +183,43 @@ int hpa_combine(const float *partial_o_dev, const float *partial_lse_dev, void *
  * usable.  status_dev: one int32 in device memory, 4-byte aligned.
  */
 int hpa_selftest_wait_timeout(int32_t *status_dev, int64_t limit_ns, hpa_stream_t stream);
+
+/*
+ * hpa_decode_attn_combine_noalloc -- hpa_decode_attn followed by hpa_combine,
+ * for callers that cannot allocate device memory; the pages have no
+ * counterpart to it.  Such callers include a plugin running inside another
+ * runtime that owns the whole device memory pool and hands out no
+ * workspace, and a serving loop that must not call cudaMalloc/cudaFree in the
+ * middle of a step (cudaFree synchronises the device; either can fail under
+ * memory pressure).  Instead of caller-provided partial_o / partial_lse, the
+ * split partials live in one fixed array inside the library's device image,
+ * HPA_NOALLOC_SCRATCH_BYTES (16 MiB) per GPU, held by every GPU that loads
+ * the library until the process exits.  The call itself allocates nothing.
+ *
+ * Arguments are those of hpa_decode_attn (minus the partial buffers) and of
+ * hpa_combine (out_dev, out_lse_dev), with the same layouts and checks.  The
+ * partials need (B + num_ctas - 1) * q_len * Hq * (d + 1) floats; a problem
+ * larger than the array returns HPA_ERR_NOALLOC_CAPACITY before any launch
+ * (e.g. 64 requests x 2 tokens x 64 heads with 38 partitions uses 6.7 MB).
+ *
+ * The first call on a device resolves the array's device address with that
+ * device current (cudaGetSymbolAddress, which may load the module); make that
+ * first call before any stream capture.  All calls share the one array and
+ * it keeps the last call's contents: nothing in it needs to start at zero
+ * (each call writes every partial it reads), but calls that overlap on the
+ * GPU -- on different streams, or from several host threads -- race on it
+ * and must be serialised by the caller.
+ */
+#define HPA_NOALLOC_SCRATCH_BYTES (16u << 20)
+int hpa_decode_attn_combine_noalloc(const void *q_dev, const void *k_pool_dev,
+                                    const void *v_pool_dev, int32_t kv_dtype,
+                                    const float *k_scale_dev, const float *v_scale_dev,
+                                    int64_t num_pages, const int32_t *page_indptr_dev,
+                                    const int32_t *page_indices_dev, int32_t page_size,
+                                    int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv,
+                                    int32_t d, float sm_scale, void *taskmap_dev,
+                                    int32_t num_ctas, void *out_dev, float *out_lse_dev,
+                                    hpa_stream_t stream);
 
 /* Static description of a return code. */
 const char *hpa_error_string(int code);

@@ -251,6 +251,7 @@ const char *hpa_error_string(int code) {
     case HPA_ERR_WORKSPACE: return "task map buffer too small";
     case HPA_ERR_ALIGN: return "misaligned pointer";
     case HPA_ERR_CUDA: return "CUDA runtime error";
+    case HPA_ERR_NOALLOC_CAPACITY: return "problem exceeds the fixed no-alloc scratch array";
     default: return "unknown error";
   }
 }

@@ -55,6 +55,9 @@ def lib():
                                      I32, F, P, I32, P, P, P], ctypes.c_int),
                 "hpa_combine": ([P, P, P, I32, I32, I32, I32, I32, P, P, P], ctypes.c_int),
                 "hpa_selftest_wait_timeout": ([P, I64, P], ctypes.c_int),
+                "hpa_decode_attn_combine_noalloc": ([P, P, P, I32, P, P, I64, P, P, I32, I32,
+                                                     I32, I32, I32, I32, F, P, I32, P, P, P],
+                                                    ctypes.c_int),
                 "hpa_error_string": ([ctypes.c_int], ctypes.c_char_p),
                 "hpa_last_cuda_error": ([], ctypes.c_int),
             }
@@ -190,6 +193,31 @@ def hpa_selftest_wait_timeout(status, limit_ns: int, stream=None):
     _dev(status, "status", torch.int32)
     _check(lib().hpa_selftest_wait_timeout(_ptr(status), int(limit_ns), _stream(stream)),
            "hpa_selftest_wait_timeout")
+
+
+def hpa_decode_attn_combine_noalloc(q, k_pool, v_pool, page_indptr, page_indices, taskmap,
+                                    num_ctas: int, out, out_lse=None, k_scale=None,
+                                    v_scale=None, sm_scale: float | None = None, stream=None):
+    """Attention + combine with the split partials in the library's fixed device array.
+
+    For callers that cannot allocate device memory during a decode step (a
+    plugin inside a runtime that owns the memory pool, a serving loop that
+    must not call cudaMalloc/cudaFree).  Calls that overlap on the GPU share
+    that array and race; serialise them.
+    """
+    for t, n in ((q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"), (page_indptr, "page_indptr"),
+                 (page_indices, "page_indices"), (taskmap, "taskmap"), (out, "out")):
+        _dev(t, n)
+    kv = KV_BF16 if k_pool.dtype == torch.bfloat16 else KV_E4M3
+    B, q_len, Hq, d = q.shape
+    P, Hkv, page, _ = k_pool.shape
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d)
+    _check(lib().hpa_decode_attn_combine_noalloc(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), kv, _ptr(k_scale), _ptr(v_scale), P,
+        _ptr(page_indptr), _ptr(page_indices), page, B, q_len, Hq, Hkv, d, float(sm_scale),
+        _ptr(taskmap), num_ctas, _ptr(out), _ptr(out_lse), _stream(stream)),
+        "hpa_decode_attn_combine_noalloc")
 
 
 # ----------------------------------------------------------------------------- workspace helper
