@@ -39,7 +39,13 @@ UNIT = "us/batch"
 
 # DRAM traffic of one decode_attn_kernel launch from an ncu capture, valid only
 # for the kernel source it was taken on (sha256 of decode_attn.cu); else null.
-TRAFFIC_PROFILE = {"source_sha256": None, "bytes_per_kv_byte": None, "workload": None}
+# Taken on the uniform 32 x 8192 batch (1.07 GB KV; the mixed batch is too large to capture
+# with every section) and scaled by KV bytes, since traffic grows with the KV read.
+TRAFFIC_PROFILE = {
+    "source_sha256": "d04dd3711dc952a1c39f72cc5b3298bb872a90a61fcb9ab0a8dcc42b204f3978",
+    "bytes_per_kv_byte": (1.074384e9 + 3.900160e6) / 1073741824,
+    "workload": "uniform_32x8k_paged (profiles/decode_attn_uniform_32x8k_bf16_full.md)",
+}
 
 
 def peaks():
