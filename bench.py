@@ -141,7 +141,7 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    b = W.make_config(args.config, seed=args.seed + rank)
+    b = W.make_config(args.config, seed=args.seed + rank, max_requests=args.requests)
     kv = hpa.KV_BF16 if b.kv_dtype == "bf16" else hpa.KV_E4M3
     C = b.num_ctas or hpa.hpa_default_num_ctas(b.Hkv, b.q_len, kv)
     q = b.q.to(dev)
@@ -177,18 +177,29 @@ def run_ours(args, rank, world, local_rank):
             import torch.distributed as dist
             dist.barrier()
 
-    def timed(fn, steps, warmup, sampler=None):
+    def timed(fn, steps, warmup, breakdown=True):
+        """ms per step over `steps` back-to-back steps (events only at the two ends, so
+        consecutive kernels keep their programmatic-dependent-launch overlap), then,
+        if asked, a second pass with events around each kernel for the breakdown."""
         for _ in range(warmup):
             fn()
-        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
+        t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         torch.cuda.synchronize(dev)
         barrier()
         torch.cuda.synchronize(dev)
+        t0.record(stream)
+        for _ in range(steps):
+            fn()
+        t1.record(stream)
+        torch.cuda.synchronize(dev)
+        barrier()
+        total = t0.elapsed_time(t1)
+        if not breakdown:
+            return total / steps, [], [], []
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
         for i in range(steps):
             fn(ev=evs[i])
         torch.cuda.synchronize(dev)
-        barrier()
-        total = evs[0][0].elapsed_time(evs[-1][3])
         attn = [e[1].elapsed_time(e[2]) for e in evs]
         plan = [e[0].elapsed_time(e[1]) for e in evs]
         comb = [e[2].elapsed_time(e[3]) for e in evs]
@@ -213,7 +224,8 @@ def run_ours(args, rank, world, local_rank):
         res = {}
         for s in sweep:
             wss = hpa.Workspace(b.B, b.q_len, b.Hq, b.d, splits=s, device=dev)
-            res[s] = timed(lambda ev=None, w=wss: step(w, ev), max(3, args.steps // 2), 2)[0]
+            res[s] = timed(lambda ev=None, w=wss: step(w, ev), max(3, args.steps // 2), 3,
+                           breakdown=False)[0]
         best = min(res, key=res.get)
         comparator = {
             "static_heuristic": {"splits": heur, "us_per_batch": round(res[heur] * 1e3, 2)},
@@ -250,7 +262,8 @@ def run_ours(args, rank, world, local_rank):
             for e in ev[1:]:
                 e.record(stream)
 
-    e2e_ms = max_over_ranks(timed(e2e_step, args.steps, args.warmup)[0], world, dev)
+    e2e_ms = max_over_ranks(timed(e2e_step, args.steps, args.warmup, breakdown=False)[0],
+                            world, dev)
 
     return dict(b=b, C=C, ms=ms, attn=attn, plan=plan_ms, comb=comb_ms, clocks=clocks,
                 comparator=comparator, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
@@ -290,7 +303,7 @@ def oracle_sample(b, target_s):
 def run_reference(args, rank, world):
     if rank != 0:
         return None
-    b = W.make_config(args.config, seed=args.seed)
+    b = W.make_config(args.config, seed=args.seed, max_requests=args.requests)
     for _ in range(args.warmup):
         oracle_sample(b, 1.0)
     secs, threads, desc = [], 0, ""
@@ -325,6 +338,8 @@ def main():
     ap.add_argument("--config", type=int, default=3, choices=[1, 2, 3, 4, 5])
     ap.add_argument("--seed", type=int, default=0)
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    ap.add_argument("--requests", type=int, default=None,
+                    help="keep only the first N requests of the workload (smaller case)")
     ap.add_argument("--no-static", action="store_true", help="skip the static comparators")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -366,7 +381,9 @@ def main():
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": round(r["ms"], 4),
         "higher_is_better": False, "scaling": "weak", "vs_baseline": None,
         "dtype": b.kv_dtype, "data": "synthetic",
-        "config": {"workload": W.CONFIGS[args.config], "batch": int(b.B),
+        "config": {"workload": W.CONFIGS[args.config] + (
+                       "" if args.requests is None else " (first %d requests)" % b.B),
+                   "batch": int(b.B),
                    "kv_tokens": int(b.seq_lens.sum()), "q_len": b.q_len, "heads": "64q/8kv",
                    "head_dim": 128, "page": 64, "tile": b.tile, "num_ctas": int(r["C"]),
                    "kv_dtype": b.kv_dtype, "kv_bytes": int(kv_bytes),

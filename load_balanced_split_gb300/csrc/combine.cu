@@ -2,11 +2,14 @@
 // log-sum-exp ("Hy3 Preview AI Infra 推理优化精读笔记", §3.1 方案 step 5;
 // "腾讯混元AI Infra进化：HPC-Ops推理核心算子全面升级", §二.1 Combine Kernel).
 //
-// One warp per (request r, query token j, head g); lane i owns head dims
-// [4i, 4i+4).  Over r's segments s:
+// One 128-thread block per (request r, query token j, head g).  Over r's
+// segments s:
 //   M = max lse_s, w_s = exp(lse_s - M), out = sum w_s o_s / sum w_s,
 //   out_lse = M + ln sum w_s.
-// A task map whose status word is non-zero makes every output NaN.
+// The four warps take every fourth segment (lane i owns head dims [4i, 4i+4))
+// with several loads in flight per warp, so a request split over many
+// partitions costs a few round trips, not one per segment.  A task map whose
+// status word is non-zero makes every output NaN.
 #include <math_constants.h>
 
 #include "hpa_internal.cuh"
@@ -14,59 +17,95 @@
 namespace hpa {
 namespace {
 
-constexpr int kWarps = 8;
+constexpr int kWarps = 4;
+constexpr int kUnroll = 4;
 
 __global__ void __launch_bounds__(kWarps * 32)
     combine_kernel(const float *__restrict__ po, const float *__restrict__ plse,
                    const int32_t *__restrict__ tm, int B, int C, int q_len, int Hq,
                    __nv_bfloat16 *__restrict__ out, float *__restrict__ out_lse) {
-  const int lane = threadIdx.x & 31;
-  const int64_t item = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  const int64_t n_items = static_cast<int64_t>(B) * q_len * Hq;
-  if (item >= n_items) return;
-  const int r = static_cast<int>(item / (static_cast<int64_t>(q_len) * Hq));
-  const int jg = static_cast<int>(item % (static_cast<int64_t>(q_len) * Hq));  // j * Hq + g
+  pdl_wait();  // partials come from the attention kernel just before
+  const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
+  const int64_t item = blockIdx.x;  // (r * q_len + j) * Hq + g
+  const int64_t per_req = static_cast<int64_t>(q_len) * Hq;
+  const int r = static_cast<int>(item / per_req);
+  const int64_t jg = item % per_req;
+  __shared__ float s_max[kWarps], s_w[kWarps];
+  __shared__ float4 s_acc[kWarps][32];
+
   const TaskMapLayout lay = TaskMapLayout::make(B, C);
-  const bool bad = tm[TM_STATUS] != 0 || tm[TM_B] != B || tm[TM_C] != C;
+  if (tm[TM_STATUS] != 0 || tm[TM_B] != B || tm[TM_C] != C) {
+    if (w == 0) {
+      const float nan = CUDART_NAN_F;
+      const __nv_bfloat162 n2 = __floats2bfloat162_rn(nan, nan);
+      uint2 pk;
+      pk.x = pk.y = *reinterpret_cast<const uint32_t *>(&n2);
+      reinterpret_cast<uint2 *>(out + item * HEAD_DIM)[lane] = pk;
+      if (out_lse != nullptr && lane == 0) out_lse[item] = nan;
+    }
+    return;
+  }
+  const int s0 = tm[lay.seg_off + r], s1 = tm[lay.seg_off + r + 1];
+
+  float m = -CUDART_INF_F;
+  for (int s = s0 + threadIdx.x; s < s1; s += kWarps * 32) m = fmaxf(m, plse[s * per_req + jg]);
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  if (lane == 0) s_max[w] = m;
+  __syncthreads();
+  float M = s_max[0];
+#pragma unroll
+  for (int x = 1; x < kWarps; ++x) M = fmaxf(M, s_max[x]);
+  const float Mb = M == -CUDART_INF_F ? 0.f : M;
 
   float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-  float lse;
-  if (bad) {
-    acc = make_float4(CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F, CUDART_NAN_F);
-    lse = CUDART_NAN_F;
-  } else {
-    const int s0 = tm[lay.seg_off + r], s1 = tm[lay.seg_off + r + 1];
-    const int64_t stride = static_cast<int64_t>(q_len) * Hq;  // per segment
-    float M = -CUDART_INF_F;
-    for (int s = s0 + lane; s < s1; s += 32) M = fmaxf(M, plse[s * stride + jg]);
+  float W = 0.f;
+  for (int s = s0 + w; s < s1; s += kWarps * kUnroll) {
+    float l[kUnroll];
+    float4 v[kUnroll];
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
-    const float Mb = M == -CUDART_INF_F ? 0.f : M;
-    float W = 0.f;
-    for (int s = s0; s < s1; ++s) {
-      const float w = expf(plse[s * stride + jg] - Mb);
-      const float4 v =
-          reinterpret_cast<const float4 *>(po + (s * stride + jg) * HEAD_DIM)[lane];
-      acc.x += w * v.x;
-      acc.y += w * v.y;
-      acc.z += w * v.z;
-      acc.w += w * v.w;
-      W += w;
+    for (int u = 0; u < kUnroll; ++u) {
+      const int ss = s + u * kWarps;
+      if (ss < s1) {
+        l[u] = plse[ss * per_req + jg];
+        v[u] = reinterpret_cast<const float4 *>(po + (ss * per_req + jg) * HEAD_DIM)[lane];
+      }
     }
-    const float inv = W > 0.f ? 1.f / W : 0.f;
-    acc.x *= inv;
-    acc.y *= inv;
-    acc.z *= inv;
-    acc.w *= inv;
-    lse = W > 0.f ? Mb + logf(W) : -CUDART_INF_F;
+#pragma unroll
+    for (int u = 0; u < kUnroll; ++u) {
+      if (s + u * kWarps < s1) {
+        const float wt = expf(l[u] - Mb);
+        acc.x += wt * v[u].x;
+        acc.y += wt * v[u].y;
+        acc.z += wt * v[u].z;
+        acc.w += wt * v[u].w;
+        W += wt;
+      }
+    }
   }
-  __nv_bfloat162 lo = __floats2bfloat162_rn(acc.x, acc.y);
-  __nv_bfloat162 hi = __floats2bfloat162_rn(acc.z, acc.w);
+  s_acc[w][lane] = acc;
+  if (lane == 0) s_w[w] = W;
+  __syncthreads();
+  if (w != 0) return;
+  float Wt = 0.f;
+  float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+  for (int x = 0; x < kWarps; ++x) {
+    const float4 t = s_acc[x][lane];
+    a.x += t.x;
+    a.y += t.y;
+    a.z += t.z;
+    a.w += t.w;
+    Wt += s_w[x];
+  }
+  const float inv = Wt > 0.f ? 1.f / Wt : 0.f;
+  const __nv_bfloat162 lo = __floats2bfloat162_rn(a.x * inv, a.y * inv);
+  const __nv_bfloat162 hi = __floats2bfloat162_rn(a.z * inv, a.w * inv);
   uint2 pk;
-  pk.x = *reinterpret_cast<uint32_t *>(&lo);
-  pk.y = *reinterpret_cast<uint32_t *>(&hi);
+  pk.x = *reinterpret_cast<const uint32_t *>(&lo);
+  pk.y = *reinterpret_cast<const uint32_t *>(&hi);
   reinterpret_cast<uint2 *>(out + item * HEAD_DIM)[lane] = pk;
-  if (out_lse != nullptr && lane == 0) out_lse[item] = lse;
+  if (out_lse != nullptr && lane == 0) out_lse[item] = Wt > 0.f ? Mb + logf(Wt) : -CUDART_INF_F;
 }
 
 }  // namespace
@@ -75,10 +114,17 @@ cudaError_t launch_combine(const float *po, const float *plse, int32_t *tm, int 
                            int q_len, int Hq, __nv_bfloat16 *out, float *out_lse,
                            cudaStream_t s) {
   const int64_t items = static_cast<int64_t>(B) * q_len * Hq;
-  const int64_t blocks = (items + kWarps - 1) / kWarps;
-  combine_kernel<<<static_cast<unsigned>(blocks), kWarps * 32, 0, s>>>(po, plse, tm, B, C,
-                                                                       q_len, Hq, out, out_lse);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(static_cast<unsigned>(items));
+  cfg.blockDim = dim3(kWarps * 32);
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, combine_kernel, po, static_cast<const float *>(plse),
+                            static_cast<const int32_t *>(tm), B, C, q_len, Hq, out, out_lse);
 }
 
 }  // namespace hpa

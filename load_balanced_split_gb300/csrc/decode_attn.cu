@@ -486,6 +486,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int c = blockIdx.x, h = blockIdx.y;
   __shared__ int hdr[4];  // go, tile, s_begin, s_end -- read once, used by all threads
   const uint32_t base = smem_u32(smem);
+  // Nothing above this line reads memory that an earlier kernel writes: with
+  // programmatic dependent launch the prologue overlaps the previous kernel.
+  pdl_wait();
   if (threadIdx.x == 0) {
     const int32_t *tm = p.tm;
     const int tile = tm[TM_TILE];
@@ -509,6 +512,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   for (int v = threadIdx.x; v < MAX_ROWS * HEAD_DIM / 4; v += kThreads)
     mb4[v] = make_float4(0.f, 0.f, 0.f, 0.f);
   __syncthreads();
+  pdl_launch_dependents();  // the combine kernel may be scheduled; it waits for this grid
   if (!hdr[0]) return;  // bad map, or a partition with no tiles
   const int tile = hdr[1], s_begin = hdr[2], s_end = hdr[3];
 
@@ -531,9 +535,17 @@ cudaError_t launch(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMa
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
-  dim3 grid(p.C, p.Hkv);
-  decode_attn_kernel<KV><<<grid, kThreads, Smem<KV>::kAlloc, s>>>(tmk, tmv, p);
-  return cudaGetLastError();
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.C, p.Hkv);
+  cfg.blockDim = dim3(kThreads);
+  cfg.dynamicSmemBytes = Smem<KV>::kAlloc;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_attn_kernel<KV>, tmk, tmv, p);
 }
 
 template <int KV>

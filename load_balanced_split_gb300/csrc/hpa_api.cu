@@ -224,7 +224,7 @@ int hpa_combine(const float *partial_o_dev, const float *partial_lse_dev, void *
   if (B < 1 || B > kMaxB || num_ctas < 1 || num_ctas > kMaxC || q_len < 1 || Hq < 1)
     return HPA_ERR_INVALID;
   if (d != hpa::HEAD_DIM) return HPA_ERR_UNSUPPORTED;
-  if (int64_t(B) * q_len * Hq > (int64_t(1) << 34)) return HPA_ERR_UNSUPPORTED;
+  if (int64_t(B) * q_len * Hq > INT_MAX) return HPA_ERR_UNSUPPORTED;  // one block per row
   if (!aligned(partial_o_dev, 16) || !aligned(out_dev, 8) || !aligned(taskmap_dev, 16))
     return HPA_ERR_ALIGN;
   cudaError_t e = hpa::launch_combine(partial_o_dev, partial_lse_dev,

@@ -200,6 +200,15 @@ __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
 
+// Programmatic dependent launch: a grid launched with programmatic stream
+// serialisation may start before its predecessor ends; pdl_wait() blocks until
+// the predecessor grids have completed and their writes are visible (a no-op
+// when the grid was launched without the attribute).
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+__device__ __forceinline__ void pdl_launch_dependents() {
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+}
+
 __device__ __forceinline__ void status_or(int32_t *tm, int bits) {
   atomicOr(reinterpret_cast<int *>(tm + TM_STATUS), bits);
 }

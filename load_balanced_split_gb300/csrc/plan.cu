@@ -57,11 +57,19 @@ __device__ int upper_bound(const int32_t *a, int n, long long x) {
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__restrict__ lens_in,
                                                             int B, int tile, int C, int kind,
                                                             int splits, int32_t *tm,
-                                                            long long s_cap) {
+                                                            long long s_cap, int staged) {
+  // Let the attention kernel that follows start its prologue now; it waits for
+  // this grid's completion before it reads the map.
+  pdl_launch_dependents();
   const TaskMapLayout lay = TaskMapLayout::make(B, C);
-  int32_t *lens = tm + lay.lens, *cu = tm + lay.cu_tiles, *cb = tm + lay.cta_begin;
+  int32_t *lens = tm + lay.lens, *cu_g = tm + lay.cu_tiles, *cb_g = tm + lay.cta_begin;
   int32_t *cs = tm + lay.cta_seg, *so = tm + lay.seg_off;
   int4 *seg = reinterpret_cast<int4 *>(tm + lay.segs);
+  // Working copies of cu_tiles and cta_begin: in shared memory when they fit
+  // (the binary searches below then cost shared- instead of L2 latency).
+  extern __shared__ int32_t stage_buf[];
+  int32_t *cu = staged ? stage_buf : cu_g;
+  int32_t *cb = staged ? stage_buf + B + 1 : cb_g;
   __shared__ long long wbuf[kPlanThreads / 32];
   __shared__ int s_bad;
   const int tid = threadIdx.x;
@@ -80,10 +88,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
       else n = (L - 1) / tile + 1;
     }
     const long long incl = block_scan(n, wbuf, total);
-    if (i < B) cu[i + 1] = static_cast<int32_t>(carry + incl);
+    if (i < B) cu[i + 1] = cu_g[i + 1] = static_cast<int32_t>(carry + incl);
     carry += total;
   }
-  if (tid == 0) cu[0] = 0;
+  if (tid == 0) cu[0] = cu_g[0] = 0;
   if (carry > INT_MAX && tid == 0) atomicOr(&s_bad, HPA_STATUS_OVERFLOW);
   __syncthreads();
   const long long T = carry;
@@ -119,9 +127,9 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
         begin = cu[r + 1];
       }
     }
-    cb[c] = static_cast<int32_t>(begin);
+    cb[c] = cb_g[c] = static_cast<int32_t>(begin);
   }
-  if (tid == 0) cb[C] = static_cast<int32_t>(T);
+  if (tid == 0) cb[C] = cb_g[C] = static_cast<int32_t>(T);
   __syncthreads();
 
   // a4: segments per partition, their running sum, then the segment rows
@@ -158,14 +166,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
       const int lo = (b > cu[r] ? b : cu[r]) - cu[r];
       const int hi = (e < cu[r + 1] ? e : cu[r + 1]) - cu[r];
       seg[out] = make_int4(r, lo, hi, c);
+      if (lo == 0) so[r] = out;  // the partition holding r's first tile holds its first segment
     }
   }
   for (long long s = S + tid; s < s_cap; s += kPlanThreads) seg[s] = make_int4(-1, -1, -1, -1);
-  __syncthreads();
-  for (long long s = tid; s < S; s += kPlanThreads) {
-    const int r = seg[s].x;
-    if (s == 0 || seg[s - 1].x != r) so[r] = static_cast<int32_t>(s);
-  }
   if (tid == 0) {
     so[B] = static_cast<int32_t>(S);
     for (int w = TM_SCAP + 1; w < TM_HEADER_WORDS; ++w) tm[w] = 0;
@@ -187,7 +191,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
 
 cudaError_t launch_plan(const int32_t *seq_lens, int B, int tile, int C, int kind, int splits,
                         int32_t *tm, int64_t s_cap, cudaStream_t s) {
-  plan_kernel<<<1, kPlanThreads, 0, s>>>(seq_lens, B, tile, C, kind, splits, tm, s_cap);
+  // cu_tiles and cta_begin are staged in shared memory when they fit in 40 KB
+  const size_t stage_bytes = (static_cast<size_t>(B) + 1 + C + 1) * sizeof(int32_t);
+  const int staged = stage_bytes <= 40 * 1024;
+  plan_kernel<<<1, kPlanThreads, staged ? stage_bytes : 0, s>>>(seq_lens, B, tile, C, kind,
+                                                                  splits, tm, s_cap, staged);
   return cudaGetLastError();
 }
 

@@ -239,9 +239,14 @@ def config_lens(cfg: int, seed: int = 0) -> np.ndarray:
             4: lens_long, 5: lambda: lens_lognormal(seed)}[cfg]()
 
 
-def make_config(cfg: int, seed: int = 0) -> Batch:
-    """The five decode workloads (sizes in the module docstring of each length recipe)."""
+def make_config(cfg: int, seed: int = 0, max_requests: int | None = None) -> Batch:
+    """The five decode workloads (sizes in the docstring of each length recipe).
+
+    max_requests keeps only the first requests of the batch (smaller cases of
+    the same workload, e.g. for profiling)."""
     lens = config_lens(cfg, seed)
+    if max_requests is not None:
+        lens = lens[:max_requests]
     if cfg == 1:
         return make_batch(lens, seed=seed, shuffle_pages=False, name=CONFIGS[1], num_ctas=4)
     if cfg == 5:
