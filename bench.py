@@ -143,7 +143,7 @@ def run_ours(args, rank, world, local_rank):
     dev = torch.device("cuda", local_rank)
     b = W.make_config(args.config, seed=args.seed + rank, max_requests=args.requests)
     kv = hpa.KV_BF16 if b.kv_dtype == "bf16" else hpa.KV_E4M3
-    C = b.num_ctas or hpa.hpa_default_num_ctas(b.Hkv, b.q_len, kv)
+    C = args.num_ctas or b.num_ctas or hpa.hpa_default_num_ctas(b.Hkv, b.q_len, kv)
     q = b.q.to(dev)
     k, v = b.k_pool.to(dev), b.v_pool.to(dev)
     ks = vs = None
@@ -215,6 +215,20 @@ def run_ours(args, rank, world, local_rank):
 
     ms = max_over_ranks(ms, world, dev)       # the slowest rank sets the step time
 
+    def traced_tail(w, reps=3):
+        """Per-CTA timestamps of the attention kernel (outside the timed region)."""
+        tr = torch.zeros(4 * w.num_ctas * b.Hkv, dtype=torch.int64, device=dev)
+        out_t = None
+        for _ in range(reps):
+            w.plan(lens, b.tile, stream)
+            hpa.hpa_decode_attn_traced(q, k, v, indptr, indices, w.taskmap, w.num_ctas,
+                                       w.partial_o, w.partial_lse, tr, ks, vs, stream=stream)
+            torch.cuda.synchronize(dev)
+            out_t = hpa.trace_summary(tr, w.num_ctas, b.Hkv)
+        return {k2: round(v2, 3) if isinstance(v2, float) else v2 for k2, v2 in out_t.items()}
+
+    tail = traced_tail(ws)
+
     # static split-KV comparators through the same kernels (heuristic and best of a sweep)
     comparator = None
     if not args.no_static and rank == 0:
@@ -227,9 +241,13 @@ def run_ours(args, rank, world, local_rank):
             res[s] = timed(lambda ev=None, w=wss: step(w, ev), max(3, args.steps // 2), 3,
                            breakdown=False)[0]
         best = min(res, key=res.get)
+        wsb = hpa.Workspace(b.B, b.q_len, b.Hq, b.d, splits=best, device=dev)
+        _, attn_b, _, _ = timed(lambda ev=None, w=wsb: step(w, ev), max(3, args.steps // 2), 3)
         comparator = {
             "static_heuristic": {"splits": heur, "us_per_batch": round(res[heur] * 1e3, 2)},
-            "static_best": {"splits": best, "us_per_batch": round(res[best] * 1e3, 2)},
+            "static_best": {"splits": best, "us_per_batch": round(res[best] * 1e3, 2),
+                            "attention_us": round(statistics.mean(attn_b) * 1e3, 2),
+                            "tail": traced_tail(wsb)},
             "sweep_us": {str(s): round(t * 1e3, 2) for s, t in res.items()},
             "speedup_vs_static_heuristic": round(res[heur] / ms, 3),
             "speedup_vs_static_best": round(res[best] / ms, 3),
@@ -265,7 +283,7 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = max_over_ranks(timed(e2e_step, args.steps, args.warmup, breakdown=False)[0],
                             world, dev)
 
-    return dict(b=b, C=C, ms=ms, attn=attn, plan=plan_ms, comb=comb_ms, clocks=clocks,
+    return dict(b=b, C=C, ms=ms, attn=attn, plan=plan_ms, comb=comb_ms, clocks=clocks, tail=tail,
                 comparator=comparator, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
 
 
@@ -340,6 +358,8 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--requests", type=int, default=None,
                     help="keep only the first N requests of the workload (smaller case)")
+    ap.add_argument("--num-ctas", type=int, default=None,
+                    help="partitions per KV head (default: the device default)")
     ap.add_argument("--no-static", action="store_true", help="skip the static comparators")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     args = ap.parse_args()
@@ -397,6 +417,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "decode_attn_kernel", "peak_kind": peak_kind + " (hbm_gbs)"},
+        "tail": r["tail"],
         "cpu_baseline": cpu,
         "e2e": {"value": round(per_batch_us(r["e2e_ms"], world), 2), "unit": UNIT,
                 "h2d_bytes_per_step": int(r["h2d"]), "d2h_bytes_per_step": int(r["d2h"])},

@@ -163,6 +163,23 @@ int hpa_decode_attn(const void *q_dev, const void *k_pool_dev, const void *v_poo
                     float *partial_lse_dev, hpa_stream_t stream);
 
 /*
+ * hpa_decode_attn_traced -- hpa_decode_attn that also records, for every CTA,
+ * four uint64 words at trace_dev[4 * (h * num_ctas + c)]: the %globaltimer (ns)
+ * at kernel entry, after the task map was read, after the CTA's last segment
+ * was stored, and (smid | segments << 32).  Used to measure SM busy time and
+ * the tail idle of the last CTA (the pages watch "attention kernel tail idle",
+ * "Hy3 Preview AI Infra 推理优化精读笔记", §3.1 对我们的启发).  trace_dev: device,
+ * 8-byte aligned, >= 4 * num_ctas * Hkv words.
+ */
+int hpa_decode_attn_traced(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
+                           int32_t kv_dtype, const float *k_scale_dev, const float *v_scale_dev,
+                           int64_t num_pages, const int32_t *page_indptr_dev,
+                           const int32_t *page_indices_dev, int32_t page_size, int32_t B,
+                           int32_t q_len, int32_t Hq, int32_t Hkv, int32_t d, float sm_scale,
+                           void *taskmap_dev, int32_t num_ctas, float *partial_o_dev,
+                           float *partial_lse_dev, uint64_t *trace_dev, hpa_stream_t stream);
+
+/*
  * hpa_combine -- the Combine kernel ([Notes §3.1] step 5, [HPC-Ops §二.1]).
  * For every (request r, token j, head g) over r's segments s:
  *   M = max_s lse_s,  w_s = exp(lse_s - M),

@@ -35,10 +35,13 @@ constexpr uint32_t kFull = 0xffffffffu;
 
 template <int KV>
 struct Cfg;
+// Ring depth: bf16 pages stream best with few bytes in flight per CTA (two
+// 32 KB stages: fairer sharing of DRAM between the CTAs of one wave, a shorter
+// tail); E4M3 consumers do more work per byte and want a deeper ring.
 template <>
 struct Cfg<HPA_KV_BF16> {
   static constexpr int kKBytes = 16384;  // one page-head of K: 64 x 128 bf16
-  static constexpr int kStages = 3;
+  static constexpr int kStages = 2;
 };
 template <>
 struct Cfg<HPA_KV_E4M3> {
@@ -191,6 +194,9 @@ __device__ __forceinline__ void qk(float (&s)[2][4], const uint32_t (&qa)[8][4],
       mma_bf16(s[1], qa[ks], b2, b3);
     }
   } else {
+    // thread (r8, qd) reads head dims [32 qd, 32 qd + 32) of its key row and widens
+    // them to f16; k-step ks covers dims 32 qd + 4 ks + [0, 4), the same
+    // permutation of the head dimension the query fragments use.
     const int r8 = lane >> 2, qd = lane & 3;
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
@@ -381,12 +387,16 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
       }
       l0 = l0 * a0 + (sc[0][0] + sc[0][1] + sc[1][0] + sc[1][1]);
       l1 = l1 * a1 + (sc[0][2] + sc[0][3] + sc[1][2] + sc[1][3]);
+      // the running max rarely moves once a segment is under way: skip the
+      // rescale when no row of this warp changed it (alpha == 1 exactly)
+      if (__any_sync(kFull, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        o[i][0] *= a0;
-        o[i][1] *= a0;
-        o[i][2] *= a1;
-        o[i][3] *= a1;
+        for (int i = 0; i < 16; ++i) {
+          o[i][0] *= a0;
+          o[i][1] *= a0;
+          o[i][2] *= a1;
+          o[i][3] *= a1;
+        }
       }
       uint32_t pa[4];
       if (KV == HPA_KV_BF16) {
@@ -486,6 +496,9 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int c = blockIdx.x, h = blockIdx.y;
   __shared__ int hdr[4];  // go, tile, s_begin, s_end -- read once, used by all threads
   const uint32_t base = smem_u32(smem);
+  unsigned long long *trace =
+      p.trace ? p.trace + 4 * (static_cast<int64_t>(h) * p.C + c) : nullptr;
+  if (trace && threadIdx.x == 0) trace[0] = globaltimer_ns();
   // Nothing above this line reads memory that an earlier kernel writes: with
   // programmatic dependent launch the prologue overlaps the previous kernel.
   pdl_wait();
@@ -513,13 +526,22 @@ __global__ void __launch_bounds__(kThreads, 2)
     mb4[v] = make_float4(0.f, 0.f, 0.f, 0.f);
   __syncthreads();
   pdl_launch_dependents();  // the combine kernel may be scheduled; it waits for this grid
-  if (!hdr[0]) return;  // bad map, or a partition with no tiles
+  if (trace && threadIdx.x == 0) {
+    trace[1] = globaltimer_ns();
+    trace[3] = smid() | (static_cast<unsigned long long>(hdr[3] - hdr[2]) << 32);
+  }
+  if (!hdr[0]) {  // bad map, or a partition with no tiles
+    if (trace && threadIdx.x == 0) trace[2] = globaltimer_ns();
+    return;
+  }
   const int tile = hdr[1], s_begin = hdr[2], s_end = hdr[3];
 
-  if (threadIdx.x >= kConsumerWarps * 32)
+  if (threadIdx.x >= kConsumerWarps * 32) {
     producer<KV>(p, &tmk, &tmv, smem, s_begin, s_end, tile, h);
-  else
+  } else {
     consumer<KV>(p, smem, s_begin, s_end, tile, h);
+    if (trace && threadIdx.x == 0) trace[2] = globaltimer_ns();  // after the last epilogue
+  }
 }
 
 template <int KV>

@@ -167,13 +167,14 @@ int hpa_plan_static(const int32_t *seq_lens_dev, int32_t B, int32_t tile, int32_
   return e == cudaSuccess ? HPA_OK : cuda_fail(e);
 }
 
-int hpa_decode_attn(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
-                    int32_t kv_dtype, const float *k_scale_dev, const float *v_scale_dev,
-                    int64_t num_pages, const int32_t *page_indptr_dev,
-                    const int32_t *page_indices_dev, int32_t page_size, int32_t B,
-                    int32_t q_len, int32_t Hq, int32_t Hkv, int32_t d, float sm_scale,
-                    void *taskmap_dev, int32_t num_ctas, float *partial_o_dev,
-                    float *partial_lse_dev, hpa_stream_t stream) {
+static int decode_attn_impl(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
+                            int32_t kv_dtype, const float *k_scale_dev,
+                            const float *v_scale_dev, int64_t num_pages,
+                            const int32_t *page_indptr_dev, const int32_t *page_indices_dev,
+                            int32_t page_size, int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv,
+                            int32_t d, float sm_scale, void *taskmap_dev, int32_t num_ctas,
+                            float *partial_o_dev, float *partial_lse_dev, uint64_t *trace_dev,
+                            hpa_stream_t stream) {
   if (!q_dev || !k_pool_dev || !v_pool_dev || !page_indptr_dev || !page_indices_dev ||
       !taskmap_dev || !partial_o_dev || !partial_lse_dev)
     return HPA_ERR_INVALID;
@@ -202,6 +203,7 @@ int hpa_decode_attn(const void *q_dev, const void *k_pool_dev, const void *v_poo
   p.v_scale = v_scale_dev;
   p.partial_o = partial_o_dev;
   p.partial_lse = partial_lse_dev;
+  p.trace = reinterpret_cast<unsigned long long *>(trace_dev);
   p.num_pages = num_pages;
   p.lay = hpa::TaskMapLayout::make(B, num_ctas);
   p.B = B;
@@ -215,6 +217,34 @@ int hpa_decode_attn(const void *q_dev, const void *k_pool_dev, const void *v_poo
   cudaError_t e = hpa::launch_decode_attn(p, tmk, tmv, kv_dtype,
                                           reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? HPA_OK : cuda_fail(e);
+}
+
+int hpa_decode_attn(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
+                    int32_t kv_dtype, const float *k_scale_dev, const float *v_scale_dev,
+                    int64_t num_pages, const int32_t *page_indptr_dev,
+                    const int32_t *page_indices_dev, int32_t page_size, int32_t B,
+                    int32_t q_len, int32_t Hq, int32_t Hkv, int32_t d, float sm_scale,
+                    void *taskmap_dev, int32_t num_ctas, float *partial_o_dev,
+                    float *partial_lse_dev, hpa_stream_t stream) {
+  return decode_attn_impl(q_dev, k_pool_dev, v_pool_dev, kv_dtype, k_scale_dev, v_scale_dev,
+                          num_pages, page_indptr_dev, page_indices_dev, page_size, B, q_len, Hq,
+                          Hkv, d, sm_scale, taskmap_dev, num_ctas, partial_o_dev,
+                          partial_lse_dev, nullptr, stream);
+}
+
+int hpa_decode_attn_traced(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
+                           int32_t kv_dtype, const float *k_scale_dev, const float *v_scale_dev,
+                           int64_t num_pages, const int32_t *page_indptr_dev,
+                           const int32_t *page_indices_dev, int32_t page_size, int32_t B,
+                           int32_t q_len, int32_t Hq, int32_t Hkv, int32_t d, float sm_scale,
+                           void *taskmap_dev, int32_t num_ctas, float *partial_o_dev,
+                           float *partial_lse_dev, uint64_t *trace_dev, hpa_stream_t stream) {
+  if (!trace_dev) return HPA_ERR_INVALID;
+  if (!aligned(trace_dev, 8)) return HPA_ERR_ALIGN;
+  return decode_attn_impl(q_dev, k_pool_dev, v_pool_dev, kv_dtype, k_scale_dev, v_scale_dev,
+                          num_pages, page_indptr_dev, page_indices_dev, page_size, B, q_len, Hq,
+                          Hkv, d, sm_scale, taskmap_dev, num_ctas, partial_o_dev,
+                          partial_lse_dev, trace_dev, stream);
 }
 
 int hpa_combine(const float *partial_o_dev, const float *partial_lse_dev, void *taskmap_dev,

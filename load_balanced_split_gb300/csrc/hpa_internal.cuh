@@ -46,6 +46,7 @@ struct AttnParams {
   const int32_t *page_indptr, *page_indices;
   const float *k_scale, *v_scale;
   float *partial_o, *partial_lse;
+  unsigned long long *trace;  // optional: 4 words per CTA (entry, go, end, smid | segs << 32)
   int64_t num_pages;
   TaskMapLayout lay;
   int B, C, q_len, Hq, Hkv, G, rows;
@@ -90,6 +91,12 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
       : "r"(bar), "r"(parity)
       : "memory");
   return ok != 0;
+}
+
+__device__ __forceinline__ uint32_t smid() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%smid;" : "=r"(r));
+  return r;
 }
 
 __device__ __forceinline__ uint64_t globaltimer_ns() {
@@ -182,8 +189,9 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
 // Two E4M3 codes (low 16 bits of `v`, element 0 in the low byte) -> f16x2 with
 // element 0 in the low half (exact: every E4M3 value is an f16 value).
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint16_t v) {
-  const __half2_raw h = __nv_cvt_fp8x2_to_halfraw2(static_cast<__nv_fp8x2_storage_t>(v), __NV_E4M3);
-  return static_cast<uint32_t>(h.x) | (static_cast<uint32_t>(h.y) << 16);
+  uint32_t r;
+  asm("cvt.rn.f16x2.e4m3x2 %0, %1;" : "=r"(r) : "h"(v));
+  return r;
 }
 
 __device__ __forceinline__ uint32_t pack_bf16(float lo, float hi) {

@@ -53,6 +53,8 @@ def lib():
                 "hpa_plan_static": ([P, I32, I32, I32, P, SZ, P], ctypes.c_int),
                 "hpa_decode_attn": ([P, P, P, I32, P, P, I64, P, P, I32, I32, I32, I32, I32,
                                      I32, F, P, I32, P, P, P], ctypes.c_int),
+                "hpa_decode_attn_traced": ([P, P, P, I32, P, P, I64, P, P, I32, I32, I32, I32,
+                                            I32, I32, F, P, I32, P, P, P, P], ctypes.c_int),
                 "hpa_combine": ([P, P, P, I32, I32, I32, I32, I32, P, P, P], ctypes.c_int),
                 "hpa_selftest_wait_timeout": ([P, I64, P], ctypes.c_int),
                 "hpa_decode_attn_combine_noalloc": ([P, P, P, I32, P, P, I64, P, P, I32, I32,
@@ -172,6 +174,57 @@ def hpa_decode_attn(q, k_pool, v_pool, page_indptr, page_indices, taskmap, num_c
         _ptr(page_indptr), _ptr(page_indices), page, B, q_len, Hq, Hkv, d, float(sm_scale),
         _ptr(taskmap), num_ctas, _ptr(partial_o), _ptr(partial_lse), _stream(stream)),
         "hpa_decode_attn")
+
+
+def hpa_decode_attn_traced(q, k_pool, v_pool, page_indptr, page_indices, taskmap, num_ctas: int,
+                           partial_o, partial_lse, trace, k_scale=None, v_scale=None,
+                           sm_scale: float | None = None, stream=None):
+    """hpa_decode_attn plus per-CTA timestamps: trace is int64 [num_ctas * Hkv * 4] on device."""
+    _dev(trace, "trace", torch.int64)
+    B, q_len, Hq, d = q.shape
+    kv = KV_BF16 if k_pool.dtype == torch.bfloat16 else KV_E4M3
+    P, Hkv, page, _ = k_pool.shape
+    if trace.numel() < 4 * num_ctas * Hkv:
+        raise HpaError("trace buffer too small")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d)
+    _check(lib().hpa_decode_attn_traced(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), kv, _ptr(k_scale), _ptr(v_scale), P,
+        _ptr(page_indptr), _ptr(page_indices), page, B, q_len, Hq, Hkv, d, float(sm_scale),
+        _ptr(taskmap), num_ctas, _ptr(partial_o), _ptr(partial_lse), _ptr(trace),
+        _stream(stream)), "hpa_decode_attn_traced")
+
+
+def trace_summary(trace, num_ctas: int, Hkv: int) -> dict:
+    """SM busy and tail figures from a hpa_decode_attn_traced buffer (host-side arithmetic)."""
+    import numpy as np
+    t = trace.view(-1, 4).cpu().numpy().astype(np.int64)[:num_ctas * Hkv]
+    entry, go, end, info = t[:, 0], t[:, 1], t[:, 2], t[:, 3]
+    sm = info & 0xffffffff
+    busy = t[(info >> 32) > 0]
+    t0 = int(entry.min())
+    span = int(end.max()) - t0
+    ends = np.sort(busy[:, 2]) if len(busy) else np.sort(end)
+    per_sm = {}
+    for s_, a, b_ in zip(sm, go, end):
+        per_sm.setdefault(int(s_), []).append((int(a), int(b_)))
+    occ = []
+    for iv in per_sm.values():
+        iv.sort()
+        tot, cur_a, cur_b = 0, iv[0][0], iv[0][1]
+        for a, b_ in iv[1:]:
+            if a > cur_b:
+                tot += cur_b - cur_a
+                cur_a, cur_b = a, b_
+            else:
+                cur_b = max(cur_b, b_)
+        occ.append(tot + cur_b - cur_a)
+    return {"span_us": span / 1e3,
+            "first_go_us": (int(go.min()) - t0) / 1e3,
+            "median_cta_end_us": (float(np.median(ends)) - t0) / 1e3,
+            "last_cta_tail_us": (float(ends[-1]) - float(np.median(ends))) / 1e3,
+            "sm_busy_frac": float(np.mean(occ)) / span if span > 0 else 0.0,
+            "sms_used": len(per_sm)}
 
 
 def hpa_combine(partial_o, partial_lse, taskmap, num_ctas: int, out, out_lse=None, stream=None):

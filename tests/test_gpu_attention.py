@@ -153,3 +153,29 @@ def test_sm_scale_argument():
     ref, ref_lse = oracle.attention(b, sm_scale=0.05)
     assert_close(out.float().cpu().numpy(), ref, "bf16")
     assert_lse_close(lse.cpu().numpy(), ref_lse)
+
+
+def test_traced_call_matches_and_records_every_cta():
+    b = W.make_batch([3000, 40, 12000, 700], seed=9)
+    db = DeviceBatch(b)
+    C = 6
+    ws = hpa.Workspace(b.B, 1, 64, 128, num_ctas=C)
+    ws.plan(db.lens)
+    hpa.hpa_decode_attn(db.q, db.k, db.v, db.indptr, db.indices, ws.taskmap, C, ws.partial_o,
+                        ws.partial_lse)
+    torch.cuda.synchronize()
+    S = int(ws.taskmap[5].item())
+    ref_o = ws.partial_o[:S * 64 * 128].clone()
+    trace = torch.zeros(4 * C * b.Hkv, dtype=torch.int64, device="cuda")
+    hpa.hpa_decode_attn_traced(db.q, db.k, db.v, db.indptr, db.indices, ws.taskmap, C,
+                               ws.partial_o, ws.partial_lse, trace)
+    torch.cuda.synchronize()
+    got = ws.partial_o[:S * 64 * 128]
+    assert torch.allclose(got, ref_o, rtol=1e-5, atol=1e-6)
+    t = trace.view(-1, 4).cpu().numpy()
+    assert (t[:, 0] > 0).all() and (t[:, 0] <= t[:, 1]).all() and (t[:, 1] <= t[:, 2]).all()
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert ((t[:, 3] & 0xffffffff) < sms).all()
+    assert int((t[:, 3] >> 32).sum()) == S * b.Hkv      # every segment, once per KV head
+    summ = hpa.trace_summary(trace, C, b.Hkv)
+    assert summ["span_us"] > 0 and 0 < summ["sm_busy_frac"] <= 1.0
