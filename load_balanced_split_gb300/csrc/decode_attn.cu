@@ -30,6 +30,10 @@ namespace hpa {
 namespace {
 
 constexpr int kConsumerWarps = 4;
+// Segment-end merge buffer: one row of 128 partial-output columns per query row,
+// held in accumulator-fragment order (n-tile i, column n -> i * 8 + n) and padded
+// to 136 floats so the four warps' shared-memory adds hit at most 2 lanes per bank.
+constexpr int kMergeStride = HEAD_DIM + 8;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr uint32_t kFull = 0xffffffffu;
 
@@ -53,8 +57,8 @@ template <int KV>
 struct Smem {
   static constexpr int kStageBytes = 2 * Cfg<KV>::kKBytes;
   static constexpr int kStages = Cfg<KV>::kStages;
-  static constexpr int kMerge = kStages * kStageBytes;     // float[16][128]
-  static constexpr int kStats = kMerge + MAX_ROWS * HEAD_DIM * 4;  // m[4][16], l[4][16]
+  static constexpr int kMerge = kStages * kStageBytes;     // float[16][kMergeStride]
+  static constexpr int kStats = kMerge + MAX_ROWS * kMergeStride * 4;  // m[4][16], l[4][16]
   static constexpr int kBars = kStats + 2 * kConsumerWarps * MAX_ROWS * 4;
   static constexpr int kFlag = kBars + 2 * kStages * 8;
   static constexpr int kBytes = kFlag + 16;
@@ -198,16 +202,20 @@ __device__ __forceinline__ void qk(float (&s)[2][4], const uint32_t (&qa)[8][4],
     // them to f16; k-step ks covers dims 32 qd + 4 ks + [0, 4), the same
     // permutation of the head dimension the query fragments use.
     const int r8 = lane >> 2, qd = lane & 3;
+    uint32_t u[2][8];
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
       const uint32_t row = kt + (16 * w + 8 * nt + r8) * 128;
-      uint32_t u[8];
-      lds128(row + (((2 * qd) ^ r8) << 4), u[0], u[1], u[2], u[3]);
-      lds128(row + (((2 * qd + 1) ^ r8) << 4), u[4], u[5], u[6], u[7]);
+      lds128(row + (((2 * qd) ^ r8) << 4), u[nt][0], u[nt][1], u[nt][2], u[nt][3]);
+      lds128(row + (((2 * qd + 1) ^ r8) << 4), u[nt][4], u[nt][5], u[nt][6], u[nt][7]);
+    }
+    // the two n-tiles' accumulation chains are interleaved to hide MMA latency
 #pragma unroll
-      for (int ks = 0; ks < 8; ++ks) {
-        const uint32_t b0 = e4m3x2_to_f16x2(static_cast<uint16_t>(u[ks] & 0xffffu));
-        const uint32_t b1 = e4m3x2_to_f16x2(static_cast<uint16_t>(u[ks] >> 16));
+    for (int ks = 0; ks < 8; ++ks) {
+#pragma unroll
+      for (int nt = 0; nt < 2; ++nt) {
+        const uint32_t b0 = e4m3x2_to_f16x2(static_cast<uint16_t>(u[nt][ks] & 0xffffu));
+        const uint32_t b1 = e4m3x2_to_f16x2(static_cast<uint16_t>(u[nt][ks] >> 16));
         mma_f16(s[nt], qa[ks], b0, b1);
       }
     }
@@ -257,12 +265,13 @@ __device__ __forceinline__ void pv(float (&o)[16][4], const uint32_t (&pa)[4], u
   }
 }
 
-// Head-dim index of accumulator o[i][e] (row pair aside) for this lane.
+// Merge-buffer position of head dim dd.  The bf16 accumulators hold dim 8 i + n in
+// n-tile i, column n; the E4M3 ones hold dim 16 n + i (the output-column permutation
+// of the 8-bit V path).  The buffer is in fragment order i * 8 + n either way.
 template <int KV>
-__device__ __forceinline__ int out_dim(int i, int e, int lane) {
-  const int qd = lane & 3;
-  if (KV == HPA_KV_BF16) return 8 * i + 2 * qd + e;
-  return 16 * (2 * qd + e) + i;
+__device__ __forceinline__ int merge_pos(int dd) {
+  if (KV == HPA_KV_BF16) return dd;
+  return (dd & 15) * 8 + (dd >> 4);
 }
 
 // ----------------------------------------------------------------------------- consumer
@@ -459,19 +468,31 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
     for (int i = 0; i < 16; ++i)
 #pragma unroll
       for (int e = 0; e < 2; ++e) {
-        const int dd = out_dim<KV>(i, e, lane);
-        if (v0) atomicAdd(&mbuf[row0 * HEAD_DIM + dd], o[i][e] * f0);
-        if (v1) atomicAdd(&mbuf[row1 * HEAD_DIM + dd], o[i][2 + e] * f1);
+        const int pos = i * 8 + 2 * qd + e;
+        if (v0) atomicAdd(&mbuf[row0 * kMergeStride + pos], o[i][e] * f0);
+        if (v1) atomicAdd(&mbuf[row1 * kMergeStride + pos], o[i][2 + e] * f1);
       }
     named_barrier(1, kConsumerWarps * 32);
     const int tid = threadIdx.x;
-    float4 *mb4 = reinterpret_cast<float4 *>(mbuf);
     for (int v = tid; v < rows * (HEAD_DIM / 4); v += kConsumerWarps * 32) {
       const int row = v / (HEAD_DIM / 4), c4 = v % (HEAD_DIM / 4);
       const int j = row / G, g = row % G;
       const int64_t dst = ((static_cast<int64_t>(s) * q_len + j) * p.Hq + h * G + g) * HEAD_DIM;
-      reinterpret_cast<float4 *>(p.partial_o + dst)[c4] = mb4[v];
-      mb4[v] = make_float4(0.f, 0.f, 0.f, 0.f);
+      float *mrow = mbuf + row * kMergeStride;
+      float4 val;
+      if (KV == HPA_KV_BF16) {
+        val = *reinterpret_cast<float4 *>(mrow + 4 * c4);
+        *reinterpret_cast<float4 *>(mrow + 4 * c4) = make_float4(0.f, 0.f, 0.f, 0.f);
+      } else {
+        float *x = &val.x;
+#pragma unroll
+        for (int k = 0; k < 4; ++k) {
+          const int pos = merge_pos<KV>(4 * c4 + k);
+          x[k] = mrow[pos];
+          mrow[pos] = 0.f;
+        }
+      }
+      reinterpret_cast<float4 *>(p.partial_o + dst)[c4] = val;
     }
     if (tid < rows) {
       float M, Lsum;
@@ -522,7 +543,7 @@ __global__ void __launch_bounds__(kThreads, 2)
     fence_barrier_init();
   }
   float4 *mb4 = reinterpret_cast<float4 *>(smem + S::kMerge);
-  for (int v = threadIdx.x; v < MAX_ROWS * HEAD_DIM / 4; v += kThreads)
+  for (int v = threadIdx.x; v < MAX_ROWS * kMergeStride / 4; v += kThreads)
     mb4[v] = make_float4(0.f, 0.f, 0.f, 0.f);
   __syncthreads();
   pdl_launch_dependents();  // the combine kernel may be scheduled; it waits for this grid
