@@ -141,7 +141,7 @@ int hpa_plan_static(const int32_t *seq_lens_dev, int32_t B, int32_t tile, int32_
  *   partial_o[seg][j][head][d] = o,  partial_lse[seg][j][head] = m + ln l
  * (natural log; -inf and o = 0 for a row that sees no key of the segment).
  *
- * q_dev:        bf16 [B][q_len][Hq][d], 4-byte aligned.
+ * q_dev:        bf16 [B][q_len][Hq][d], 16-byte aligned.
  * k_pool_dev, v_pool_dev: [num_pages][Hkv][page_size][d] of bf16 or E4M3
  *               bytes, 16-byte aligned (read with TMA tensor copies).
  * k_scale_dev, v_scale_dev: fp32 [Hkv] for HPA_KV_E4M3, ignored for bf16.

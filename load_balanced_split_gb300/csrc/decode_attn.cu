@@ -34,6 +34,9 @@ constexpr int kConsumerWarps = 4;
 // held in accumulator-fragment order (n-tile i, column n -> i * 8 + n) and padded
 // to 136 floats so the four warps' shared-memory adds hit at most 2 lanes per bank.
 constexpr int kMergeStride = HEAD_DIM + 8;
+// Largest score excess (log2 units) over the running reference max before the
+// accumulators are rescaled: P values stay <= 256, well inside bf16/f16 range.
+constexpr float kRescaleSlack = 8.f;
 constexpr int kThreads = (kConsumerWarps + 1) * 32;
 constexpr uint32_t kFull = 0xffffffffu;
 
@@ -50,8 +53,14 @@ struct Cfg<HPA_KV_BF16> {
 template <>
 struct Cfg<HPA_KV_E4M3> {
   static constexpr int kKBytes = 8192;  // 64 x 128 bytes
-  static constexpr int kStages = 6;
+  static constexpr int kStages = 5;
 };
+
+// Per-segment staging written by the producer warp ahead of the consumers: the
+// segment's (request, length, key range) and its query rows, in a 2-slot ring.
+// Query rows are 256 B padded to 272 B so fragment loads are free of conflicts.
+constexpr int kQRowBytes = 272;
+constexpr int kQSlotBytes = MAX_ROWS * kQRowBytes;
 
 template <int KV>
 struct Smem {
@@ -59,8 +68,10 @@ struct Smem {
   static constexpr int kStages = Cfg<KV>::kStages;
   static constexpr int kMerge = kStages * kStageBytes;     // float[16][kMergeStride]
   static constexpr int kStats = kMerge + MAX_ROWS * kMergeStride * 4;  // m[4][16], l[4][16]
-  static constexpr int kBars = kStats + 2 * kConsumerWarps * MAX_ROWS * 4;
-  static constexpr int kFlag = kBars + 2 * kStages * 8;
+  static constexpr int kQ = kStats + 2 * kConsumerWarps * MAX_ROWS * 4;  // 2 query slots
+  static constexpr int kInfo = kQ + 2 * kQSlotBytes;                      // int4[2]
+  static constexpr int kBars = kInfo + 2 * 16;  // full[kStages] empty[kStages] qfull[2] qempty[2]
+  static constexpr int kFlag = kBars + (2 * kStages + 4) * 8;
   static constexpr int kBytes = kFlag + 16;
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 B
 };
@@ -96,11 +107,34 @@ __device__ void producer(const AttnParams &p, const CUtensorMap *tmk, const CUte
     prefetch_tmap(tmk);
     prefetch_tmap(tmv);
   }
+  const uint32_t qfull0 = empty0 + 8 * S::kStages, qempty0 = qfull0 + 16;
   int stage = 0;
   uint32_t phase = 0, issued = 0, parity_bits = 0;
   bool ok = true;
   for (int s = s_begin; s < s_end && ok; ++s) {
     const SegInfo f = seg_info(p, s, tile);
+    // stage the segment's info and query rows for the consumers
+    {
+      const int k = s - s_begin, slot = k & 1;
+      const uint32_t qphase = (k >> 1) & 1;
+      int good = 1;
+      if (lane == 0) good = !*abort_flag && mbar_wait_bounded(qempty0 + 8 * slot, qphase ^ 1);
+      if (!__shfl_sync(kFull, good, 0)) {
+        ok = false;
+        break;
+      }
+      uint8_t *qs = smem + S::kQ + slot * kQSlotBytes;
+      const int G = p.G;
+      for (int ch = lane; ch < p.rows * 16; ch += 32) {  // 16-byte chunks of 256-byte rows
+        const int row = ch >> 4, c16 = ch & 15, j = row / G, g = row % G;
+        const int4 v = reinterpret_cast<const int4 *>(
+            p.q + ((static_cast<int64_t>(f.r) * p.q_len + j) * p.Hq + h * G + g) * HEAD_DIM)[c16];
+        *reinterpret_cast<int4 *>(qs + row * kQRowBytes + c16 * 16) = v;
+      }
+      if (lane == 0)
+        reinterpret_cast<int4 *>(smem + S::kInfo)[slot] = make_int4(f.r, f.L, f.klo, f.khi);
+      mbar_arrive(qfull0 + 8 * slot);  // every lane publishes its own stores
+    }
     const int pstart = p.page_indptr[f.r];
     const int pcount = p.page_indptr[f.r + 1] - pstart;  // pages listed for request r
     const int32_t *pidx = p.page_indices + pstart;
@@ -298,22 +332,34 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
   const bool v0 = row0 < rows, v1 = row1 < rows;
   const int j0 = row0 / G, g0 = row0 % G, j1 = row1 / G, g1 = row1 % G;
 
+  const uint32_t qfull0 = empty0 + 8 * S::kStages, qempty0 = qfull0 + 16;
   int stage = 0;
   uint32_t phase = 0;
   for (int s = s_begin; s < s_end; ++s) {
-    const SegInfo f = seg_info(p, s, tile);
-    if (f.L < q_len && w == 0 && lane == 0) status_or(p.tm, HPA_STATUS_BAD_SEQLEN);
+    const int k = s - s_begin, slot = k & 1;
+    bool ok = !*abort_flag && mbar_wait_bounded(qfull0 + 8 * slot, (k >> 1) & 1);
+    ok = __all_sync(kFull, ok);
+    SegInfo f;
+    {
+      const int4 inf = reinterpret_cast<const int4 *>(smem + S::kInfo)[slot];
+      f.r = inf.x;
+      f.L = inf.y;
+      f.klo = inf.z;
+      f.khi = inf.w;
+      f.pg0 = f.klo / PAGE;
+      f.pg1 = ok ? (f.khi + PAGE - 1) / PAGE : f.pg0;  // no pages if the wait gave up
+    }
+    if (ok && f.L < q_len && w == 0 && lane == 0) status_or(p.tm, HPA_STATUS_BAD_SEQLEN);
     const int lim_min = f.L - q_len + 1;  // first key hidden from some row
     const int lim0 = v0 ? f.L - q_len + 1 + j0 : f.L;
     const int lim1 = v1 ? f.L - q_len + 1 + j1 : f.L;
 
-    // query fragments (A operand, 16 rows x 128)
+    // query fragments (A operand, 16 rows x 128) from the staged rows
     uint32_t qa[8][4];
     {
-      const __nv_bfloat16 *q0 =
-          p.q + ((static_cast<int64_t>(f.r) * q_len + j0) * p.Hq + h * G + g0) * HEAD_DIM;
-      const __nv_bfloat16 *q1 =
-          p.q + ((static_cast<int64_t>(f.r) * q_len + j1) * p.Hq + h * G + g1) * HEAD_DIM;
+      const uint8_t *qs = smem + S::kQ + slot * kQSlotBytes;
+      const __nv_bfloat16 *q0 = reinterpret_cast<const __nv_bfloat16 *>(qs + row0 * kQRowBytes);
+      const __nv_bfloat16 *q1 = reinterpret_cast<const __nv_bfloat16 *>(qs + row1 * kQRowBytes);
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         if (KV == HPA_KV_BF16) {
@@ -335,6 +381,8 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
         }
       }
     }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(qempty0 + 8 * slot);  // the slot may be refilled
 
     float m0 = -CUDART_INF_F, m1 = -CUDART_INF_F, l0 = 0.f, l1 = 0.f;
     float o[16][4];
@@ -343,7 +391,6 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
 #pragma unroll
       for (int e = 0; e < 4; ++e) o[i][e] = 0.f;
 
-    bool ok = true;
     for (int pg = f.pg0; pg < f.pg1; ++pg) {
       const bool got = !(*abort_flag) && mbar_wait_bounded(full0 + 8 * stage, phase);
       if (!__all_sync(kFull, got)) {
@@ -381,7 +428,12 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
       mx0 = fmaxf(mx0, __shfl_xor_sync(kFull, mx0, 2));
       mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 1));
       mx1 = fmaxf(mx1, __shfl_xor_sync(kFull, mx1, 2));
-      const float mn0 = fmaxf(m0, mx0), mn1 = fmaxf(m1, mx1);
+      // Conditional rescale: the reference max m moves only when a score exceeds it
+      // by more than kRescaleSlack (base 2), so p = 2^(s - m) <= 2^kRescaleSlack and
+      // O / l keep one consistent reference; exact up to rounding, and the O rescale
+      // below is almost always skipped after a segment's first pages.
+      const float mn0 = mx0 > m0 + kRescaleSlack ? mx0 : m0;
+      const float mn1 = mx1 > m1 + kRescaleSlack ? mx1 : m1;
       const float b0 = mn0 == -CUDART_INF_F ? 0.f : mn0;
       const float b1 = mn1 == -CUDART_INF_F ? 0.f : mn1;
       const float a0 = exp2f(m0 - b0), a1 = exp2f(m1 - b1);
@@ -396,8 +448,7 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
       }
       l0 = l0 * a0 + (sc[0][0] + sc[0][1] + sc[1][0] + sc[1][1]);
       l1 = l1 * a1 + (sc[0][2] + sc[0][3] + sc[1][2] + sc[1][3]);
-      // the running max rarely moves once a segment is under way: skip the
-      // rescale when no row of this warp changed it (alpha == 1 exactly)
+      // skip the rescale when no row of this warp moved its reference (alpha == 1)
       if (__any_sync(kFull, a0 != 1.f || a1 != 1.f)) {
 #pragma unroll
         for (int i = 0; i < 16; ++i) {
@@ -538,6 +589,10 @@ __global__ void __launch_bounds__(kThreads, 2)
     for (int st = 0; st < S::kStages; ++st) {
       mbar_init(base + S::kBars + 8 * st, 1);
       mbar_init(base + S::kBars + 8 * (S::kStages + st), kConsumerWarps);
+    }
+    for (int sl = 0; sl < 2; ++sl) {
+      mbar_init(base + S::kBars + 8 * (2 * S::kStages + sl), 32);                 // qfull
+      mbar_init(base + S::kBars + 8 * (2 * S::kStages + 2 + sl), kConsumerWarps);  // qempty
     }
     *reinterpret_cast<int *>(smem + S::kFlag) = 0;
     fence_barrier_init();

@@ -187,7 +187,7 @@ static int decode_attn_impl(const void *q_dev, const void *k_pool_dev, const voi
       (Hq / Hkv) * q_len > hpa::MAX_ROWS)
     return HPA_ERR_UNSUPPORTED;
   if (num_pages * Hkv > INT_MAX) return HPA_ERR_UNSUPPORTED;
-  if (!aligned(q_dev, 4) || !aligned(k_pool_dev, 16) || !aligned(v_pool_dev, 16) ||
+  if (!aligned(q_dev, 16) || !aligned(k_pool_dev, 16) || !aligned(v_pool_dev, 16) ||
       !aligned(taskmap_dev, 16) || !aligned(partial_o_dev, 16) || !aligned(partial_lse_dev, 4))
     return HPA_ERR_ALIGN;
   CUtensorMap tmk, tmv;
