@@ -42,8 +42,8 @@ UNIT = "us/batch"
 # Taken on the uniform 32 x 8192 batch (1.07 GB KV; the mixed batch is too large to capture
 # with every section) and scaled by KV bytes, since traffic grows with the KV read.
 TRAFFIC_PROFILE = {
-    "source_sha256": "d04dd3711dc952a1c39f72cc5b3298bb872a90a61fcb9ab0a8dcc42b204f3978",
-    "bytes_per_kv_byte": (1.074384e9 + 3.900160e6) / 1073741824,
+    "source_sha256": "94cc50c584ac7b2cb5b7b6e89cd5e0745ced947ec7599bffa731161613012da0",
+    "bytes_per_kv_byte": (1.074477e9 + 3.813888e6) / 1073741824,
     "workload": "uniform_32x8k_paged (profiles/decode_attn_uniform_32x8k_bf16_full.md)",
 }
 
