@@ -229,6 +229,14 @@ def run_ours(args, rank, world, local_rank):
 
     tail = traced_tail(ws)
 
+    # the same step with the combine folded into the attention launch (one kernel fewer)
+    def fused_step(ev=None):
+        hpa.decode_step(ws, q, k, v, lens, indptr, indices, out, out_lse, ks, vs, tile=b.tile,
+                        stream=stream, fused=True)
+
+    fused_ms = max_over_ranks(timed(fused_step, args.steps, args.warmup, breakdown=False)[0],
+                              world, dev)
+
     # static split-KV comparators through the same kernels (heuristic and best of a sweep)
     comparator = None
     if not args.no_static and rank == 0:
@@ -284,7 +292,7 @@ def run_ours(args, rank, world, local_rank):
                             world, dev)
 
     return dict(b=b, C=C, ms=ms, attn=attn, plan=plan_ms, comb=comb_ms, clocks=clocks, tail=tail,
-                comparator=comparator, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
+                fused_ms=fused_ms, comparator=comparator, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -418,6 +426,8 @@ def main():
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "decode_attn_kernel", "peak_kind": peak_kind + " (hbm_gbs)"},
         "tail": r["tail"],
+        "fused_combine": {"us_per_batch": round(per_batch_us(r["fused_ms"], world), 2),
+                          "speedup_vs_three_calls": round(r["ms"] / r["fused_ms"], 3)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(per_batch_us(r["e2e_ms"], world), 2), "unit": UNIT,
                 "h2d_bytes_per_step": int(r["h2d"]), "d2h_bytes_per_step": int(r["d2h"])},

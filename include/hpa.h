@@ -180,6 +180,34 @@ int hpa_decode_attn_traced(const void *q_dev, const void *k_pool_dev, const void
                            float *partial_lse_dev, uint64_t *trace_dev, hpa_stream_t stream);
 
 /*
+ * hpa_decode_attn_fused -- hpa_decode_attn with the combine folded in (one
+ * launch instead of two).  Same arguments and layouts, plus the combine's
+ * outputs out_dev (bf16 [B][q_len][Hq][d], 8-byte aligned) and out_lse_dev
+ * (fp32 [B][q_len][Hq] or NULL), and arrivals_dev: int32 [B][Hkv]
+ * (hpa_arrivals_elems), zero before the first call.
+ *   - A request with one segment is written straight to out_dev.
+ *   - Otherwise every CTA stores its partial, then counts itself in
+ *     arrivals[r][h] with an atomic add (after a fence); the CTA whose add
+ *     completes the count merges the request's partials for that KV head,
+ *     exactly as hpa_combine does, and resets the counter to zero.  No CTA
+ *     waits for another.
+ * After a call whose map reports a non-zero status, re-zero arrivals_dev
+ * before the next call.  A bad map makes every output NaN, as with
+ * hpa_combine.  This is the fused combine the pages' three-module design
+ * leaves as a later step ("Hy3 Preview AI Infra 推理优化精读笔记", §3.1 step 5:
+ * a combine merges the split-KV results).
+ */
+size_t hpa_arrivals_elems(int32_t B, int32_t Hkv);
+int hpa_decode_attn_fused(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
+                          int32_t kv_dtype, const float *k_scale_dev, const float *v_scale_dev,
+                          int64_t num_pages, const int32_t *page_indptr_dev,
+                          const int32_t *page_indices_dev, int32_t page_size, int32_t B,
+                          int32_t q_len, int32_t Hq, int32_t Hkv, int32_t d, float sm_scale,
+                          void *taskmap_dev, int32_t num_ctas, float *partial_o_dev,
+                          float *partial_lse_dev, void *out_dev, float *out_lse_dev,
+                          int32_t *arrivals_dev, hpa_stream_t stream);
+
+/*
  * hpa_combine -- the Combine kernel ([Notes §3.1] step 5, [HPC-Ops §二.1]).
  * For every (request r, token j, head g) over r's segments s:
  *   M = max_s lse_s,  w_s = exp(lse_s - M),

@@ -69,10 +69,10 @@ struct Smem {
   static constexpr int kMerge = kStages * kStageBytes;     // float[16][kMergeStride]
   static constexpr int kStats = kMerge + MAX_ROWS * kMergeStride * 4;  // m[4][16], l[4][16]
   static constexpr int kQ = kStats + 2 * kConsumerWarps * MAX_ROWS * 4;  // 2 query slots
-  static constexpr int kInfo = kQ + 2 * kQSlotBytes;                      // int4[2]
-  static constexpr int kBars = kInfo + 2 * 16;  // full[kStages] empty[kStages] qfull[2] qempty[2]
+  static constexpr int kInfo = kQ + 2 * kQSlotBytes;                      // int4[2][2]
+  static constexpr int kBars = kInfo + 4 * 16;  // full[kStages] empty[kStages] qfull[2] qempty[2]
   static constexpr int kFlag = kBars + (2 * kStages + 4) * 8;
-  static constexpr int kBytes = kFlag + 16;
+  static constexpr int kBytes = kFlag + 16;  // abort flag, last-arriver flag
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 B
 };
 
@@ -93,7 +93,7 @@ __device__ __forceinline__ SegInfo seg_info(const AttnParams &p, int s, int tile
 }
 
 // ----------------------------------------------------------------------------- producer
-template <int KV>
+template <int KV, bool FUSED>
 __device__ void producer(const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv,
                          uint8_t *smem, int s_begin, int s_end, int tile, int h) {
   using S = Smem<KV>;
@@ -131,8 +131,14 @@ __device__ void producer(const AttnParams &p, const CUtensorMap *tmk, const CUte
             p.q + ((static_cast<int64_t>(f.r) * p.q_len + j) * p.Hq + h * G + g) * HEAD_DIM)[c16];
         *reinterpret_cast<int4 *>(qs + row * kQRowBytes + c16 * 16) = v;
       }
-      if (lane == 0)
-        reinterpret_cast<int4 *>(smem + S::kInfo)[slot] = make_int4(f.r, f.L, f.klo, f.khi);
+      if (lane == 0) {
+        int4 *info = reinterpret_cast<int4 *>(smem + S::kInfo) + 2 * slot;
+        info[0] = make_int4(f.r, f.L, f.klo, f.khi);
+        if (FUSED) {  // fused combine: the request's segment range
+          const int so = p.tm[p.lay.seg_off + f.r];
+          info[1] = make_int4(so, p.tm[p.lay.seg_off + f.r + 1] - so, 0, 0);
+        }
+      }
       mbar_arrive(qfull0 + 8 * slot);  // every lane publishes its own stores
     }
     const int pstart = p.page_indptr[f.r];
@@ -308,8 +314,61 @@ __device__ __forceinline__ int merge_pos(int dd) {
   return (dd & 15) * 8 + (dd >> 4);
 }
 
-// ----------------------------------------------------------------------------- consumer
+__device__ __forceinline__ void store_bf16x4(__nv_bfloat16 *dst, float4 v) {
+  uint2 pk;
+  pk.x = pack_bf16(v.x, v.y);
+  pk.y = pack_bf16(v.z, v.w);
+  *reinterpret_cast<uint2 *>(dst) = pk;
+}
+
+// Fused combine by the last-arriving CTA: log-sum-exp merge of segments
+// [seg_first, seg_first + nseg) of request r for the G * q_len rows of KV head h,
+// read through L2 (other CTAs wrote them), written as the final bf16 output.
 template <int KV>
+__device__ void merge_request(const AttnParams &p, int r, int h, int seg_first, int nseg,
+                              int tid) {
+  const int G = p.G, q_len = p.q_len;
+  const int64_t per_seg = static_cast<int64_t>(q_len) * p.Hq;
+  for (int v = tid; v < p.rows * (HEAD_DIM / 4); v += kConsumerWarps * 32) {
+    const int row = v / (HEAD_DIM / 4), c4 = v % (HEAD_DIM / 4);
+    const int64_t col = static_cast<int64_t>(row / G) * p.Hq + h * G + row % G;
+    float M = -CUDART_INF_F;
+    for (int i = 0; i < nseg; ++i) M = fmaxf(M, __ldcg(p.partial_lse + (seg_first + i) * per_seg + col));
+    const float Mb = M == -CUDART_INF_F ? 0.f : M;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+    float W = 0.f;
+    for (int i0 = 0; i0 < nseg; i0 += 4) {
+      float l[4];
+      float4 o[4];
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i0 + u < nseg) {
+          const int64_t sr = (seg_first + i0 + u) * per_seg + col;
+          l[u] = __ldcg(p.partial_lse + sr);
+          o[u] = __ldcg(reinterpret_cast<const float4 *>(p.partial_o + sr * HEAD_DIM) + c4);
+        }
+#pragma unroll
+      for (int u = 0; u < 4; ++u)
+        if (i0 + u < nseg) {
+          const float wt = expf(l[u] - Mb);
+          acc.x += wt * o[u].x;
+          acc.y += wt * o[u].y;
+          acc.z += wt * o[u].z;
+          acc.w += wt * o[u].w;
+          W += wt;
+        }
+    }
+    const float inv = W > 0.f ? 1.f / W : 0.f;
+    const int64_t orow = (static_cast<int64_t>(r) * per_seg + col) * HEAD_DIM;
+    store_bf16x4(p.out + orow + 4 * c4,
+                 make_float4(acc.x * inv, acc.y * inv, acc.z * inv, acc.w * inv));
+    if (c4 == 0 && p.out_lse != nullptr)
+      p.out_lse[static_cast<int64_t>(r) * per_seg + col] = W > 0.f ? Mb + logf(W) : -CUDART_INF_F;
+  }
+}
+
+// ----------------------------------------------------------------------------- consumer
+template <int KV, bool FUSED>
 __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_end, int tile,
                          int h) {
   using S = Smem<KV>;
@@ -341,7 +400,7 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
     ok = __all_sync(kFull, ok);
     SegInfo f;
     {
-      const int4 inf = reinterpret_cast<const int4 *>(smem + S::kInfo)[slot];
+      const int4 inf = reinterpret_cast<const int4 *>(smem + S::kInfo)[2 * slot];
       f.r = inf.x;
       f.L = inf.y;
       f.klo = inf.z;
@@ -350,6 +409,13 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
       f.pg1 = ok ? (f.khi + PAGE - 1) / PAGE : f.pg0;  // no pages if the wait gave up
     }
     if (ok && f.L < q_len && w == 0 && lane == 0) status_or(p.tm, HPA_STATUS_BAD_SEQLEN);
+    // fused combine: first segment and segment count of this request
+    int seg_first = 0, nseg = 0;
+    if (FUSED) {
+      const int4 inf2 = reinterpret_cast<const int4 *>(smem + S::kInfo)[2 * slot + 1];
+      seg_first = inf2.x;
+      nseg = inf2.y;
+    }
     const int lim_min = f.L - q_len + 1;  // first key hidden from some row
     const int lim0 = v0 ? f.L - q_len + 1 + j0 : f.L;
     const int lim1 = v1 ? f.L - q_len + 1 + j1 : f.L;
@@ -525,10 +591,13 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
       }
     named_barrier(1, kConsumerWarps * 32);
     const int tid = threadIdx.x;
+    // fused combine, single-segment request: this segment is the whole result
+    const bool direct = FUSED && nseg == 1;
     for (int v = tid; v < rows * (HEAD_DIM / 4); v += kConsumerWarps * 32) {
       const int row = v / (HEAD_DIM / 4), c4 = v % (HEAD_DIM / 4);
       const int j = row / G, g = row % G;
-      const int64_t dst = ((static_cast<int64_t>(s) * q_len + j) * p.Hq + h * G + g) * HEAD_DIM;
+      const int64_t dst = ((static_cast<int64_t>(direct ? f.r : s) * q_len + j) * p.Hq + h * G + g) *
+                          HEAD_DIM;
       float *mrow = mbuf + row * kMergeStride;
       float4 val;
       if (KV == HPA_KV_BF16) {
@@ -543,21 +612,42 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
           mrow[pos] = 0.f;
         }
       }
-      reinterpret_cast<float4 *>(p.partial_o + dst)[c4] = val;
+      if (direct)
+        store_bf16x4(p.out + dst + 4 * c4, val);
+      else
+        reinterpret_cast<float4 *>(p.partial_o + dst)[c4] = val;
     }
     if (tid < rows) {
       float M, Lsum;
       row_stats(tid, M, Lsum);
       const int j = tid / G, g = tid % G;
-      p.partial_lse[(static_cast<int64_t>(s) * q_len + j) * p.Hq + h * G + g] =
-          Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -CUDART_INF_F;
+      const float lse = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -CUDART_INF_F;
+      if (!direct)
+        p.partial_lse[(static_cast<int64_t>(s) * q_len + j) * p.Hq + h * G + g] = lse;
+      else if (p.out_lse != nullptr)
+        p.out_lse[(static_cast<int64_t>(f.r) * q_len + j) * p.Hq + h * G + g] = lse;
+    }
+    if (FUSED && !direct) {  // CTA-uniform: all consumer warps take the barriers
+      // Fused combine: count this partial in; the CTA that brings the count to
+      // nseg merges all of the request's partials for this KV head.  Nobody waits:
+      // every other CTA just moves on.
+      __threadfence();  // this CTA's partial stores before its arrival
+      named_barrier(1, kConsumerWarps * 32);
+      volatile int *last = reinterpret_cast<volatile int *>(smem + S::kFlag + 4);
+      if (tid == 0) *last = atomicAdd(p.arrivals + f.r * p.Hkv + h, 1) == nseg - 1;
+      named_barrier(1, kConsumerWarps * 32);
+      if (*last) {
+        __threadfence();
+        merge_request<KV>(p, f.r, h, seg_first, nseg, tid);
+        if (tid == 0) p.arrivals[f.r * p.Hkv + h] = 0;  // ready for the next call
+      }
     }
     named_barrier(1, kConsumerWarps * 32);
   }
 }
 
 // ----------------------------------------------------------------------------- kernel
-template <int KV>
+template <int KV, bool FUSED>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
@@ -566,7 +656,7 @@ __global__ void __launch_bounds__(kThreads, 2)
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
   const int c = blockIdx.x, h = blockIdx.y;
-  __shared__ int hdr[4];  // go, tile, s_begin, s_end -- read once, used by all threads
+  __shared__ int hdr[5];  // go, tile, s_begin, s_end, bad map -- read once, used by all threads
   const uint32_t base = smem_u32(smem);
   unsigned long long *trace =
       p.trace ? p.trace + 4 * (static_cast<int64_t>(h) * p.C + c) : nullptr;
@@ -582,6 +672,7 @@ __global__ void __launch_bounds__(kThreads, 2)
       if (c == 0 && h == 0) status_or(p.tm, HPA_STATUS_MISMATCH);
       go = 0;
     }
+    hdr[4] = !go;
     hdr[1] = tile;
     hdr[2] = go ? tm[p.lay.cta_seg + c] : 0;
     hdr[3] = go ? tm[p.lay.cta_seg + c + 1] : 0;
@@ -607,20 +698,33 @@ __global__ void __launch_bounds__(kThreads, 2)
     trace[3] = smid() | (static_cast<unsigned long long>(hdr[3] - hdr[2]) << 32);
   }
   if (!hdr[0]) {  // bad map, or a partition with no tiles
+    if (FUSED && hdr[4]) {
+      // fused combine on a bad map: NaN outputs, as the combine kernel writes;
+      // CTA (c, h) covers requests c, c + C, ... for the heads of group h
+      const float nan = CUDART_NAN_F;
+      for (int r = c; r < p.B; r += p.C)
+        for (int v = threadIdx.x; v < p.rows * (HEAD_DIM / 4); v += kThreads) {
+          const int row = v / (HEAD_DIM / 4), c4 = v % (HEAD_DIM / 4);
+          const int64_t col = static_cast<int64_t>(row / p.G) * p.Hq + h * p.G + row % p.G;
+          const int64_t orow = static_cast<int64_t>(r) * p.q_len * p.Hq + col;
+          store_bf16x4(p.out + orow * HEAD_DIM + 4 * c4, make_float4(nan, nan, nan, nan));
+          if (c4 == 0 && p.out_lse != nullptr) p.out_lse[orow] = nan;
+        }
+    }
     if (trace && threadIdx.x == 0) trace[2] = globaltimer_ns();
     return;
   }
   const int tile = hdr[1], s_begin = hdr[2], s_end = hdr[3];
 
   if (threadIdx.x >= kConsumerWarps * 32) {
-    producer<KV>(p, &tmk, &tmv, smem, s_begin, s_end, tile, h);
+    producer<KV, FUSED>(p, &tmk, &tmv, smem, s_begin, s_end, tile, h);
   } else {
-    consumer<KV>(p, smem, s_begin, s_end, tile, h);
+    consumer<KV, FUSED>(p, smem, s_begin, s_end, tile, h);
     if (trace && threadIdx.x == 0) trace[2] = globaltimer_ns();  // after the last epilogue
   }
 }
 
-template <int KV>
+template <int KV, bool FUSED>
 cudaError_t launch(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                    cudaStream_t s) {
   static int configured[64] = {0};
@@ -628,8 +732,8 @@ cudaError_t launch(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMa
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(decode_attn_kernel<KV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                             Smem<KV>::kAlloc);
+    e = cudaFuncSetAttribute(decode_attn_kernel<KV, FUSED>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<KV>::kAlloc);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
@@ -643,17 +747,17 @@ cudaError_t launch(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMa
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_attn_kernel<KV>, tmk, tmv, p);
+  return cudaLaunchKernelEx(&cfg, decode_attn_kernel<KV, FUSED>, tmk, tmv, p);
 }
 
 template <int KV>
 int occupancy(int *ctas) {
-  cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<KV>,
+  cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<KV, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Smem<KV>::kAlloc);
   if (e != cudaSuccess) return -1;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, decode_attn_kernel<KV>, kThreads,
-                                                    Smem<KV>::kAlloc);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, decode_attn_kernel<KV, false>,
+                                                    kThreads, Smem<KV>::kAlloc);
   return e == cudaSuccess ? 0 : -1;
 }
 
@@ -661,8 +765,12 @@ int occupancy(int *ctas) {
 
 cudaError_t launch_decode_attn(const AttnParams &p, const CUtensorMap &tmk,
                                const CUtensorMap &tmv, int kv_dtype, cudaStream_t s) {
-  return kv_dtype == HPA_KV_BF16 ? launch<HPA_KV_BF16>(p, tmk, tmv, s)
-                                 : launch<HPA_KV_E4M3>(p, tmk, tmv, s);
+  const bool fused = p.out != nullptr;  // the fused combine is its own instantiation
+  if (kv_dtype == HPA_KV_BF16)
+    return fused ? launch<HPA_KV_BF16, true>(p, tmk, tmv, s)
+                 : launch<HPA_KV_BF16, false>(p, tmk, tmv, s);
+  return fused ? launch<HPA_KV_E4M3, true>(p, tmk, tmv, s)
+               : launch<HPA_KV_E4M3, false>(p, tmk, tmv, s);
 }
 
 int attn_ctas_per_sm(int kv_dtype, int q_len, int *ctas) {

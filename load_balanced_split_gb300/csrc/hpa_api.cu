@@ -174,6 +174,7 @@ static int decode_attn_impl(const void *q_dev, const void *k_pool_dev, const voi
                             int32_t page_size, int32_t B, int32_t q_len, int32_t Hq, int32_t Hkv,
                             int32_t d, float sm_scale, void *taskmap_dev, int32_t num_ctas,
                             float *partial_o_dev, float *partial_lse_dev, uint64_t *trace_dev,
+                            void *out_dev, float *out_lse_dev, int32_t *arrivals_dev,
                             hpa_stream_t stream) {
   if (!q_dev || !k_pool_dev || !v_pool_dev || !page_indptr_dev || !page_indices_dev ||
       !taskmap_dev || !partial_o_dev || !partial_lse_dev)
@@ -204,6 +205,9 @@ static int decode_attn_impl(const void *q_dev, const void *k_pool_dev, const voi
   p.partial_o = partial_o_dev;
   p.partial_lse = partial_lse_dev;
   p.trace = reinterpret_cast<unsigned long long *>(trace_dev);
+  p.out = static_cast<__nv_bfloat16 *>(out_dev);
+  p.out_lse = out_lse_dev;
+  p.arrivals = arrivals_dev;
   p.num_pages = num_pages;
   p.lay = hpa::TaskMapLayout::make(B, num_ctas);
   p.B = B;
@@ -229,7 +233,7 @@ int hpa_decode_attn(const void *q_dev, const void *k_pool_dev, const void *v_poo
   return decode_attn_impl(q_dev, k_pool_dev, v_pool_dev, kv_dtype, k_scale_dev, v_scale_dev,
                           num_pages, page_indptr_dev, page_indices_dev, page_size, B, q_len, Hq,
                           Hkv, d, sm_scale, taskmap_dev, num_ctas, partial_o_dev,
-                          partial_lse_dev, nullptr, stream);
+                          partial_lse_dev, nullptr, nullptr, nullptr, nullptr, stream);
 }
 
 int hpa_decode_attn_traced(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
@@ -244,7 +248,28 @@ int hpa_decode_attn_traced(const void *q_dev, const void *k_pool_dev, const void
   return decode_attn_impl(q_dev, k_pool_dev, v_pool_dev, kv_dtype, k_scale_dev, v_scale_dev,
                           num_pages, page_indptr_dev, page_indices_dev, page_size, B, q_len, Hq,
                           Hkv, d, sm_scale, taskmap_dev, num_ctas, partial_o_dev,
-                          partial_lse_dev, trace_dev, stream);
+                          partial_lse_dev, trace_dev, nullptr, nullptr, nullptr, stream);
+}
+
+size_t hpa_arrivals_elems(int32_t B, int32_t Hkv) {
+  if (B < 1 || B > kMaxB || Hkv < 1 || Hkv > 65535) return 0;
+  return static_cast<size_t>(B) * Hkv;
+}
+
+int hpa_decode_attn_fused(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
+                          int32_t kv_dtype, const float *k_scale_dev, const float *v_scale_dev,
+                          int64_t num_pages, const int32_t *page_indptr_dev,
+                          const int32_t *page_indices_dev, int32_t page_size, int32_t B,
+                          int32_t q_len, int32_t Hq, int32_t Hkv, int32_t d, float sm_scale,
+                          void *taskmap_dev, int32_t num_ctas, float *partial_o_dev,
+                          float *partial_lse_dev, void *out_dev, float *out_lse_dev,
+                          int32_t *arrivals_dev, hpa_stream_t stream) {
+  if (!out_dev || !arrivals_dev) return HPA_ERR_INVALID;
+  if (!aligned(out_dev, 8) || !aligned(arrivals_dev, 4)) return HPA_ERR_ALIGN;
+  return decode_attn_impl(q_dev, k_pool_dev, v_pool_dev, kv_dtype, k_scale_dev, v_scale_dev,
+                          num_pages, page_indptr_dev, page_indices_dev, page_size, B, q_len, Hq,
+                          Hkv, d, sm_scale, taskmap_dev, num_ctas, partial_o_dev,
+                          partial_lse_dev, nullptr, out_dev, out_lse_dev, arrivals_dev, stream);
 }
 
 int hpa_combine(const float *partial_o_dev, const float *partial_lse_dev, void *taskmap_dev,

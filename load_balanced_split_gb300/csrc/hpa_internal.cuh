@@ -47,6 +47,9 @@ struct AttnParams {
   const float *k_scale, *v_scale;
   float *partial_o, *partial_lse;
   unsigned long long *trace;  // optional: 4 words per CTA (entry, go, end, smid | segs << 32)
+  __nv_bfloat16 *out;         // fused combine: final output (nullptr: write partials only)
+  float *out_lse;             // fused combine: final lse (optional)
+  int32_t *arrivals;          // fused combine: [B][Hkv] arrival counters, zero between calls
   int64_t num_pages;
   TaskMapLayout lay;
   int B, C, q_len, Hq, Hkv, G, rows;

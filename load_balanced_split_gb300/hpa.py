@@ -56,6 +56,10 @@ def lib():
                 "hpa_decode_attn_traced": ([P, P, P, I32, P, P, I64, P, P, I32, I32, I32, I32,
                                             I32, I32, F, P, I32, P, P, P, P], ctypes.c_int),
                 "hpa_combine": ([P, P, P, I32, I32, I32, I32, I32, P, P, P], ctypes.c_int),
+                "hpa_arrivals_elems": ([I32, I32], SZ),
+                "hpa_decode_attn_fused": ([P, P, P, I32, P, P, I64, P, P, I32, I32, I32, I32,
+                                           I32, I32, F, P, I32, P, P, P, P, P, P],
+                                          ctypes.c_int),
                 "hpa_selftest_wait_timeout": ([P, I64, P], ctypes.c_int),
                 "hpa_decode_attn_combine_noalloc": ([P, P, P, I32, P, P, I64, P, P, I32, I32,
                                                      I32, I32, I32, I32, F, P, I32, P, P, P],
@@ -227,6 +231,36 @@ def trace_summary(trace, num_ctas: int, Hkv: int) -> dict:
             "sms_used": len(per_sm)}
 
 
+def hpa_arrivals_elems(B: int, Hkv: int) -> int:
+    return int(lib().hpa_arrivals_elems(B, Hkv))
+
+
+def hpa_decode_attn_fused(q, k_pool, v_pool, page_indptr, page_indices, taskmap, num_ctas: int,
+                          partial_o, partial_lse, out, arrivals, out_lse=None, k_scale=None,
+                          v_scale=None, sm_scale: float | None = None, stream=None):
+    """Attention with the combine folded in; arrivals: int32 [B * Hkv], zero between calls."""
+    _dev(q, "q", torch.bfloat16)
+    _dev(out, "out", torch.bfloat16)
+    _dev(arrivals, "arrivals", torch.int32)
+    if out_lse is not None:
+        _dev(out_lse, "out_lse", torch.float32)
+    B, q_len, Hq, d = q.shape
+    kv = KV_BF16 if k_pool.dtype == torch.bfloat16 else KV_E4M3
+    P, Hkv, page, _ = k_pool.shape
+    need = hpa_max_segments(B, num_ctas) * q_len * Hq
+    if partial_lse.numel() < need or partial_o.numel() < need * d:
+        raise HpaError("partial buffers too small: need (B + num_ctas - 1) segments")
+    if arrivals.numel() < B * Hkv or tuple(out.shape) != (B, q_len, Hq, d):
+        raise HpaError("arrivals or out has the wrong size")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d)
+    _check(lib().hpa_decode_attn_fused(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), kv, _ptr(k_scale), _ptr(v_scale), P,
+        _ptr(page_indptr), _ptr(page_indices), page, B, q_len, Hq, Hkv, d, float(sm_scale),
+        _ptr(taskmap), num_ctas, _ptr(partial_o), _ptr(partial_lse), _ptr(out), _ptr(out_lse),
+        _ptr(arrivals), _stream(stream)), "hpa_decode_attn_fused")
+
+
 def hpa_combine(partial_o, partial_lse, taskmap, num_ctas: int, out, out_lse=None, stream=None):
     """out bf16 [B][q_len][Hq][d]; out_lse fp32 [B][q_len][Hq] or None."""
     _dev(partial_o, "partial_o", torch.float32)
@@ -282,7 +316,7 @@ class Workspace:
     library itself never allocates.
     """
 
-    def __init__(self, B, q_len, Hq, d, num_ctas=None, splits=None, device="cuda"):
+    def __init__(self, B, q_len, Hq, d, num_ctas=None, splits=None, device="cuda", Hkv=8):
         if splits is not None:
             self.num_ctas = hpa_static_num_ctas(B, splits)
             nbytes = hpa_static_taskmap_bytes(B, splits)
@@ -297,6 +331,7 @@ class Workspace:
         self.taskmap = torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device=device)
         self.partial_o = torch.empty(cap * q_len * Hq * d, dtype=torch.float32, device=device)
         self.partial_lse = torch.empty(cap * q_len * Hq, dtype=torch.float32, device=device)
+        self.arrivals = torch.zeros(B * Hkv, dtype=torch.int32, device=device)  # fused combine
 
     def plan(self, seq_lens, tile=512, stream=None):
         if self.splits is not None:
@@ -310,10 +345,18 @@ class Workspace:
 
 
 def decode_step(ws: Workspace, q, k_pool, v_pool, seq_lens, page_indptr, page_indices, out,
-                out_lse=None, k_scale=None, v_scale=None, tile=512, plan=True, stream=None):
-    """plan (optional) -> split-KV attention -> combine, all enqueued on one stream."""
+                out_lse=None, k_scale=None, v_scale=None, tile=512, plan=True, stream=None,
+                fused=False):
+    """plan (optional) -> split-KV attention -> combine, all enqueued on one stream.
+
+    fused=True runs the attention kernel with the combine folded in (one launch)."""
     if plan:
         ws.plan(seq_lens, tile, stream)
+    if fused:
+        hpa_decode_attn_fused(q, k_pool, v_pool, page_indptr, page_indices, ws.taskmap,
+                              ws.num_ctas, ws.partial_o, ws.partial_lse, out, ws.arrivals,
+                              out_lse, k_scale, v_scale, stream=stream)
+        return
     hpa_decode_attn(q, k_pool, v_pool, page_indptr, page_indices, ws.taskmap, ws.num_ctas,
                     ws.partial_o, ws.partial_lse, k_scale, v_scale, stream=stream)
     hpa_combine(ws.partial_o, ws.partial_lse, ws.taskmap, ws.num_ctas, out, out_lse, stream)

@@ -78,8 +78,9 @@ def num_ctas_for(b) -> int:
                                     else hpa.KV_E4M3)
 
 
-def run_gpu(b, num_ctas=None, splits=None, tile=512, db=None):
-    """plan -> attention -> combine on the GPU.  Returns host numpy results."""
+def run_gpu(b, num_ctas=None, splits=None, tile=512, db=None, fused=False):
+    """plan -> attention -> combine on the GPU (fused: one attention launch with the
+    combine folded in).  Returns host numpy results."""
     db = db or DeviceBatch(b)
     if splits is None and num_ctas is None:
         num_ctas = num_ctas_for(b)
@@ -89,8 +90,10 @@ def run_gpu(b, num_ctas=None, splits=None, tile=512, db=None):
     out = torch.empty((b.B, b.q_len, b.Hq, b.d), dtype=torch.bfloat16, device="cuda")
     out_lse = torch.empty((b.B, b.q_len, b.Hq), dtype=torch.float32, device="cuda")
     hpa.decode_step(ws, db.q, db.k, db.v, db.lens, db.indptr, db.indices, out, out_lse,
-                    db.ks, db.vs, tile=tile)
+                    db.ks, db.vs, tile=tile, fused=fused)
     torch.cuda.synchronize()
+    if fused:
+        assert int(ws.arrivals.abs().sum().item()) == 0, "arrival counters not reset"
     tm = decode_taskmap(ws.taskmap.cpu().numpy(), b.B, ws.num_ctas)
     S = tm["S"]
     po = ws.partial_o.view(-1, b.q_len, b.Hq, b.d)[:S].cpu().numpy().astype(np.float64)

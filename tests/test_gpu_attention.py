@@ -18,8 +18,9 @@ from gpu_helpers import (DeviceBatch, assert_close, assert_lse_close, expect_tas
 pytestmark = pytest.mark.gpu
 
 
-def check(b, num_ctas=None, splits=None, tile=512, db=None, check_partials=True):
-    g = run_gpu(b, num_ctas=num_ctas, splits=splits, tile=tile, db=db)
+def check(b, num_ctas=None, splits=None, tile=512, db=None, check_partials=True, fused=False):
+    g = run_gpu(b, num_ctas=num_ctas, splits=splits, tile=tile, db=db, fused=fused)
+    check_partials = check_partials and not fused  # fused: single-segment partials skipped
     if splits is None:
         ref_plan = oracle.plan(b.seq_lens, tile, g["num_ctas"])
     else:
@@ -179,3 +180,48 @@ def test_traced_call_matches_and_records_every_cta():
     assert int((t[:, 3] >> 32).sum()) == S * b.Hkv      # every segment, once per KV head
     summ = hpa.trace_summary(trace, C, b.Hkv)
     assert summ["span_us"] > 0 and 0 < summ["sm_busy_frac"] <= 1.0
+
+
+# ----------------------------------------------------------------------------- fused combine
+FUSED_CASES = [
+    dict(lens=[2, 63, 64, 65, 511, 512, 513, 1000, 3333, 4113], q_len=1, kv="bf16", C=5),
+    dict(lens=[2, 63, 64, 65, 511, 512, 513, 1000, 3333, 4113], q_len=2, kv="e4m3", C=23),
+    dict(lens=[100, 700, 30], q_len=1, kv="bf16", C=40),          # surplus partitions
+    dict(lens=[196608 // 8], q_len=1, kv="bf16", C=38),           # one request over 38 CTAs
+    dict(lens=[3000, 9000, 64 * 7, 2], q_len=2, kv="bf16", C=9),
+]
+
+
+@pytest.mark.parametrize("case", range(len(FUSED_CASES)))
+def test_fused_combine(case):
+    c = FUSED_CASES[case]
+    b = W.make_batch(c["lens"], q_len=c["q_len"], kv_dtype=c["kv"], seed=60 + case)
+    check(b, num_ctas=c["C"], fused=True)
+
+
+@pytest.mark.parametrize("splits", [1, 3])
+def test_fused_combine_static_plan(splits):
+    b = W.make_batch([100, 2000, 9000, 1], seed=70 + splits)
+    check(b, splits=splits, fused=True)
+
+
+def test_fused_combine_reused_map_and_bad_map():
+    b = W.make_batch([3000, 40, 12000], seed=80)
+    db = DeviceBatch(b)
+    ws = hpa.Workspace(b.B, 1, 64, 128, num_ctas=7)
+    ws.plan(db.lens)
+    ref, _ = oracle.attention(b)
+    for layer in range(3):
+        out = torch.empty((b.B, 1, 64, 128), dtype=torch.bfloat16, device="cuda")
+        hpa.decode_step(ws, db.q, db.k, db.v, db.lens, db.indptr, db.indices, out, plan=False,
+                        fused=True)
+        assert_close(out.float().cpu().numpy(), ref, "bf16")
+    assert int(ws.arrivals.abs().sum().item()) == 0
+    bad = db.lens.clone()
+    bad[1] = 0
+    ws.plan(bad)
+    out = torch.zeros((b.B, 1, 64, 128), dtype=torch.bfloat16, device="cuda")
+    hpa.decode_step(ws, db.q, db.k, db.v, bad, db.indptr, db.indices, out, plan=False,
+                    fused=True)
+    torch.cuda.synchronize()
+    assert torch.isnan(out.float()).all()

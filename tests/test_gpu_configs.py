@@ -44,4 +44,8 @@ def test_config_full_size(cfg):
                          gs["capacity"])
     assert_close(gs["out"], out, b.kv_dtype, "static out")
     assert_lse_close(gs["lse"], lse, "static out_lse")
+    # the fused combine through one attention launch
+    gf = run_gpu(b, db=db, fused=True)
+    assert_close(gf["out"], out, b.kv_dtype, "fused out")
+    assert_lse_close(gf["lse"], lse, "fused out_lse")
     print("cfg%d %s: max|d| %.3g, max rel %.3g" % (cfg, b.name, e_abs, e_rel))
