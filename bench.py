@@ -42,8 +42,8 @@ UNIT = "us/batch"
 # Taken on the uniform 32 x 8192 batch (1.07 GB KV; the mixed batch is too large to capture
 # with every section) and scaled by KV bytes, since traffic grows with the KV read.
 TRAFFIC_PROFILE = {
-    "source_sha256": "94cc50c584ac7b2cb5b7b6e89cd5e0745ced947ec7599bffa731161613012da0",
-    "bytes_per_kv_byte": (1.074477e9 + 3.813888e6) / 1073741824,
+    "source_sha256": "c2091614876c4003c0a5ec3777f69120861211c3a2c2bec27911ab901f3e0771",
+    "bytes_per_kv_byte": (1074369536 + 3426560) / 1073741824,
     "workload": "uniform_32x8k_paged (profiles/decode_attn_uniform_32x8k_bf16_full.md)",
 }
 
@@ -142,6 +142,8 @@ def run_ours(args, rank, world, local_rank):
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
     b = W.make_config(args.config, seed=args.seed + rank, max_requests=args.requests)
+    if args.tile:
+        b.tile = args.tile
     kv = hpa.KV_BF16 if b.kv_dtype == "bf16" else hpa.KV_E4M3
     C = args.num_ctas or b.num_ctas or hpa.hpa_default_num_ctas(b.Hkv, b.q_len, kv)
     q = b.q.to(dev)
@@ -366,6 +368,7 @@ def main():
     ap.add_argument("--impl", default="ours", choices=["ours", "reference"])
     ap.add_argument("--requests", type=int, default=None,
                     help="keep only the first N requests of the workload (smaller case)")
+    ap.add_argument("--tile", type=int, default=None, help="tile size in tokens (default 512)")
     ap.add_argument("--num-ctas", type=int, default=None,
                     help="partitions per KV head (default: the device default)")
     ap.add_argument("--no-static", action="store_true", help="skip the static comparators")
