@@ -155,7 +155,8 @@ def run_ours(args, rank, world, local_rank):
     lens = torch.from_numpy(b.seq_lens).to(dev)
     indptr = torch.from_numpy(b.page_indptr).to(dev)
     indices = torch.from_numpy(b.page_indices).to(dev)
-    ws = hpa.Workspace(b.B, b.q_len, b.Hq, b.d, num_ctas=C, device=dev)
+    ws = hpa.Workspace(b.B, b.q_len, b.Hq, b.d, num_ctas=C, device=dev,
+                       weighted=args.plan == "weighted")
     out = torch.empty((b.B, b.q_len, b.Hq, b.d), dtype=torch.bfloat16, device=dev)
     out_lse = torch.empty((b.B, b.q_len, b.Hq), dtype=torch.float32, device=dev)
     stream = torch.cuda.Stream(device=dev)
@@ -369,6 +370,8 @@ def main():
     ap.add_argument("--requests", type=int, default=None,
                     help="keep only the first N requests of the workload (smaller case)")
     ap.add_argument("--tile", type=int, default=None, help="tile size in tokens (default 512)")
+    ap.add_argument("--plan", default="tiles", choices=["tiles", "weighted"],
+                    help="tile budgets (the pages' method) or the token-weighted variant")
     ap.add_argument("--num-ctas", type=int, default=None,
                     help="partitions per KV head (default: the device default)")
     ap.add_argument("--no-static", action="store_true", help="skip the static comparators")
@@ -417,7 +420,7 @@ def main():
                    "batch": int(b.B),
                    "kv_tokens": int(b.seq_lens.sum()), "q_len": b.q_len, "heads": "64q/8kv",
                    "head_dim": 128, "page": 64, "tile": b.tile, "num_ctas": int(r["C"]),
-                   "kv_dtype": b.kv_dtype, "kv_bytes": int(kv_bytes),
+                   "kv_dtype": b.kv_dtype, "kv_bytes": int(kv_bytes), "plan": args.plan,
                    "l2": "inputs larger than L2 (%.2f GB KV), no flush" % (kv_bytes / 1e9),
                    "parallelism": "dp%d replicas" % world, "seed": args.seed},
         "kv_gbs": round(kv_bytes / (r["ms"] * 1e-3) / 1e9, 1),

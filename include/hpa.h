@@ -75,7 +75,7 @@ typedef struct CUstream_st *hpa_stream_t;
  * hpa_plan_static and read by hpa_decode_attn and hpa_combine.  One map
  * serves every layer of a decode step ([HPC-Ops §二.1]).  Layout (int32 words):
  *   [0,16)  header: T, base, rem, C, B, S (segments), status, tile, kind
- *           (0 dynamic / 1 static), splits, S_cap, 0...
+ *           (0 dynamic / 1 static / 2 token-weighted), splits, S_cap, 0...
  *   lens[B]            copy of the sequence lengths
  *   cu_tiles[B+1]      exclusive running sum of tiles per request
  *   cta_begin[C+1]     first stream tile of each partition
@@ -119,6 +119,21 @@ int32_t hpa_default_num_ctas(int32_t Hkv, int32_t q_len, int32_t kv_dtype);
  */
 int hpa_plan(const int32_t *seq_lens_dev, int32_t B, int32_t tile, int32_t num_ctas,
              void *taskmap_dev, size_t taskmap_bytes, hpa_stream_t stream);
+
+/*
+ * hpa_plan_weighted -- the token-weighted variant of hpa_plan (a reading the
+ * pages leave open: a partial last tile costs its fill, not a whole tile).
+ * Same stream, same contiguous partitions and map format (kind 2), with
+ * budgets in keys: with K = sum L_r, P_t the keys before stream tile t and w_t
+ * the keys in it, tile t goes to partition floor(C (2 P_t + w_t) / (2 K)) --
+ * the partition whose equal share of the key stream holds the tile's middle
+ * key.  Header words base / rem hold K / C and K % C.  Sizes as hpa_plan;
+ * requires (B + C) small enough for the plan's 40 KB shared-memory staging
+ * (about B + C <= 3400), else HPA_ERR_UNSUPPORTED; K > 2^40 sets
+ * HPA_STATUS_OVERFLOW.
+ */
+int hpa_plan_weighted(const int32_t *seq_lens_dev, int32_t B, int32_t tile, int32_t num_ctas,
+                      void *taskmap_dev, size_t taskmap_bytes, hpa_stream_t stream);
 
 /*
  * hpa_plan_static -- the static split-KV comparator the pages contrast the

@@ -389,7 +389,7 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
   const int G = p.G, rows = p.rows, q_len = p.q_len;
   const int row0 = r8, row1 = r8 + 8;
   const bool v0 = row0 < rows, v1 = row1 < rows;
-  const int j0 = row0 / G, g0 = row0 % G, j1 = row1 / G, g1 = row1 % G;
+  const int j0 = row0 / G, j1 = row1 / G;
 
   const uint32_t qfull0 = empty0 + 8 * S::kStages, qempty0 = qfull0 + 16;
   int stage = 0;

@@ -155,6 +155,18 @@ int hpa_plan(const int32_t *seq_lens_dev, int32_t B, int32_t tile, int32_t num_c
   return e == cudaSuccess ? HPA_OK : cuda_fail(e);
 }
 
+int hpa_plan_weighted(const int32_t *seq_lens_dev, int32_t B, int32_t tile, int32_t num_ctas,
+                      void *taskmap_dev, size_t taskmap_bytes, hpa_stream_t stream) {
+  const int64_t s_cap = int64_t(B) + num_ctas - 1;
+  int rc = check_plan_args(seq_lens_dev, B, tile, num_ctas, taskmap_dev, taskmap_bytes, s_cap);
+  if (rc != HPA_OK) return rc;
+  if (hpa::plan_stage_bytes(B, num_ctas, 2) > hpa::kPlanStageLimit) return HPA_ERR_UNSUPPORTED;
+  cudaError_t e = hpa::launch_plan(seq_lens_dev, B, tile, num_ctas, 2, 0,
+                                   static_cast<int32_t *>(taskmap_dev), s_cap,
+                                   reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? HPA_OK : cuda_fail(e);
+}
+
 int hpa_plan_static(const int32_t *seq_lens_dev, int32_t B, int32_t tile, int32_t splits,
                     void *taskmap_dev, size_t taskmap_bytes, hpa_stream_t stream) {
   const int32_t C = hpa_static_num_ctas(B, splits);

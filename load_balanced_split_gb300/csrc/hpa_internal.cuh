@@ -56,6 +56,8 @@ struct AttnParams {
   float scale_log2;  // sm_scale * log2(e)
 };
 
+constexpr size_t kPlanStageLimit = 40 * 1024;  // shared memory the plan kernel may stage in
+size_t plan_stage_bytes(int B, int C, int kind);
 cudaError_t launch_plan(const int32_t *seq_lens, int B, int tile, int C, int kind, int splits,
                         int32_t *tm, int64_t s_cap, cudaStream_t s);
 cudaError_t launch_combine(const float *po, const float *plse, int32_t *tm, int B, int C,

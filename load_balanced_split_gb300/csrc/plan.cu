@@ -10,6 +10,10 @@
 // Static map (the fixed split-KV the same §3.1 contrasts it with): request r
 //   is cut into min(splits, n_r) near-equal chunks, partition r*splits+s owns
 //   chunk s.
+// Token-weighted map (kind 2): the same contiguous partitions of the tile
+//   stream, with budgets in keys: tile t (keys P_t before it, w_t in it) goes
+//   to partition floor(C (2 P_t + w_t) / (2 K)), K the total key count, so a
+//   partial last tile weighs its fill.
 #include <climits>
 
 #include "hpa_internal.cuh"
@@ -67,31 +71,42 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
   int4 *seg = reinterpret_cast<int4 *>(tm + lay.segs);
   // Working copies of cu_tiles and cta_begin: in shared memory when they fit
   // (the binary searches below then cost shared- instead of L2 latency).
-  extern __shared__ int32_t stage_buf[];
+  extern __shared__ __align__(8) int32_t stage_buf[];
   int32_t *cu = staged ? stage_buf : cu_g;
   int32_t *cb = staged ? stage_buf + B + 1 : cb_g;
+  // keys before each request (token-weighted map only; always staged then)
+  long long *kc = reinterpret_cast<long long *>(stage_buf + ((B + 1 + C + 1 + 1) & ~1));
   __shared__ long long wbuf[kPlanThreads / 32];
   __shared__ int s_bad;
   const int tid = threadIdx.x;
   if (tid == 0) s_bad = 0;
   __syncthreads();
 
-  // a1 + a2: tile counts and their running sum
-  long long carry = 0, total;
+  // a1 + a2: tile counts and their running sum (and, for kind 2, the key prefix)
+  long long carry = 0, kcarry = 0, total;
   for (int base = 0; base < B; base += kPlanThreads) {
     const int i = base + tid;
-    long long n = 0;
+    long long n = 0, keys = 0;
     if (i < B) {
       const int L = lens_in[i];
       lens[i] = L;
       if (L < 1) atomicOr(&s_bad, HPA_STATUS_BAD_SEQLEN);
-      else n = (L - 1) / tile + 1;
+      else n = (L - 1) / tile + 1, keys = L;
     }
     const long long incl = block_scan(n, wbuf, total);
     if (i < B) cu[i + 1] = cu_g[i + 1] = static_cast<int32_t>(carry + incl);
     carry += total;
+    if (kind == 2) {
+      const long long kincl = block_scan(keys, wbuf, total);
+      if (i < B) kc[i + 1] = kcarry + kincl;
+      kcarry += total;
+    }
   }
-  if (tid == 0) cu[0] = cu_g[0] = 0;
+  if (tid == 0) {
+    cu[0] = cu_g[0] = 0;
+    if (kind == 2) kc[0] = 0;
+  }
+  if (kind == 2 && kcarry > (1ll << 40) && tid == 0) atomicOr(&s_bad, HPA_STATUS_OVERFLOW);
   if (carry > INT_MAX && tid == 0) atomicOr(&s_bad, HPA_STATUS_OVERFLOW);
   __syncthreads();
   const long long T = carry;
@@ -116,6 +131,30 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
     long long begin;
     if (kind == 0) {
       begin = c * tbase + (c < trem ? c : trem);
+    } else if (kind == 2) {
+      // first tile whose doubled middle key 2 P_t + w_t reaches X = ceil(2 K c / C)
+      const long long K = kcarry;
+      const long long X = (2 * K * c + C - 1) / C;
+      // last tile of request r has 2 P + w = kc[r] + kc[r+1] + (n_r - 1) * tile
+      int lo = 0, hi = B;  // smallest r with that >= X (B if none)
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        const long long e = kc[mid] + kc[mid + 1] + static_cast<long long>(cu[mid + 1] - cu[mid] - 1) * tile;
+        if (e >= X) hi = mid;
+        else lo = mid + 1;
+      }
+      if (c == 0) {
+        begin = 0;
+      } else if (lo == B) {
+        begin = T;
+      } else {
+        const int n = cu[lo + 1] - cu[lo];
+        // full tile i: 2 P + w = 2 kc[r] + (2 i + 1) tile >= X  <=>  i >= (X - 2 kc - tile) / (2 tile)
+        const long long num = X - 2 * kc[lo] - tile;
+        long long i0 = num <= 0 ? 0 : (num + 2 * tile - 1) / (2 * tile);
+        if (i0 > n - 1) i0 = n - 1;  // otherwise the last tile (its middle reaches X)
+        begin = cu[lo] + i0;
+      }
     } else {
       const int r = c / splits, s = c % splits;
       const int n = cu[r + 1] - cu[r];
@@ -174,8 +213,14 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
     so[B] = static_cast<int32_t>(S);
     for (int w = TM_SCAP + 1; w < TM_HEADER_WORDS; ++w) tm[w] = 0;
     tm[TM_T] = static_cast<int32_t>(T);
-    tm[TM_BASE] = kind == 0 ? static_cast<int32_t>(tbase) : -1;
-    tm[TM_REM] = kind == 0 ? static_cast<int32_t>(trem) : -1;
+    if (kind == 2) {  // key budget: K / C (clamped) and K % C
+      const long long kb = kcarry / C;
+      tm[TM_BASE] = static_cast<int32_t>(kb > INT_MAX ? INT_MAX : kb);
+      tm[TM_REM] = static_cast<int32_t>(kcarry % C);
+    } else {
+      tm[TM_BASE] = kind == 0 ? static_cast<int32_t>(tbase) : -1;
+      tm[TM_REM] = kind == 0 ? static_cast<int32_t>(trem) : -1;
+    }
     tm[TM_C] = C;
     tm[TM_B] = B;
     tm[TM_S] = static_cast<int32_t>(S);
@@ -189,11 +234,18 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
 
 }  // namespace
 
+size_t plan_stage_bytes(int B, int C, int kind) {
+  size_t words = (static_cast<size_t>(B) + 1 + C + 1 + 1) & ~static_cast<size_t>(1);
+  if (kind == 2) words += 2 * (static_cast<size_t>(B) + 1);  // int64 key prefix
+  return words * sizeof(int32_t);
+}
+
 cudaError_t launch_plan(const int32_t *seq_lens, int B, int tile, int C, int kind, int splits,
                         int32_t *tm, int64_t s_cap, cudaStream_t s) {
-  // cu_tiles and cta_begin are staged in shared memory when they fit in 40 KB
-  const size_t stage_bytes = (static_cast<size_t>(B) + 1 + C + 1) * sizeof(int32_t);
-  const int staged = stage_bytes <= 40 * 1024;
+  // cu_tiles and cta_begin (and the key prefix) are staged in shared memory when
+  // they fit in 40 KB; the token-weighted map requires it (checked by the caller)
+  const size_t stage_bytes = plan_stage_bytes(B, C, kind);
+  const int staged = stage_bytes <= kPlanStageLimit;
   plan_kernel<<<1, kPlanThreads, staged ? stage_bytes : 0, s>>>(seq_lens, B, tile, C, kind,
                                                                   splits, tm, s_cap, staged);
   return cudaGetLastError();

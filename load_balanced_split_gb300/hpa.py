@@ -51,6 +51,7 @@ def lib():
                 "hpa_default_num_ctas": ([I32, I32, I32], I32),
                 "hpa_plan": ([P, I32, I32, I32, P, SZ, P], ctypes.c_int),
                 "hpa_plan_static": ([P, I32, I32, I32, P, SZ, P], ctypes.c_int),
+                "hpa_plan_weighted": ([P, I32, I32, I32, P, SZ, P], ctypes.c_int),
                 "hpa_decode_attn": ([P, P, P, I32, P, P, I64, P, P, I32, I32, I32, I32, I32,
                                      I32, F, P, I32, P, P, P], ctypes.c_int),
                 "hpa_decode_attn_traced": ([P, P, P, I32, P, P, I64, P, P, I32, I32, I32, I32,
@@ -132,6 +133,14 @@ def hpa_plan(seq_lens, tile: int, num_ctas: int, taskmap, stream=None):
     _dev(taskmap, "taskmap")
     _check(lib().hpa_plan(_ptr(seq_lens), seq_lens.numel(), tile, num_ctas, _ptr(taskmap),
                           taskmap.numel() * taskmap.element_size(), _stream(stream)), "hpa_plan")
+
+
+def hpa_plan_weighted(seq_lens, tile: int, num_ctas: int, taskmap, stream=None):
+    _dev(seq_lens, "seq_lens", torch.int32)
+    _dev(taskmap, "taskmap")
+    _check(lib().hpa_plan_weighted(_ptr(seq_lens), seq_lens.numel(), tile, num_ctas,
+                                   _ptr(taskmap), taskmap.numel() * taskmap.element_size(),
+                                   _stream(stream)), "hpa_plan_weighted")
 
 
 def hpa_plan_static(seq_lens, tile: int, splits: int, taskmap, stream=None):
@@ -316,7 +325,8 @@ class Workspace:
     library itself never allocates.
     """
 
-    def __init__(self, B, q_len, Hq, d, num_ctas=None, splits=None, device="cuda", Hkv=8):
+    def __init__(self, B, q_len, Hq, d, num_ctas=None, splits=None, device="cuda", Hkv=8,
+                 weighted=False):
         if splits is not None:
             self.num_ctas = hpa_static_num_ctas(B, splits)
             nbytes = hpa_static_taskmap_bytes(B, splits)
@@ -327,6 +337,7 @@ class Workspace:
         if nbytes == 0 or cap == 0:
             raise HpaError("workspace size query failed")
         self.splits = splits
+        self.weighted = weighted
         self.capacity = cap
         self.taskmap = torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device=device)
         self.partial_o = torch.empty(cap * q_len * Hq * d, dtype=torch.float32, device=device)
@@ -336,6 +347,8 @@ class Workspace:
     def plan(self, seq_lens, tile=512, stream=None):
         if self.splits is not None:
             hpa_plan_static(seq_lens, tile, self.splits, self.taskmap, stream)
+        elif self.weighted:
+            hpa_plan_weighted(seq_lens, tile, self.num_ctas, self.taskmap, stream)
         else:
             hpa_plan(seq_lens, tile, self.num_ctas, self.taskmap, stream)
 

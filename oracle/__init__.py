@@ -25,7 +25,7 @@ import threading
 import numpy as np
 
 from . import scheduler  # noqa: F401
-from .scheduler import plan, plan_static, segment_key_ranges  # noqa: F401
+from .scheduler import plan, plan_static, plan_weighted, segment_key_ranges  # noqa: F401
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _BUILD = os.path.join(_HERE, "_build")

@@ -22,6 +22,9 @@ Readings adopted where the pages are silent, ambiguous or at odds:
   5. a partial last tile counts as one whole tile of budget;
   6. when there are more CTAs than tiles, the surplus CTAs get no work.
 
+Token-weighted variant (plan_weighted): the same stream and contiguous
+partitions, with budgets counted in keys instead of tiles.
+
 Static split-KV comparator ([Notes §3.1] 问题; the pages do not give its
 rule): request r is cut into min(S, n_r) contiguous chunks of near-equal tile
 counts (the first n_r % chunks get one more); CTA c = r * S + s owns chunk s of
@@ -89,6 +92,48 @@ def plan(seq_lens, tile, num_ctas):
         cta_begin.append(cta_begin[-1] + load[c])
     return _assemble(seq_lens, tile, num_ctas, counts, cu, cta_begin, segs, base, rem,
                      kind=0, splits=0)
+
+
+def plan_weighted(seq_lens, tile, num_ctas):
+    """Token-weighted variant: tiles are shared out by the keys they hold.
+
+    A partial last tile weighs its fill, not one whole tile (a reading the
+    pages leave open).  With K the total number of keys, P_t the keys before
+    stream tile t and w_t the keys in it, tile t goes to the partition whose
+    equal share of the key stream holds the tile's middle key:
+    floor(C * (2 P_t + w_t) / (2 K)).  Walking the stream, partition c takes
+    tiles while their middles fall within its share [c K / C, (c+1) K / C).
+    Each partition's key load is within one tile of K / C.
+    """
+    if tile <= 0 or num_ctas <= 0:
+        raise ValueError("tile and num_ctas must be positive")
+    counts = tile_counts(seq_lens, tile)
+    cu = stream_offsets(counts)
+    K = sum(int(L) for L in seq_lens)
+    owner, before = [], 0                  # before = keys ahead of the current tile
+    for r, L in enumerate(seq_lens):
+        for i in range(counts[r]):
+            w = min(tile, int(L) - i * tile)
+            owner.append((num_ctas * (2 * before + w)) // (2 * K))
+            before += w
+    segs = []
+    for r, n in enumerate(counts):
+        for i in range(n):
+            c = owner[cu[r] + i]
+            if segs and segs[-1][0] == r and segs[-1][3] == c:
+                segs[-1][2] = i + 1
+            else:
+                segs.append([r, i, i + 1, c])
+    cta_begin = []
+    t = 0
+    for c in range(num_ctas):
+        while t < len(owner) and owner[t] < c:
+            t += 1
+        cta_begin.append(t)
+    cta_begin.append(cu[-1])
+    base = min(K // num_ctas, 2**31 - 1)
+    return _assemble(seq_lens, tile, num_ctas, counts, cu, cta_begin, segs, base,
+                     K % num_ctas, kind=2, splits=0)
 
 
 def plan_static(seq_lens, tile, splits):

@@ -39,7 +39,7 @@ def expect_taskmap_equal(gpu: dict, ref: dict, s_cap: int):
     """Bit-exact comparison of every field of the decoded map with the oracle plan."""
     for k in ("T", "C", "B", "S", "tile", "kind", "splits"):
         assert gpu[k] == ref[k], (k, gpu[k], ref[k])
-    if ref["kind"] == 0:
+    if ref["kind"] in (0, 2):        # tile budget, or key budget for the token-weighted map
         assert (gpu["base"], gpu["rem"]) == (ref["base"], ref["rem"])
     else:
         assert (gpu["base"], gpu["rem"]) == (-1, -1)
@@ -78,13 +78,14 @@ def num_ctas_for(b) -> int:
                                     else hpa.KV_E4M3)
 
 
-def run_gpu(b, num_ctas=None, splits=None, tile=512, db=None, fused=False):
+def run_gpu(b, num_ctas=None, splits=None, tile=512, db=None, fused=False, weighted=False):
     """plan -> attention -> combine on the GPU (fused: one attention launch with the
     combine folded in).  Returns host numpy results."""
     db = db or DeviceBatch(b)
     if splits is None and num_ctas is None:
         num_ctas = num_ctas_for(b)
-    ws = hpa.Workspace(b.B, b.q_len, b.Hq, b.d, num_ctas=num_ctas, splits=splits)
+    ws = hpa.Workspace(b.B, b.q_len, b.Hq, b.d, num_ctas=num_ctas, splits=splits,
+                       weighted=weighted)
     ws.partial_o.fill_(float("nan"))
     ws.partial_lse.fill_(float("nan"))
     out = torch.empty((b.B, b.q_len, b.Hq, b.d), dtype=torch.bfloat16, device="cuda")

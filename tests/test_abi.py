@@ -120,3 +120,11 @@ def test_selftest_argument_checks():
     assert L.hpa_selftest_wait_timeout(None, 10**6, None) == -1
     assert L.hpa_selftest_wait_timeout(FAKE, 10, None) == -1
     assert L.hpa_selftest_wait_timeout(FAKE + 2, 10**6, None) == -4
+
+
+def test_weighted_plan_size_limit():
+    L = hpa.lib()
+    B, C = 3000, 2000                            # too large to stage the key prefix
+    nb = hpa.hpa_taskmap_bytes(B, C)
+    assert L.hpa_plan_weighted(FAKE, B, 512, C, FAKE, nb, None) == -2
+    assert L.hpa_plan_weighted(None, 3, 512, 4, FAKE, hpa.hpa_taskmap_bytes(3, 4), None) == -1

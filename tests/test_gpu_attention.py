@@ -18,10 +18,14 @@ from gpu_helpers import (DeviceBatch, assert_close, assert_lse_close, expect_tas
 pytestmark = pytest.mark.gpu
 
 
-def check(b, num_ctas=None, splits=None, tile=512, db=None, check_partials=True, fused=False):
-    g = run_gpu(b, num_ctas=num_ctas, splits=splits, tile=tile, db=db, fused=fused)
+def check(b, num_ctas=None, splits=None, tile=512, db=None, check_partials=True, fused=False,
+          weighted=False):
+    g = run_gpu(b, num_ctas=num_ctas, splits=splits, tile=tile, db=db, fused=fused,
+                weighted=weighted)
     check_partials = check_partials and not fused  # fused: single-segment partials skipped
-    if splits is None:
+    if weighted:
+        ref_plan = oracle.plan_weighted(b.seq_lens, tile, g["num_ctas"])
+    elif splits is None:
         ref_plan = oracle.plan(b.seq_lens, tile, g["num_ctas"])
     else:
         ref_plan = oracle.plan_static(b.seq_lens, tile, splits)
@@ -225,3 +229,37 @@ def test_fused_combine_reused_map_and_bad_map():
                     fused=True)
     torch.cuda.synchronize()
     assert torch.isnan(out.float()).all()
+
+
+def test_three_calls_capture_in_a_cuda_graph():
+    """plan -> attention -> combine recorded once in a CUDA graph and replayed on new lengths."""
+    b = W.make_batch([3000, 40, 12000, 700], seed=90)
+    db = DeviceBatch(b)
+    ws = hpa.Workspace(b.B, 1, 64, 128, num_ctas=11)
+    out = torch.empty((b.B, 1, 64, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((b.B, 1, 64), dtype=torch.float32, device="cuda")
+    lens = db.lens.clone()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):                       # warm up (resolves TMA descriptors etc.)
+        hpa.decode_step(ws, db.q, db.k, db.v, lens, db.indptr, db.indices, out, lse, stream=s)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        hpa.decode_step(ws, db.q, db.k, db.v, lens, db.indptr, db.indices, out, lse, stream=s)
+    for shorten in (0, 17):                          # replay; the second time with new lengths
+        b2 = W.make_batch([3000, 40, 12000, 700], seed=90)
+        b2.seq_lens = b.seq_lens - shorten
+        lens.copy_(torch.from_numpy(b2.seq_lens))
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        ref, ref_lse = oracle.attention(b2)
+        assert_close(out.float().cpu().numpy(), ref, "bf16")
+        assert_lse_close(lse.cpu().numpy(), ref_lse)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+@pytest.mark.parametrize("q_len", [1, 2])
+def test_weighted_plan_same_kernels(kv, q_len):
+    b = W.make_batch([2, 63, 513, 1000, 3333, 4113, 600], q_len=q_len, kv_dtype=kv, seed=95)
+    check(b, num_ctas=7, weighted=True)

@@ -10,7 +10,7 @@ from gpu_helpers import decode_taskmap, expect_taskmap_equal
 pytestmark = pytest.mark.gpu
 
 
-def gpu_plan(lens, tile, C=None, splits=None):
+def gpu_plan(lens, tile, C=None, splits=None, weighted=False):
     lens_d = torch.tensor(np.asarray(lens, dtype=np.int32), device="cuda")
     B = len(lens)
     if splits is None:
@@ -19,7 +19,9 @@ def gpu_plan(lens, tile, C=None, splits=None):
         nbytes, CC = hpa.hpa_static_taskmap_bytes(B, splits), hpa.hpa_static_num_ctas(B, splits)
         cap = CC
     tm = torch.full(((nbytes + 3) // 4,), 12345, dtype=torch.int32, device="cuda")
-    if splits is None:
+    if splits is None and weighted:
+        hpa.hpa_plan_weighted(lens_d, tile, C, tm)
+    elif splits is None:
         hpa.hpa_plan(lens_d, tile, C, tm)
     else:
         hpa.hpa_plan_static(lens_d, tile, splits, tm)
@@ -82,3 +84,20 @@ def test_replan_clears_status():
     lens_d[1] = 7
     ws.plan(lens_d)
     assert ws.status() == 0
+
+
+@pytest.mark.parametrize("seed", range(12))
+def test_weighted(seed):
+    rng = np.random.default_rng(900 + seed)
+    B = int(rng.integers(1, 1500))
+    tile = int(rng.choice([64, 256, 512]))
+    lens = rng.integers(1, 100000 if tile >= 256 else 20000, size=B)
+    C = int(rng.integers(1, 1200))
+    g, cap = gpu_plan(lens, tile, C, weighted=True)
+    expect_taskmap_equal(g, oracle.plan_weighted(lens, tile, C), cap)
+
+
+def test_weighted_worked_example_and_partial_tiles():
+    for lens, C in (([1024, 5120, 2048], 4), ([513] * 4, 2), ([1025, 1], 2), ([1], 5)):
+        g, cap = gpu_plan(lens, 512, C, weighted=True)
+        expect_taskmap_equal(g, oracle.plan_weighted(lens, 512, C), cap)

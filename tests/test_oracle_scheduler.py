@@ -185,3 +185,53 @@ def test_static_plan(seed):
 def test_static_one_split_is_one_segment_per_request():
     p = oracle.plan_static([1024, 5120, 2048], 512, 1)
     assert p["segs"].tolist() == [[0, 0, 2, 0], [1, 0, 10, 1], [2, 0, 4, 2]]
+
+
+# ----------------------------------------------------------------------------- token-weighted
+def _key_loads(p, lens, tile):
+    loads = np.zeros(p["C"], dtype=np.int64)
+    for r, lo, hi, c in p["segs"]:
+        loads[c] += min(int(hi) * tile, int(lens[r])) - int(lo) * tile
+    return loads
+
+
+@pytest.mark.parametrize("seed", range(20))
+def test_weighted_plan_invariants(seed):
+    rng = np.random.default_rng(500 + seed)
+    B = int(rng.integers(1, 30))
+    lens = rng.integers(1, 30000, size=B)
+    tile = int(rng.choice([64, 256, 512]))
+    C = int(rng.integers(1, 60))
+    p = oracle.plan_weighted(lens, tile, C)
+    assert p["kind"] == 2
+    owner = _owner_from_segments(p)
+    assert (owner >= 0).all() and (np.diff(owner) >= 0).all()
+    assert p["S"] <= B + C - 1
+    K = int(np.sum(lens))
+    loads = _key_loads(p, lens, tile)
+    assert loads.sum() == K
+    # every partition is within one tile of the equal share K / C
+    assert (np.abs(loads - K / C) <= tile).all()
+
+
+def test_weighted_plan_counts_a_partial_tile_by_its_fill():
+    # 4 requests of 513 keys: 8 tiles, four of them hold a single key.  By tiles,
+    # 2 partitions take 4 tiles each; by keys, each takes about 1026 keys.
+    lens = [513] * 4
+    pt = oracle.plan(lens, 512, 2)
+    pw = oracle.plan_weighted(lens, 512, 2)
+    assert list(_key_loads(pt, lens, 512)) == [1026, 1026]
+    assert list(_key_loads(pw, lens, 512)) == [1026, 1026]
+    lens = [1024 + 1, 1]                       # tiles of 512, 512, 1 and 1 keys
+    pt = oracle.plan(lens, 512, 2)             # 2 tiles each: 1024 vs 2 keys
+    pw = oracle.plan_weighted(lens, 512, 2)    # the key shares: 512 vs 514
+    assert list(_key_loads(pt, lens, 512)) == [1024, 2]
+    assert list(_key_loads(pw, lens, 512)) == [512, 514]
+
+
+@pytest.mark.parametrize("T,C", [(7, 3), (8, 3), (10, 4), (12, 5), (1, 4), (100, 7)])
+def test_weighted_equals_tile_budgets_when_tiles_are_full(T, C):
+    lens = [512] * T
+    lt = sorted(scheduler.cta_loads(oracle.plan(lens, 512, C)))
+    lw = sorted(scheduler.cta_loads(oracle.plan_weighted(lens, 512, C)))
+    assert lt == lw                            # the same multiset of loads, max - min <= 1
