@@ -145,7 +145,8 @@ def run_ours(args, rank, world, local_rank):
     if args.tile:
         b.tile = args.tile
     kv = hpa.KV_BF16 if b.kv_dtype == "bf16" else hpa.KV_E4M3
-    C = args.num_ctas or b.num_ctas or hpa.hpa_default_num_ctas(b.Hkv, b.q_len, kv)
+    C = args.num_ctas or b.num_ctas or hpa.hpa_default_num_ctas(b.Hkv, b.q_len, kv, b.Hq)
+    groups = (b.Hq // b.Hkv * b.q_len + 15) // 16  # query-row groups per (partition, head)
     q = b.q.to(dev)
     k, v = b.k_pool.to(dev), b.v_pool.to(dev)
     ks = vs = None
@@ -220,14 +221,14 @@ def run_ours(args, rank, world, local_rank):
 
     def traced_tail(w, reps=3):
         """Per-CTA timestamps of the attention kernel (outside the timed region)."""
-        tr = torch.zeros(4 * w.num_ctas * b.Hkv, dtype=torch.int64, device=dev)
+        tr = torch.zeros(4 * w.num_ctas * b.Hkv * groups, dtype=torch.int64, device=dev)
         out_t = None
         for _ in range(reps):
             w.plan(lens, b.tile, stream)
             hpa.hpa_decode_attn_traced(q, k, v, indptr, indices, w.taskmap, w.num_ctas,
                                        w.partial_o, w.partial_lse, tr, ks, vs, stream=stream)
             torch.cuda.synchronize(dev)
-            out_t = hpa.trace_summary(tr, w.num_ctas, b.Hkv)
+            out_t = hpa.trace_summary(tr, w.num_ctas, b.Hkv, groups)
         return {k2: round(v2, 3) if isinstance(v2, float) else v2 for k2, v2 in out_t.items()}
 
     tail = traced_tail(ws)

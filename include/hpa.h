@@ -101,9 +101,10 @@ int32_t hpa_static_num_ctas(int32_t B, int32_t splits);
 size_t hpa_static_taskmap_bytes(int32_t B, int32_t splits);
 
 /* Partitions per KV head that fill the current device once: SMs x resident
- * attention CTAs per SM / Hkv (at least 1).  Returns <= 0 on a CUDA error or
- * an unsupported (q_len, kv_dtype). */
-int32_t hpa_default_num_ctas(int32_t Hkv, int32_t q_len, int32_t kv_dtype);
+ * attention CTAs per SM / (Hkv x query-row groups), at least 1, where a group
+ * is 16 of the G * q_len query rows of a KV head.  Returns <= 0 on a CUDA
+ * error or unsupported arguments. */
+int32_t hpa_default_num_ctas(int32_t Hq, int32_t Hkv, int32_t q_len, int32_t kv_dtype);
 
 /*
  * hpa_plan -- the Task Assign step ([Notes §3.1] steps 1-4, [HPC-Ops §二.1],
@@ -148,11 +149,13 @@ int hpa_plan_static(const int32_t *seq_lens_dev, int32_t B, int32_t tile, int32_
 
 /*
  * hpa_decode_attn -- the split-KV attention kernel ([Notes §3.1] steps 4-5).
- * Grid num_ctas x Hkv; the CTA of (partition c, KV head h) walks c's
- * segments in order and, for each, computes over the segment's keys
+ * Grid num_ctas x Hkv x ceil(G q_len / 16); the CTA of (partition c, KV
+ * head h, row group z) walks c's segments in order and, for each, computes
+ * over the segment's keys
  *   s = sm_scale * q . k,  m = max s,  l = sum exp(s - m),  o = sum exp(s - m) v / l
- * for the G = Hq / Hkv query heads of h and every query token j (token j
- * of the q_len new ones sees keys [0, L_r - q_len + 1 + j)), and writes
+ * for query rows [16 z, 16 z + 16) of the G * q_len rows (row j * G + g:
+ * query head g of the G = Hq / Hkv heads of h, token j of the q_len new ones,
+ * which sees keys [0, L_r - q_len + 1 + j)), and writes
  *   partial_o[seg][j][head][d] = o,  partial_lse[seg][j][head] = m + ln l
  * (natural log; -inf and o = 0 for a row that sees no key of the segment).
  *
@@ -162,8 +165,9 @@ int hpa_plan_static(const int32_t *seq_lens_dev, int32_t B, int32_t tile, int32_
  * k_scale_dev, v_scale_dev: fp32 [Hkv] for HPA_KV_E4M3, ignored for bf16.
  * page_indptr_dev: int32 [B+1]; page_indices_dev: int32; key i of request r
  *               is slot i % page_size of page page_indices[page_indptr[r] + i / page_size].
- * Supported: d == 128, page_size == 64, Hq % Hkv == 0, (Hq / Hkv) * q_len <= 16,
- *               num_pages * Hkv < 2^31.
+ * Supported: d == 128, page_size == 64, Hq % Hkv == 0, (Hq / Hkv) * q_len <= 64,
+ *               num_pages * Hkv < 2^31.  Row groups past the first re-read the
+ *               pages (through L2 when they run together).
  * taskmap_dev:  a map from hpa_plan / hpa_plan_static for these B and num_ctas.
  * partial_o_dev: fp32, >= (B + num_ctas - 1) * q_len * Hq * d, 16-byte aligned (one
  *               row per segment; no map has more than B + num_ctas - 1 segments);
@@ -184,7 +188,8 @@ int hpa_decode_attn(const void *q_dev, const void *k_pool_dev, const void *v_poo
  * was stored, and (smid | segments << 32).  Used to measure SM busy time and
  * the tail idle of the last CTA (the pages watch "attention kernel tail idle",
  * "Hy3 Preview AI Infra 推理优化精读笔记", §3.1 对我们的启发).  trace_dev: device,
- * 8-byte aligned, >= 4 * num_ctas * Hkv words.
+ * 8-byte aligned, >= 4 * num_ctas * Hkv * row groups words, CTA (c, h, z) at
+ * word 4 * ((z * Hkv + h) * num_ctas + c).
  */
 int hpa_decode_attn_traced(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
                            int32_t kv_dtype, const float *k_scale_dev, const float *v_scale_dev,
@@ -198,11 +203,11 @@ int hpa_decode_attn_traced(const void *q_dev, const void *k_pool_dev, const void
  * hpa_decode_attn_fused -- hpa_decode_attn with the combine folded in (one
  * launch instead of two).  Same arguments and layouts, plus the combine's
  * outputs out_dev (bf16 [B][q_len][Hq][d], 8-byte aligned) and out_lse_dev
- * (fp32 [B][q_len][Hq] or NULL), and arrivals_dev: int32 [B][Hkv]
+ * (fp32 [B][q_len][Hq] or NULL), and arrivals_dev: int32 [B][Hkv][row groups]
  * (hpa_arrivals_elems), zero before the first call.
  *   - A request with one segment is written straight to out_dev.
  *   - Otherwise every CTA stores its partial, then counts itself in
- *     arrivals[r][h] with an atomic add (after a fence); the CTA whose add
+ *     arrivals[r][h][z] with an atomic add (after a fence); the CTA whose add
  *     completes the count merges the request's partials for that KV head,
  *     exactly as hpa_combine does, and resets the counter to zero.  No CTA
  *     waits for another.
@@ -212,7 +217,7 @@ int hpa_decode_attn_traced(const void *q_dev, const void *k_pool_dev, const void
  * leaves as a later step ("Hy3 Preview AI Infra 推理优化精读笔记", §3.1 step 5:
  * a combine merges the split-KV results).
  */
-size_t hpa_arrivals_elems(int32_t B, int32_t Hkv);
+size_t hpa_arrivals_elems(int32_t B, int32_t Hq, int32_t Hkv, int32_t q_len);
 int hpa_decode_attn_fused(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
                           int32_t kv_dtype, const float *k_scale_dev, const float *v_scale_dev,
                           int64_t num_pages, const int32_t *page_indptr_dev,

@@ -76,6 +76,14 @@ struct Smem {
   static constexpr int kAlloc = kBytes + 1024;  // room to align the base to 1024 B
 };
 
+// Query rows are handled in groups of 16 (one m16 MMA tile): CTA z of a
+// (partition, head) pair takes rows [16 z, 16 z + 16) of the G * q_len rows,
+// so MTP with more draft tokens (up to 64 rows) reuses the same kernel.
+__device__ __forceinline__ int row_base() { return MAX_ROWS * static_cast<int>(blockIdx.z); }
+__device__ __forceinline__ int group_rows(const AttnParams &p) {
+  return min(MAX_ROWS, p.rows - row_base());
+}
+
 struct SegInfo {
   int r, L, klo, khi, pg0, pg1;
 };
@@ -124,9 +132,9 @@ __device__ void producer(const AttnParams &p, const CUtensorMap *tmk, const CUte
         break;
       }
       uint8_t *qs = smem + S::kQ + slot * kQSlotBytes;
-      const int G = p.G;
-      for (int ch = lane; ch < p.rows * 16; ch += 32) {  // 16-byte chunks of 256-byte rows
-        const int row = ch >> 4, c16 = ch & 15, j = row / G, g = row % G;
+      const int G = p.G, rb = row_base();
+      for (int ch = lane; ch < group_rows(p) * 16; ch += 32) {  // 16-B chunks of 256-B rows
+        const int row = ch >> 4, c16 = ch & 15, j = (rb + row) / G, g = (rb + row) % G;
         const int4 v = reinterpret_cast<const int4 *>(
             p.q + ((static_cast<int64_t>(f.r) * p.q_len + j) * p.Hq + h * G + g) * HEAD_DIM)[c16];
         *reinterpret_cast<int4 *>(qs + row * kQRowBytes + c16 * 16) = v;
@@ -327,10 +335,10 @@ __device__ __forceinline__ void store_bf16x4(__nv_bfloat16 *dst, float4 v) {
 template <int KV>
 __device__ void merge_request(const AttnParams &p, int r, int h, int seg_first, int nseg,
                               int tid) {
-  const int G = p.G, q_len = p.q_len;
+  const int G = p.G, q_len = p.q_len, rb = row_base();
   const int64_t per_seg = static_cast<int64_t>(q_len) * p.Hq;
-  for (int v = tid; v < p.rows * (HEAD_DIM / 4); v += kConsumerWarps * 32) {
-    const int row = v / (HEAD_DIM / 4), c4 = v % (HEAD_DIM / 4);
+  for (int v = tid; v < group_rows(p) * (HEAD_DIM / 4); v += kConsumerWarps * 32) {
+    const int row = rb + v / (HEAD_DIM / 4), c4 = v % (HEAD_DIM / 4);
     const int64_t col = static_cast<int64_t>(row / G) * p.Hq + h * G + row % G;
     float M = -CUDART_INF_F;
     for (int i = 0; i < nseg; ++i) M = fmaxf(M, __ldcg(p.partial_lse + (seg_first + i) * per_seg + col));
@@ -386,10 +394,11 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
     sl2 *= p.k_scale[h];
     vsc = p.v_scale[h];
   }
-  const int G = p.G, rows = p.rows, q_len = p.q_len;
+  // rows of this CTA's group: local index row, global query row rb + row
+  const int G = p.G, rows = group_rows(p), q_len = p.q_len, rb = row_base();
   const int row0 = r8, row1 = r8 + 8;
   const bool v0 = row0 < rows, v1 = row1 < rows;
-  const int j0 = row0 / G, j1 = row1 / G;
+  const int j0 = (rb + row0) / G, j1 = (rb + row1) / G;
 
   const uint32_t qfull0 = empty0 + 8 * S::kStages, qempty0 = qfull0 + 16;
   int stage = 0;
@@ -595,7 +604,7 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
     const bool direct = FUSED && nseg == 1;
     for (int v = tid; v < rows * (HEAD_DIM / 4); v += kConsumerWarps * 32) {
       const int row = v / (HEAD_DIM / 4), c4 = v % (HEAD_DIM / 4);
-      const int j = row / G, g = row % G;
+      const int j = (rb + row) / G, g = (rb + row) % G;
       const int64_t dst = ((static_cast<int64_t>(direct ? f.r : s) * q_len + j) * p.Hq + h * G + g) *
                           HEAD_DIM;
       float *mrow = mbuf + row * kMergeStride;
@@ -620,7 +629,7 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
     if (tid < rows) {
       float M, Lsum;
       row_stats(tid, M, Lsum);
-      const int j = tid / G, g = tid % G;
+      const int j = (rb + tid) / G, g = (rb + tid) % G;
       const float lse = Lsum > 0.f ? (M + log2f(Lsum)) * 0.69314718055994531f : -CUDART_INF_F;
       if (!direct)
         p.partial_lse[(static_cast<int64_t>(s) * q_len + j) * p.Hq + h * G + g] = lse;
@@ -634,12 +643,13 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
       __threadfence();  // this CTA's partial stores before its arrival
       named_barrier(1, kConsumerWarps * 32);
       volatile int *last = reinterpret_cast<volatile int *>(smem + S::kFlag + 4);
-      if (tid == 0) *last = atomicAdd(p.arrivals + f.r * p.Hkv + h, 1) == nseg - 1;
+      int32_t *counter = p.arrivals + (static_cast<int64_t>(f.r) * p.Hkv + h) * gridDim.z + blockIdx.z;
+      if (tid == 0) *last = atomicAdd(counter, 1) == nseg - 1;
       named_barrier(1, kConsumerWarps * 32);
       if (*last) {
         __threadfence();
         merge_request<KV>(p, f.r, h, seg_first, nseg, tid);
-        if (tid == 0) p.arrivals[f.r * p.Hkv + h] = 0;  // ready for the next call
+        if (tid == 0) *counter = 0;  // ready for the next call
       }
     }
     named_barrier(1, kConsumerWarps * 32);
@@ -659,7 +669,8 @@ __global__ void __launch_bounds__(kThreads, 2)
   __shared__ int hdr[5];  // go, tile, s_begin, s_end, bad map -- read once, used by all threads
   const uint32_t base = smem_u32(smem);
   unsigned long long *trace =
-      p.trace ? p.trace + 4 * (static_cast<int64_t>(h) * p.C + c) : nullptr;
+      p.trace ? p.trace + 4 * ((static_cast<int64_t>(blockIdx.z) * p.Hkv + h) * p.C + c)
+              : nullptr;
   if (trace && threadIdx.x == 0) trace[0] = globaltimer_ns();
   // Nothing above this line reads memory that an earlier kernel writes: with
   // programmatic dependent launch the prologue overlaps the previous kernel.
@@ -703,8 +714,8 @@ __global__ void __launch_bounds__(kThreads, 2)
       // CTA (c, h) covers requests c, c + C, ... for the heads of group h
       const float nan = CUDART_NAN_F;
       for (int r = c; r < p.B; r += p.C)
-        for (int v = threadIdx.x; v < p.rows * (HEAD_DIM / 4); v += kThreads) {
-          const int row = v / (HEAD_DIM / 4), c4 = v % (HEAD_DIM / 4);
+        for (int v = threadIdx.x; v < group_rows(p) * (HEAD_DIM / 4); v += kThreads) {
+          const int row = row_base() + v / (HEAD_DIM / 4), c4 = v % (HEAD_DIM / 4);
           const int64_t col = static_cast<int64_t>(row / p.G) * p.Hq + h * p.G + row % p.G;
           const int64_t orow = static_cast<int64_t>(r) * p.q_len * p.Hq + col;
           store_bf16x4(p.out + orow * HEAD_DIM + 4 * c4, make_float4(nan, nan, nan, nan));
@@ -738,7 +749,7 @@ cudaError_t launch(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMa
     configured[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.C, p.Hkv);
+  cfg.gridDim = dim3(p.C, p.Hkv, (p.rows + MAX_ROWS - 1) / MAX_ROWS);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Smem<KV>::kAlloc;
   cfg.stream = s;

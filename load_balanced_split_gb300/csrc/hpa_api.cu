@@ -130,8 +130,10 @@ size_t hpa_static_taskmap_bytes(int32_t B, int32_t splits) {
   return static_cast<size_t>(taskmap_words(B, C, C)) * 4;
 }
 
-int32_t hpa_default_num_ctas(int32_t Hkv, int32_t q_len, int32_t kv_dtype) {
-  if (Hkv < 1 || q_len < 1 || (kv_dtype != HPA_KV_BF16 && kv_dtype != HPA_KV_E4M3)) return -1;
+int32_t hpa_default_num_ctas(int32_t Hq, int32_t Hkv, int32_t q_len, int32_t kv_dtype) {
+  if (Hkv < 1 || Hq < Hkv || Hq % Hkv != 0 || q_len < 1 ||
+      (kv_dtype != HPA_KV_BF16 && kv_dtype != HPA_KV_E4M3))
+    return -1;
   int dev = 0, sms = 0, per_sm = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
@@ -140,7 +142,9 @@ int32_t hpa_default_num_ctas(int32_t Hkv, int32_t q_len, int32_t kv_dtype) {
     return -1;
   }
   if (hpa::attn_ctas_per_sm(kv_dtype, q_len, &per_sm) != 0 || per_sm < 1) return -1;
-  const int c = sms * per_sm / Hkv;
+  // one CTA per (partition, KV head, group of 16 query rows)
+  const int groups = ((Hq / Hkv) * q_len + hpa::MAX_ROWS - 1) / hpa::MAX_ROWS;
+  const int c = sms * per_sm / (Hkv * groups);
   return c < 1 ? 1 : c;
 }
 
@@ -197,7 +201,7 @@ static int decode_attn_impl(const void *q_dev, const void *k_pool_dev, const voi
       Hkv < 1 || Hkv > 65535 || num_pages < 1 || !std::isfinite(sm_scale))
     return HPA_ERR_INVALID;
   if (d != hpa::HEAD_DIM || page_size != hpa::PAGE || Hq % Hkv != 0 ||
-      (Hq / Hkv) * q_len > hpa::MAX_ROWS)
+      int64_t(Hq / Hkv) * q_len > hpa::MAX_ROWS_TOTAL)
     return HPA_ERR_UNSUPPORTED;
   if (num_pages * Hkv > INT_MAX) return HPA_ERR_UNSUPPORTED;
   if (!aligned(q_dev, 16) || !aligned(k_pool_dev, 16) || !aligned(v_pool_dev, 16) ||
@@ -263,9 +267,11 @@ int hpa_decode_attn_traced(const void *q_dev, const void *k_pool_dev, const void
                           partial_lse_dev, trace_dev, nullptr, nullptr, nullptr, stream);
 }
 
-size_t hpa_arrivals_elems(int32_t B, int32_t Hkv) {
-  if (B < 1 || B > kMaxB || Hkv < 1 || Hkv > 65535) return 0;
-  return static_cast<size_t>(B) * Hkv;
+size_t hpa_arrivals_elems(int32_t B, int32_t Hq, int32_t Hkv, int32_t q_len) {
+  if (B < 1 || B > kMaxB || Hkv < 1 || Hkv > 65535 || Hq < Hkv || Hq % Hkv || q_len < 1)
+    return 0;
+  const int64_t groups = (int64_t(Hq / Hkv) * q_len + hpa::MAX_ROWS - 1) / hpa::MAX_ROWS;
+  return static_cast<size_t>(B) * Hkv * groups;
 }
 
 int hpa_decode_attn_fused(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,

@@ -37,7 +37,8 @@ struct TaskMapLayout {
 
 constexpr int PAGE = 64;       // tokens per KV page
 constexpr int HEAD_DIM = 128;  // d
-constexpr int MAX_ROWS = 16;   // G * q_len rows per KV head (one m16 MMA tile)
+constexpr int MAX_ROWS = 16;   // query rows per CTA (one m16 MMA tile)
+constexpr int MAX_ROWS_TOTAL = 64;  // G * q_len rows per KV head, in groups of 16
 
 // ----------------------------------------------------------------------------- launch blocks
 struct AttnParams {

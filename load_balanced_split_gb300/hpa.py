@@ -48,7 +48,7 @@ def lib():
                 "hpa_max_segments": ([I32, I32], I32),
                 "hpa_static_num_ctas": ([I32, I32], I32),
                 "hpa_static_taskmap_bytes": ([I32, I32], SZ),
-                "hpa_default_num_ctas": ([I32, I32, I32], I32),
+                "hpa_default_num_ctas": ([I32, I32, I32, I32], I32),
                 "hpa_plan": ([P, I32, I32, I32, P, SZ, P], ctypes.c_int),
                 "hpa_plan_static": ([P, I32, I32, I32, P, SZ, P], ctypes.c_int),
                 "hpa_plan_weighted": ([P, I32, I32, I32, P, SZ, P], ctypes.c_int),
@@ -57,7 +57,7 @@ def lib():
                 "hpa_decode_attn_traced": ([P, P, P, I32, P, P, I64, P, P, I32, I32, I32, I32,
                                             I32, I32, F, P, I32, P, P, P, P], ctypes.c_int),
                 "hpa_combine": ([P, P, P, I32, I32, I32, I32, I32, P, P, P], ctypes.c_int),
-                "hpa_arrivals_elems": ([I32, I32], SZ),
+                "hpa_arrivals_elems": ([I32, I32, I32, I32], SZ),
                 "hpa_decode_attn_fused": ([P, P, P, I32, P, P, I64, P, P, I32, I32, I32, I32,
                                            I32, I32, F, P, I32, P, P, P, P, P, P],
                                           ctypes.c_int),
@@ -120,8 +120,8 @@ def hpa_static_taskmap_bytes(B: int, splits: int) -> int:
     return int(lib().hpa_static_taskmap_bytes(B, splits))
 
 
-def hpa_default_num_ctas(Hkv: int, q_len: int, kv_dtype: int) -> int:
-    c = int(lib().hpa_default_num_ctas(Hkv, q_len, kv_dtype))
+def hpa_default_num_ctas(Hkv: int, q_len: int, kv_dtype: int, Hq: int = 64) -> int:
+    c = int(lib().hpa_default_num_ctas(Hq, Hkv, q_len, kv_dtype))
     if c <= 0:
         raise HpaError("hpa_default_num_ctas failed (cudaError %d)" % lib().hpa_last_cuda_error())
     return c
@@ -197,7 +197,8 @@ def hpa_decode_attn_traced(q, k_pool, v_pool, page_indptr, page_indices, taskmap
     B, q_len, Hq, d = q.shape
     kv = KV_BF16 if k_pool.dtype == torch.bfloat16 else KV_E4M3
     P, Hkv, page, _ = k_pool.shape
-    if trace.numel() < 4 * num_ctas * Hkv:
+    groups = (Hq // Hkv * q_len + 15) // 16
+    if trace.numel() < 4 * num_ctas * Hkv * groups:
         raise HpaError("trace buffer too small")
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(d)
@@ -208,10 +209,10 @@ def hpa_decode_attn_traced(q, k_pool, v_pool, page_indptr, page_indices, taskmap
         _stream(stream)), "hpa_decode_attn_traced")
 
 
-def trace_summary(trace, num_ctas: int, Hkv: int) -> dict:
+def trace_summary(trace, num_ctas: int, Hkv: int, groups: int = 1) -> dict:
     """SM busy and tail figures from a hpa_decode_attn_traced buffer (host-side arithmetic)."""
     import numpy as np
-    t = trace.view(-1, 4).cpu().numpy().astype(np.int64)[:num_ctas * Hkv]
+    t = trace.view(-1, 4).cpu().numpy().astype(np.int64)[:num_ctas * Hkv * groups]
     entry, go, end, info = t[:, 0], t[:, 1], t[:, 2], t[:, 3]
     sm = info & 0xffffffff
     busy = t[(info >> 32) > 0]
@@ -240,14 +241,15 @@ def trace_summary(trace, num_ctas: int, Hkv: int) -> dict:
             "sms_used": len(per_sm)}
 
 
-def hpa_arrivals_elems(B: int, Hkv: int) -> int:
-    return int(lib().hpa_arrivals_elems(B, Hkv))
+def hpa_arrivals_elems(B: int, Hq: int, Hkv: int, q_len: int) -> int:
+    return int(lib().hpa_arrivals_elems(B, Hq, Hkv, q_len))
 
 
 def hpa_decode_attn_fused(q, k_pool, v_pool, page_indptr, page_indices, taskmap, num_ctas: int,
                           partial_o, partial_lse, out, arrivals, out_lse=None, k_scale=None,
                           v_scale=None, sm_scale: float | None = None, stream=None):
-    """Attention with the combine folded in; arrivals: int32 [B * Hkv], zero between calls."""
+    """Attention with the combine folded in; arrivals: int32, hpa_arrivals_elems(B, Hq, Hkv,
+    q_len) elements, zero between calls."""
     _dev(q, "q", torch.bfloat16)
     _dev(out, "out", torch.bfloat16)
     _dev(arrivals, "arrivals", torch.int32)
@@ -259,7 +261,8 @@ def hpa_decode_attn_fused(q, k_pool, v_pool, page_indptr, page_indices, taskmap,
     need = hpa_max_segments(B, num_ctas) * q_len * Hq
     if partial_lse.numel() < need or partial_o.numel() < need * d:
         raise HpaError("partial buffers too small: need (B + num_ctas - 1) segments")
-    if arrivals.numel() < B * Hkv or tuple(out.shape) != (B, q_len, Hq, d):
+    if arrivals.numel() < hpa_arrivals_elems(B, Hq, Hkv, q_len) or \
+            tuple(out.shape) != (B, q_len, Hq, d):
         raise HpaError("arrivals or out has the wrong size")
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(d)
@@ -342,7 +345,8 @@ class Workspace:
         self.taskmap = torch.zeros((nbytes + 3) // 4, dtype=torch.int32, device=device)
         self.partial_o = torch.empty(cap * q_len * Hq * d, dtype=torch.float32, device=device)
         self.partial_lse = torch.empty(cap * q_len * Hq, dtype=torch.float32, device=device)
-        self.arrivals = torch.zeros(B * Hkv, dtype=torch.int32, device=device)  # fused combine
+        self.arrivals = torch.zeros(hpa_arrivals_elems(B, Hq, Hkv, q_len), dtype=torch.int32,
+                                    device=device)  # fused combine
 
     def plan(self, seq_lens, tile=512, stream=None):
         if self.splits is not None:

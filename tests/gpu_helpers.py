@@ -75,7 +75,7 @@ def num_ctas_for(b) -> int:
     if b.num_ctas is not None:
         return b.num_ctas
     return hpa.hpa_default_num_ctas(b.Hkv, b.q_len, hpa.KV_BF16 if b.kv_dtype == "bf16"
-                                    else hpa.KV_E4M3)
+                                    else hpa.KV_E4M3, b.Hq)
 
 
 def run_gpu(b, num_ctas=None, splits=None, tile=512, db=None, fused=False, weighted=False):

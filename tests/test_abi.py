@@ -96,7 +96,7 @@ def test_attention_argument_checks():
     assert call(d=64) == -2
     assert call(page=32) == -2
     assert call(Hq=60) == -2                      # Hq not a multiple of Hkv
-    assert call(q_len=3) == -2                    # 8 * 3 rows > 16
+    assert call(q_len=9) == -2                    # 8 * 9 rows > 64
     assert call(P=1 << 29) == -2                  # page*head index beyond int32
     assert call(k=FAKE + 8) == -4
     assert call(po=FAKE + 4) == -4

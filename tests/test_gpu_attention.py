@@ -263,3 +263,17 @@ def test_three_calls_capture_in_a_cuda_graph():
 def test_weighted_plan_same_kernels(kv, q_len):
     b = W.make_batch([2, 63, 513, 1000, 3333, 4113, 600], q_len=q_len, kv_dtype=kv, seed=95)
     check(b, num_ctas=7, weighted=True)
+
+
+@pytest.mark.parametrize("q_len,kv", [(3, "bf16"), (4, "bf16"), (4, "e4m3"), (8, "bf16")])
+def test_mtp_more_draft_tokens(q_len, kv):
+    """G * q_len up to 64 query rows per KV head, in groups of 16 (grid z)."""
+    lens = [q_len, 70, 513, 1000, 3333, 9000]
+    b = W.make_batch(lens, q_len=q_len, kv_dtype=kv, seed=100 + q_len)
+    check(b, num_ctas=6)
+    check(b, num_ctas=6, fused=True)
+
+
+def test_mtp_rows_not_a_multiple_of_16():
+    b = W.make_batch([100, 2000], q_len=3, Hq=24, Hkv=4, seed=7)    # 6 heads x 3 tokens = 18 rows
+    check(b, num_ctas=4)
