@@ -141,7 +141,8 @@ def run_ours(args, rank, world, local_rank):
 
     torch.cuda.set_device(local_rank)
     dev = torch.device("cuda", local_rank)
-    b = W.make_config(args.config, seed=args.seed + rank, max_requests=args.requests)
+    b = W.make_config(args.config, seed=args.seed + rank, max_requests=args.requests,
+                      q_len=args.q_len)
     if args.tile:
         b.tile = args.tile
     kv = hpa.KV_BF16 if b.kv_dtype == "bf16" else hpa.KV_E4M3
@@ -371,6 +372,8 @@ def main():
     ap.add_argument("--requests", type=int, default=None,
                     help="keep only the first N requests of the workload (smaller case)")
     ap.add_argument("--tile", type=int, default=None, help="tile size in tokens (default 512)")
+    ap.add_argument("--q-len", type=int, default=None,
+                    help="query tokens per request (default: the workload's, 1 or 2)")
     ap.add_argument("--plan", default="tiles", choices=["tiles", "weighted"],
                     help="tile budgets (the pages' method) or the token-weighted variant")
     ap.add_argument("--num-ctas", type=int, default=None,

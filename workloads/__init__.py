@@ -239,16 +239,19 @@ def config_lens(cfg: int, seed: int = 0) -> np.ndarray:
             4: lens_long, 5: lambda: lens_lognormal(seed)}[cfg]()
 
 
-def make_config(cfg: int, seed: int = 0, max_requests: int | None = None) -> Batch:
+def make_config(cfg: int, seed: int = 0, max_requests: int | None = None,
+                q_len: int | None = None) -> Batch:
     """The five decode workloads (sizes in the docstring of each length recipe).
 
     max_requests keeps only the first requests of the batch (smaller cases of
-    the same workload, e.g. for profiling)."""
+    the same workload, e.g. for profiling); q_len overrides the number of new
+    query tokens per request (MTP variants)."""
     lens = config_lens(cfg, seed)
     if max_requests is not None:
         lens = lens[:max_requests]
     if cfg == 1:
-        return make_batch(lens, seed=seed, shuffle_pages=False, name=CONFIGS[1], num_ctas=4)
+        return make_batch(lens, q_len=q_len or 1, seed=seed, shuffle_pages=False,
+                          name=CONFIGS[1], num_ctas=4)
     if cfg == 5:
-        return make_batch(lens, q_len=2, kv_dtype="e4m3", seed=seed, name=CONFIGS[5])
-    return make_batch(lens, seed=seed, name=CONFIGS[cfg])
+        return make_batch(lens, q_len=q_len or 2, kv_dtype="e4m3", seed=seed, name=CONFIGS[5])
+    return make_batch(lens, q_len=q_len or 1, seed=seed, name=CONFIGS[cfg])
