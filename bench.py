@@ -296,8 +296,36 @@ def run_ours(args, rank, world, local_rank):
     e2e_ms = max_over_ranks(timed(e2e_step, args.steps, args.warmup, breakdown=False)[0],
                             world, dev)
 
+    feeder = None if args.no_feeder else feeder_measure(hpa, dev, stream, args, timed)
     return dict(b=b, C=C, ms=ms, attn=attn, plan=plan_ms, comb=comb_ms, clocks=clocks, tail=tail,
+                feeder=feeder,
                 fused_ms=fused_ms, comparator=comparator, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
+
+
+def feeder_measure(hpa, dev, stream, args, timed, n_tokens=65536):
+    """hpa_store_kv on a 64K-token chunk (RoPE + RMSNorm + Hadamard + E4M3 + paged store).
+
+    Algorithmic bytes per token: K and V in (8 heads x 128 x bf16 x 2 = 4096 B), the
+    token's cos/sin row (512 B) and the E4M3 K and V written (2048 B)."""
+    import torch
+    b = W.make_batch([n_tokens], q_len=1, kv_dtype="e4m3", seed=args.seed + 99)
+    fi = W.make_feeder_inputs(args.seed + 99, 1, n_tokens, max_pos=n_tokens)
+    k, v = b.k_pool.to(dev), b.v_pool.to(dev)
+    ks, vs = torch.from_numpy(b.k_scale).to(dev), torch.from_numpy(b.v_scale).to(dev)
+    lens = torch.from_numpy(b.seq_lens).to(dev)
+    ip, ix = torch.from_numpy(b.page_indptr).to(dev), torch.from_numpy(b.page_indices).to(dev)
+    kn, vn = fi.k_new.to(dev), fi.v_new.to(dev)
+    cs, w = torch.from_numpy(fi.cos_sin).to(dev), torch.from_numpy(fi.norm_w).to(dev)
+
+    def f(ev=None):
+        hpa.hpa_store_kv(kn, vn, lens, ip, ix, cs, w, k, v, eps=fi.eps, use_hadamard=True,
+                         k_scale=ks, v_scale=vs, stream=stream)
+
+    ms = timed(f, max(10, args.steps // 10), args.warmup, breakdown=False)[0]
+    nbytes = n_tokens * (4096 + 512 + 2048)
+    return {"workload": "store %d new tokens, 8 KV heads, E4M3 cache, Hadamard on" % n_tokens,
+            "us_per_call": round(ms * 1e3, 2), "algorithmic_bytes": nbytes,
+            "achieved_gbs": round(nbytes / (ms * 1e-3) / 1e9, 1)}
 
 
 # ----------------------------------------------------------------------------- CPU oracle
@@ -380,6 +408,7 @@ def main():
                     help="partitions per KV head (default: the device default)")
     ap.add_argument("--no-static", action="store_true", help="skip the static comparators")
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-feeder", action="store_true", help="skip the KV-store feeder timing")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -436,6 +465,7 @@ def main():
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "decode_attn_kernel", "peak_kind": peak_kind + " (hbm_gbs)"},
         "tail": r["tail"],
+        "kv_store_feeder": r["feeder"],
         "fused_combine": {"us_per_batch": round(per_batch_us(r["fused_ms"], world), 2),
                           "speedup_vs_three_calls": round(r["ms"] / r["fused_ms"], 3)},
         "cpu_baseline": cpu,

@@ -240,6 +240,35 @@ int hpa_combine(const float *partial_o_dev, const float *partial_lse_dev, void *
                 void *out_dev, float *out_lse_dev, hpa_stream_t stream);
 
 /*
+ * hpa_store_kv -- the fused KV-cache writer that feeds the decode path
+ * ("Hy3 Preview AI Infra 推理优化精读笔记", §4.1 "Rope + Norm + Hadamard + Quant +
+ * Store KV": the element-wise chain after the QKV projection in one pass,
+ * written straight to the low-bit cache).  For request r, new token j (at
+ * position pos = L_r - q_len + j) and KV head h:
+ *   key:   rotate-half RoPE with cos_sin[pos] (cos in columns [0, d/2), sin in
+ *          [d/2, d)), then RMSNorm over d (x / sqrt(mean x^2 + eps) * norm_w),
+ *          then, if use_hadamard, the orthonormal Sylvester Walsh-Hadamard
+ *          transform of order d; stored as bf16, or as E4M3 codes of
+ *          x / k_scale[h] (round to nearest even, saturating at +-448);
+ *   value: stored as bf16, or as E4M3 codes of v / v_scale[h];
+ * into slot pos % page_size of page page_indices[page_indptr[r] + pos / page_size]
+ * of k_pool_dev / v_pool_dev ([num_pages][Hkv][page_size][d]).
+ * k_new_dev, v_new_dev: bf16 [B][q_len][Hkv][d], 8-byte aligned.  seq_lens_dev:
+ * int32 [B], lengths including the new tokens.  cos_sin_dev: fp32 [max_pos][d],
+ * 16-byte aligned.  norm_w_dev: fp32 [d], 16-byte aligned.  d == 128,
+ * page_size == 64.  status_dev: optional int32; a position outside
+ * [0, max_pos) sets HPA_STATUS_BAD_SEQLEN, a missing or out-of-range page
+ * HPA_STATUS_BAD_PAGE, and that token is not written.
+ */
+int hpa_store_kv(const void *k_new_dev, const void *v_new_dev, const int32_t *seq_lens_dev,
+                 const int32_t *page_indptr_dev, const int32_t *page_indices_dev,
+                 int64_t num_pages, int32_t page_size, const float *cos_sin_dev, int32_t max_pos,
+                 const float *norm_w_dev, float eps, int32_t use_hadamard, int32_t kv_dtype,
+                 const float *k_scale_dev, const float *v_scale_dev, void *k_pool_dev,
+                 void *v_pool_dev, int32_t B, int32_t q_len, int32_t Hkv, int32_t d,
+                 int32_t *status_dev, hpa_stream_t stream);
+
+/*
  * hpa_selftest_wait_timeout -- diagnostic for the failure path of the
  * attention pipeline (no counterpart on the pages).  One thread waits on an
  * mbarrier phase that nothing completes, using the same time-bounded wait

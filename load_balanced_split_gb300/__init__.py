@@ -8,4 +8,5 @@ from .hpa import (KV_BF16, KV_E4M3, HpaError, Workspace, decode_step,  # noqa: F
                   hpa_decode_attn_fused,
                   hpa_decode_attn_traced, hpa_default_num_ctas, hpa_max_segments, hpa_plan,
                   hpa_plan_static, hpa_plan_weighted, hpa_selftest_wait_timeout, hpa_static_num_ctas,
-                  hpa_static_taskmap_bytes, hpa_taskmap_bytes, lib, trace_summary)
+                  hpa_static_taskmap_bytes, hpa_store_kv, hpa_taskmap_bytes, lib,
+                  trace_summary)

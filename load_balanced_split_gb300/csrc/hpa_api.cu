@@ -316,6 +316,52 @@ int hpa_selftest_wait_timeout(int32_t *status_dev, int64_t limit_ns, hpa_stream_
   return e == cudaSuccess ? HPA_OK : cuda_fail(e);
 }
 
+int hpa_store_kv(const void *k_new_dev, const void *v_new_dev, const int32_t *seq_lens_dev,
+                 const int32_t *page_indptr_dev, const int32_t *page_indices_dev,
+                 int64_t num_pages, int32_t page_size, const float *cos_sin_dev, int32_t max_pos,
+                 const float *norm_w_dev, float eps, int32_t use_hadamard, int32_t kv_dtype,
+                 const float *k_scale_dev, const float *v_scale_dev, void *k_pool_dev,
+                 void *v_pool_dev, int32_t B, int32_t q_len, int32_t Hkv, int32_t d,
+                 int32_t *status_dev, hpa_stream_t stream) {
+  if (!k_new_dev || !v_new_dev || !seq_lens_dev || !page_indptr_dev || !page_indices_dev ||
+      !cos_sin_dev || !norm_w_dev || !k_pool_dev || !v_pool_dev)
+    return HPA_ERR_INVALID;
+  if (kv_dtype != HPA_KV_BF16 && kv_dtype != HPA_KV_E4M3) return HPA_ERR_INVALID;
+  if (kv_dtype == HPA_KV_E4M3 && (!k_scale_dev || !v_scale_dev)) return HPA_ERR_INVALID;
+  if (B < 1 || B > kMaxB || q_len < 1 || Hkv < 1 || Hkv > 65535 || num_pages < 1 ||
+      max_pos < 1 || !(eps >= 0.f) || !std::isfinite(eps))
+    return HPA_ERR_INVALID;
+  if (d != hpa::HEAD_DIM || page_size != hpa::PAGE) return HPA_ERR_UNSUPPORTED;
+  if (int64_t(B) * q_len * Hkv > (int64_t(1) << 34)) return HPA_ERR_UNSUPPORTED;
+  if (!aligned(k_new_dev, 8) || !aligned(v_new_dev, 8) || !aligned(cos_sin_dev, 16) ||
+      !aligned(norm_w_dev, 16) || !aligned(k_pool_dev, 8) || !aligned(v_pool_dev, 8) ||
+      (status_dev && !aligned(status_dev, 4)))
+    return HPA_ERR_ALIGN;
+  hpa::StoreKvParams p;
+  p.k_new = static_cast<const __nv_bfloat16 *>(k_new_dev);
+  p.v_new = static_cast<const __nv_bfloat16 *>(v_new_dev);
+  p.seq_lens = seq_lens_dev;
+  p.page_indptr = page_indptr_dev;
+  p.page_indices = page_indices_dev;
+  p.num_pages = num_pages;
+  p.cos_sin = cos_sin_dev;
+  p.max_pos = max_pos;
+  p.norm_w = norm_w_dev;
+  p.eps = eps;
+  p.use_hadamard = use_hadamard != 0;
+  p.kv_dtype = kv_dtype;
+  p.k_scale = k_scale_dev;
+  p.v_scale = v_scale_dev;
+  p.k_pool = k_pool_dev;
+  p.v_pool = v_pool_dev;
+  p.B = B;
+  p.q_len = q_len;
+  p.Hkv = Hkv;
+  p.status = status_dev;
+  cudaError_t e = hpa::launch_store_kv(p, reinterpret_cast<cudaStream_t>(stream));
+  return e == cudaSuccess ? HPA_OK : cuda_fail(e);
+}
+
 const char *hpa_error_string(int code) {
   switch (code) {
     case HPA_OK: return "ok";

@@ -69,6 +69,22 @@ cudaError_t launch_decode_attn(const AttnParams &p, const CUtensorMap &tmk,
 int attn_ctas_per_sm(int kv_dtype, int q_len, int *ctas);  // occupancy query (host)
 cudaError_t launch_selftest_wait(int32_t *status, long long limit_ns, cudaStream_t s);
 
+struct StoreKvParams {
+  const __nv_bfloat16 *k_new, *v_new;
+  const int32_t *seq_lens, *page_indptr, *page_indices;
+  int64_t num_pages;
+  const float *cos_sin;
+  int max_pos;
+  const float *norm_w;
+  float eps;
+  int use_hadamard, kv_dtype;
+  const float *k_scale, *v_scale;
+  void *k_pool, *v_pool;
+  int B, q_len, Hkv;
+  int32_t *status;
+};
+cudaError_t launch_store_kv(const StoreKvParams &p, cudaStream_t s);
+
 // ----------------------------------------------------------------------------- PTX wrappers
 __device__ __forceinline__ uint32_t smem_u32(const void *p) {
   return static_cast<uint32_t>(__cvta_generic_to_shared(p));
@@ -190,6 +206,14 @@ __device__ __forceinline__ void mma_f16(float (&d)[4], const uint32_t (&a)[4], u
       "{%0,%1,%2,%3}, {%4,%5,%6,%7}, {%8,%9}, {%0,%1,%2,%3};"
       : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
       : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
+}
+
+// (lo, hi) fp32 -> two E4M3 codes, lo in the low byte; round to nearest even,
+// saturating at +-448.
+__device__ __forceinline__ uint16_t f32x2_to_e4m3x2(float lo, float hi) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
 }
 
 // Two E4M3 codes (low 16 bits of `v`, element 0 in the low byte) -> f16x2 with

@@ -65,6 +65,8 @@ def lib():
                 "hpa_decode_attn_combine_noalloc": ([P, P, P, I32, P, P, I64, P, P, I32, I32,
                                                      I32, I32, I32, I32, F, P, I32, P, P, P],
                                                     ctypes.c_int),
+                "hpa_store_kv": ([P, P, P, P, P, I64, I32, P, I32, P, F, I32, I32, P, P, P, P,
+                                  I32, I32, I32, I32, P, P], ctypes.c_int),
                 "hpa_error_string": ([ctypes.c_int], ctypes.c_char_p),
                 "hpa_last_cuda_error": ([], ctypes.c_int),
             }
@@ -317,6 +319,34 @@ def hpa_decode_attn_combine_noalloc(q, k_pool, v_pool, page_indptr, page_indices
         _ptr(page_indptr), _ptr(page_indices), page, B, q_len, Hq, Hkv, d, float(sm_scale),
         _ptr(taskmap), num_ctas, _ptr(out), _ptr(out_lse), _stream(stream)),
         "hpa_decode_attn_combine_noalloc")
+
+
+def hpa_store_kv(k_new, v_new, seq_lens, page_indptr, page_indices, cos_sin, norm_w, k_pool,
+                 v_pool, eps: float = 1e-6, use_hadamard: bool = True, k_scale=None,
+                 v_scale=None, status=None, stream=None):
+    """Fused RoPE + RMSNorm + Hadamard + quantise + paged store of the new tokens' K/V.
+
+    k_new, v_new: bf16 [B][q_len][Hkv][d]; cos_sin: fp32 [max_pos][d]; norm_w: fp32 [d];
+    pools: bf16 or uint8 (E4M3) [P][Hkv][page][d] (E4M3 needs k_scale / v_scale)."""
+    for t, n in ((k_new, "k_new"), (v_new, "v_new")):
+        _dev(t, n, torch.bfloat16)
+    _dev(cos_sin, "cos_sin", torch.float32)
+    _dev(norm_w, "norm_w", torch.float32)
+    for t, n in ((seq_lens, "seq_lens"), (page_indptr, "page_indptr"),
+                 (page_indices, "page_indices")):
+        _dev(t, n, torch.int32)
+    _dev(k_pool, "k_pool")
+    _dev(v_pool, "v_pool")
+    kv = KV_BF16 if k_pool.dtype == torch.bfloat16 else KV_E4M3
+    B, q_len, Hkv, d = k_new.shape
+    P, Hkv2, page, _ = k_pool.shape
+    if Hkv2 != Hkv:
+        raise HpaError("KV head count mismatch")
+    _check(lib().hpa_store_kv(
+        _ptr(k_new), _ptr(v_new), _ptr(seq_lens), _ptr(page_indptr), _ptr(page_indices), P,
+        page, _ptr(cos_sin), cos_sin.shape[0], _ptr(norm_w), float(eps), int(use_hadamard), kv,
+        _ptr(k_scale), _ptr(v_scale), _ptr(k_pool), _ptr(v_pool), B, q_len, Hkv, d,
+        _ptr(status), _stream(stream)), "hpa_store_kv")
 
 
 # ----------------------------------------------------------------------------- workspace helper

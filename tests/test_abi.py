@@ -128,3 +128,25 @@ def test_weighted_plan_size_limit():
     nb = hpa.hpa_taskmap_bytes(B, C)
     assert L.hpa_plan_weighted(FAKE, B, 512, C, FAKE, nb, None) == -2
     assert L.hpa_plan_weighted(None, 3, 512, 4, FAKE, hpa.hpa_taskmap_bytes(3, 4), None) == -1
+
+
+def test_store_kv_argument_checks():
+    L = hpa.lib()
+
+    def call(**kw):
+        a = dict(k=FAKE, v=FAKE, lens=FAKE, ip=FAKE, ix=FAKE, P=10, page=64, cs=FAKE, maxpos=100,
+                 w=FAKE, eps=1e-6, had=1, kv=0, ks=None, vs=None, kp=FAKE, vp=FAKE, B=2, q=1,
+                 Hkv=8, d=128, st=None)
+        a.update(kw)
+        return L.hpa_store_kv(a["k"], a["v"], a["lens"], a["ip"], a["ix"], a["P"], a["page"],
+                              a["cs"], a["maxpos"], a["w"], a["eps"], a["had"], a["kv"], a["ks"],
+                              a["vs"], a["kp"], a["vp"], a["B"], a["q"], a["Hkv"], a["d"],
+                              a["st"], None)
+
+    assert call(k=None) == -1
+    assert call(kv=1) == -1                      # E4M3 without scales
+    assert call(eps=-1.0) == -1
+    assert call(d=64) == -2
+    assert call(page=16) == -2
+    assert call(cs=FAKE + 4) == -4
+    assert call(k=FAKE + 2) == -4

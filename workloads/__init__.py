@@ -255,3 +255,33 @@ def make_config(cfg: int, seed: int = 0, max_requests: int | None = None,
     if cfg == 5:
         return make_batch(lens, q_len=q_len or 2, kv_dtype="e4m3", seed=seed, name=CONFIGS[5])
     return make_batch(lens, q_len=q_len or 1, seed=seed, name=CONFIGS[cfg])
+
+
+# ----------------------------------------------------------------------------- KV-store feeder
+def rope_cos_sin_table(max_pos: int, d: int = HEAD_DIM, theta: float = 10000.0) -> np.ndarray:
+    """fp32 [max_pos][d]: cos(pos * theta^(-2i/d)) in columns i < d/2, sin in columns d/2 + i.
+
+    The angles are formed in float64 and rounded once to fp32 (the table is an
+    input of the KV writer, as a serving engine would pass it)."""
+    inv = theta ** (-np.arange(0, d // 2, dtype=np.float64) * 2.0 / d)
+    ang = np.arange(max_pos, dtype=np.float64)[:, None] * inv[None, :]
+    return np.concatenate([np.cos(ang), np.sin(ang)], axis=1).astype(np.float32)
+
+
+@dataclass
+class FeederInputs:
+    k_new: torch.Tensor        # bf16 [B][q_len][Hkv][d], the projected keys of the new tokens
+    v_new: torch.Tensor        # bf16 [B][q_len][Hkv][d]
+    norm_w: np.ndarray         # fp32 [d], RMSNorm weight
+    cos_sin: np.ndarray        # fp32 [max_pos][d]
+    eps: float = 1e-6
+
+
+def make_feeder_inputs(seed: int, B: int, q_len: int, max_pos: int, Hkv: int = HKV,
+                       d: int = HEAD_DIM, theta: float = 10000.0) -> FeederInputs:
+    rng = np.random.default_rng([seed, 6, 0])
+    k = rng.standard_normal((B, q_len, Hkv, d), dtype=np.float32) * 3.0
+    v = rng.standard_normal((B, q_len, Hkv, d), dtype=np.float32)
+    w = (1.0 + 0.1 * rng.standard_normal(d)).astype(np.float32)
+    return FeederInputs(k_new=to_bf16(k), v_new=to_bf16(v), norm_w=w,
+                        cos_sin=rope_cos_sin_table(max_pos, d, theta))
