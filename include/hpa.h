@@ -253,7 +253,7 @@ int hpa_combine(const float *partial_o_dev, const float *partial_lse_dev, void *
  *   value: stored as bf16, or as E4M3 codes of v / v_scale[h];
  * into slot pos % page_size of page page_indices[page_indptr[r] + pos / page_size]
  * of k_pool_dev / v_pool_dev ([num_pages][Hkv][page_size][d]).
- * k_new_dev, v_new_dev: bf16 [B][q_len][Hkv][d], 8-byte aligned.  seq_lens_dev:
+ * k_new_dev, v_new_dev: bf16 [B][q_len][Hkv][d], 16-byte aligned (pools too).  seq_lens_dev:
  * int32 [B], lengths including the new tokens.  cos_sin_dev: fp32 [max_pos][d],
  * 16-byte aligned.  norm_w_dev: fp32 [d], 16-byte aligned.  d == 128,
  * page_size == 64.  status_dev: optional int32; a position outside

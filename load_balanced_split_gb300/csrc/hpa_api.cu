@@ -333,8 +333,8 @@ int hpa_store_kv(const void *k_new_dev, const void *v_new_dev, const int32_t *se
     return HPA_ERR_INVALID;
   if (d != hpa::HEAD_DIM || page_size != hpa::PAGE) return HPA_ERR_UNSUPPORTED;
   if (int64_t(B) * q_len * Hkv > (int64_t(1) << 34)) return HPA_ERR_UNSUPPORTED;
-  if (!aligned(k_new_dev, 8) || !aligned(v_new_dev, 8) || !aligned(cos_sin_dev, 16) ||
-      !aligned(norm_w_dev, 16) || !aligned(k_pool_dev, 8) || !aligned(v_pool_dev, 8) ||
+  if (!aligned(k_new_dev, 16) || !aligned(v_new_dev, 16) || !aligned(cos_sin_dev, 16) ||
+      !aligned(norm_w_dev, 16) || !aligned(k_pool_dev, 16) || !aligned(v_pool_dev, 16) ||
       (status_dev && !aligned(status_dev, 4)))
     return HPA_ERR_ALIGN;
   hpa::StoreKvParams p;

@@ -149,4 +149,4 @@ def test_store_kv_argument_checks():
     assert call(d=64) == -2
     assert call(page=16) == -2
     assert call(cs=FAKE + 4) == -4
-    assert call(k=FAKE + 2) == -4
+    assert call(k=FAKE + 8) == -4
