@@ -30,9 +30,11 @@ namespace hpa {
 namespace {
 
 constexpr int kConsumerWarps = 4;
-// Segment-end merge buffer: one row of 128 partial-output columns per query row,
-// held in accumulator-fragment order (n-tile i, column n -> i * 8 + n) and padded
-// to 136 floats so the four warps' shared-memory adds hit at most 2 lanes per bank.
+// Segment-end merge buffers (two): one row of 128 partial-output columns per
+// query row, held in accumulator-fragment order (n-tile i, column n -> i * 8 + n)
+// and padded to 136 floats so a warp's fragment stores hit at most 2 lanes per
+// bank.  Warps 0 / 1 store into buffers A / B, warps 2 / 3 add into them, and
+// the read-out sums A + B: plain shared-memory traffic, no atomics.
 constexpr int kMergeStride = HEAD_DIM + 8;
 // Largest score excess (log2 units) over the running reference max before the
 // accumulators are rescaled: P values stay <= 256, well inside bf16/f16 range.
@@ -66,8 +68,8 @@ template <int KV>
 struct Smem {
   static constexpr int kStageBytes = 2 * Cfg<KV>::kKBytes;
   static constexpr int kStages = Cfg<KV>::kStages;
-  static constexpr int kMerge = kStages * kStageBytes;     // float[16][kMergeStride]
-  static constexpr int kStats = kMerge + MAX_ROWS * kMergeStride * 4;  // m[4][16], l[4][16]
+  static constexpr int kMerge = kStages * kStageBytes;  // float[2][16][kMergeStride]
+  static constexpr int kStats = kMerge + 2 * MAX_ROWS * kMergeStride * 4;  // m[4][16], l[4][16]
   static constexpr int kQ = kStats + 2 * kConsumerWarps * MAX_ROWS * 4;  // 2 query slots
   static constexpr int kInfo = kQ + 2 * kQSlotBytes;                      // int4[2][2]
   static constexpr int kBars = kInfo + 4 * 16;  // full[kStages] empty[kStages] qfull[2] qempty[2]
@@ -590,14 +592,36 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
     row_stats(row1, M1, L1);
     const float f0 = L0 > 0.f ? exp2f(m0 - M0) / L0 * vsc : 0.f;
     const float f1 = L1 > 0.f ? exp2f(m1 - M1) / L1 * vsc : 0.f;
+    float *mine = mbuf + (w & 1) * (MAX_ROWS * kMergeStride);
+    if (w < 2) {
 #pragma unroll
-    for (int i = 0; i < 16; ++i)
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        const int pos = i * 8 + 2 * qd + e;
-        if (v0) atomicAdd(&mbuf[row0 * kMergeStride + pos], o[i][e] * f0);
-        if (v1) atomicAdd(&mbuf[row1 * kMergeStride + pos], o[i][2 + e] * f1);
+      for (int i = 0; i < 16; ++i) {
+        const int pos = i * 8 + 2 * qd;
+        if (v0)
+          *reinterpret_cast<float2 *>(mine + row0 * kMergeStride + pos) =
+              make_float2(o[i][0] * f0, o[i][1] * f0);
+        if (v1)
+          *reinterpret_cast<float2 *>(mine + row1 * kMergeStride + pos) =
+              make_float2(o[i][2] * f1, o[i][3] * f1);
       }
+    }
+    named_barrier(1, kConsumerWarps * 32);
+    if (w >= 2) {
+#pragma unroll
+      for (int i = 0; i < 16; ++i) {
+        const int pos = i * 8 + 2 * qd;
+        if (v0) {
+          float2 *d = reinterpret_cast<float2 *>(mine + row0 * kMergeStride + pos);
+          const float2 t = *d;
+          *d = make_float2(t.x + o[i][0] * f0, t.y + o[i][1] * f0);
+        }
+        if (v1) {
+          float2 *d = reinterpret_cast<float2 *>(mine + row1 * kMergeStride + pos);
+          const float2 t = *d;
+          *d = make_float2(t.x + o[i][2] * f1, t.y + o[i][3] * f1);
+        }
+      }
+    }
     named_barrier(1, kConsumerWarps * 32);
     const int tid = threadIdx.x;
     // fused combine, single-segment request: this segment is the whole result
@@ -607,18 +631,19 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
       const int j = (rb + row) / G, g = (rb + row) % G;
       const int64_t dst = ((static_cast<int64_t>(direct ? f.r : s) * q_len + j) * p.Hq + h * G + g) *
                           HEAD_DIM;
-      float *mrow = mbuf + row * kMergeStride;
+      const float *ra = mbuf + row * kMergeStride;           // buffer A
+      const float *rb2 = ra + MAX_ROWS * kMergeStride;         // buffer B
       float4 val;
       if (KV == HPA_KV_BF16) {
-        val = *reinterpret_cast<float4 *>(mrow + 4 * c4);
-        *reinterpret_cast<float4 *>(mrow + 4 * c4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 a = *reinterpret_cast<const float4 *>(ra + 4 * c4);
+        const float4 b = *reinterpret_cast<const float4 *>(rb2 + 4 * c4);
+        val = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
       } else {
         float *x = &val.x;
 #pragma unroll
         for (int k = 0; k < 4; ++k) {
           const int pos = merge_pos<KV>(4 * c4 + k);
-          x[k] = mrow[pos];
-          mrow[pos] = 0.f;
+          x[k] = ra[pos] + rb2[pos];
         }
       }
       if (direct)
@@ -699,9 +724,6 @@ __global__ void __launch_bounds__(kThreads, 2)
     *reinterpret_cast<int *>(smem + S::kFlag) = 0;
     fence_barrier_init();
   }
-  float4 *mb4 = reinterpret_cast<float4 *>(smem + S::kMerge);
-  for (int v = threadIdx.x; v < MAX_ROWS * kMergeStride / 4; v += kThreads)
-    mb4[v] = make_float4(0.f, 0.f, 0.f, 0.f);
   __syncthreads();
   pdl_launch_dependents();  // the combine kernel may be scheduled; it waits for this grid
   if (trace && threadIdx.x == 0) {
