@@ -135,6 +135,17 @@ def per_batch_us(ms_per_step: float, world: int) -> float:
 
 
 # ----------------------------------------------------------------------------- our arm
+def step_distribution(step_ms):
+    """Median and p10 / p90 of single-step times (µs), from the breakdown pass: events
+    around every kernel of every step, so each step pays its own event overhead."""
+    if not step_ms:
+        return None
+    x = np.sort(np.asarray(step_ms, dtype=np.float64) * 1e3)
+    pick = lambda f: round(float(np.quantile(x, f)), 2)
+    return {"median": pick(0.5), "p10": pick(0.1), "p90": pick(0.9), "steps": int(x.size),
+            "source": "per-step CUDA events (breakdown pass, rank 0)"}
+
+
 def run_ours(args, rank, world, local_rank):
     import torch
     import load_balanced_split_gb300 as hpa
@@ -200,7 +211,7 @@ def run_ours(args, rank, world, local_rank):
         barrier()
         total = t0.elapsed_time(t1)
         if not breakdown:
-            return total / steps, [], [], []
+            return total / steps, [], [], [], []
         evs = [[torch.cuda.Event(enable_timing=True) for _ in range(4)] for _ in range(steps)]
         for i in range(steps):
             fn(ev=evs[i])
@@ -208,10 +219,11 @@ def run_ours(args, rank, world, local_rank):
         attn = [e[1].elapsed_time(e[2]) for e in evs]
         plan = [e[0].elapsed_time(e[1]) for e in evs]
         comb = [e[2].elapsed_time(e[3]) for e in evs]
-        return total / steps, attn, plan, comb
+        whole = [e[0].elapsed_time(e[3]) for e in evs]
+        return total / steps, attn, plan, comb, whole
 
     with ClockSampler(local_rank) as clk:
-        ms, attn, plan_ms, comb_ms = timed(step, args.steps, args.warmup)
+        ms, attn, plan_ms, comb_ms, step_ms = timed(step, args.steps, args.warmup)
     clocks = clk.summary()
     torch.cuda.synchronize(dev)
     status = ws.status()
@@ -255,7 +267,7 @@ def run_ours(args, rank, world, local_rank):
                            breakdown=False)[0]
         best = min(res, key=res.get)
         wsb = hpa.Workspace(b.B, b.q_len, b.Hq, b.d, splits=best, device=dev)
-        _, attn_b, _, _ = timed(lambda ev=None, w=wsb: step(w, ev), max(3, args.steps // 2), 3)
+        _, attn_b, _, _, _ = timed(lambda ev=None, w=wsb: step(w, ev), max(3, args.steps // 2), 3)
         comparator = {
             "static_heuristic": {"splits": heur, "us_per_batch": round(res[heur] * 1e3, 2)},
             "static_best": {"splits": best, "us_per_batch": round(res[best] * 1e3, 2),
@@ -297,7 +309,8 @@ def run_ours(args, rank, world, local_rank):
                             world, dev)
 
     feeder = None if args.no_feeder else feeder_measure(hpa, dev, stream, args, timed)
-    return dict(b=b, C=C, ms=ms, attn=attn, plan=plan_ms, comb=comb_ms, clocks=clocks, tail=tail,
+    return dict(b=b, C=C, ms=ms, attn=attn, plan=plan_ms, comb=comb_ms, step_ms=step_ms,
+                clocks=clocks, tail=tail,
                 feeder=feeder,
                 fused_ms=fused_ms, comparator=comparator, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
 
@@ -469,6 +482,7 @@ def main():
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": "decode_attn_kernel", "peak_kind": peak_kind + " (hbm_gbs)"},
+        "step_us_distribution": step_distribution(r["step_ms"]),
         "tail": r["tail"],
         "kv_store_feeder": r["feeder"],
         "fused_combine": {"us_per_batch": round(per_batch_us(r["fused_ms"], world), 2),
