@@ -157,7 +157,9 @@ def run_ours(args, rank, world, local_rank):
     if args.tile:
         b.tile = args.tile
     kv = hpa.KV_BF16 if b.kv_dtype == "bf16" else hpa.KV_E4M3
-    C = args.num_ctas or b.num_ctas or hpa.hpa_default_num_ctas(b.Hkv, b.q_len, kv, b.Hq)
+    tc = args.attn == "tc"
+    default_c = hpa.hpa_default_num_ctas_tc if tc else hpa.hpa_default_num_ctas
+    C = args.num_ctas or b.num_ctas or default_c(b.Hkv, b.q_len, kv, b.Hq)
     groups = (b.Hq // b.Hkv * b.q_len + 15) // 16  # query-row groups per (partition, head)
     q = b.q.to(dev)
     k, v = b.k_pool.to(dev), b.v_pool.to(dev)
@@ -181,7 +183,7 @@ def run_ours(args, rank, world, local_rank):
         if ev is not None:
             ev[1].record(stream)
         hpa.hpa_decode_attn(q, k, v, indptr, indices, w.taskmap, w.num_ctas, w.partial_o,
-                            w.partial_lse, ks, vs, stream=stream)
+                            w.partial_lse, ks, vs, stream=stream, tc=tc)
         if ev is not None:
             ev[2].record(stream)
         hpa.hpa_combine(w.partial_o, w.partial_lse, w.taskmap, w.num_ctas, out, out_lse, stream)
@@ -234,6 +236,8 @@ def run_ours(args, rank, world, local_rank):
 
     def traced_tail(w, reps=3):
         """Per-CTA timestamps of the attention kernel (outside the timed region)."""
+        if tc:
+            return None  # the tcgen05 kernel has no traced variant
         tr = torch.zeros(4 * w.num_ctas * b.Hkv * groups, dtype=torch.int64, device=dev)
         out_t = None
         for _ in range(reps):
@@ -251,8 +255,8 @@ def run_ours(args, rank, world, local_rank):
         hpa.decode_step(ws, q, k, v, lens, indptr, indices, out, out_lse, ks, vs, tile=b.tile,
                         stream=stream, fused=True)
 
-    fused_ms = max_over_ranks(timed(fused_step, args.steps, args.warmup, breakdown=False)[0],
-                              world, dev)
+    fused_ms = None if tc else max_over_ranks(
+        timed(fused_step, args.steps, args.warmup, breakdown=False)[0], world, dev)
 
     # static split-KV comparators through the same kernels (heuristic and best of a sweep)
     comparator = None
@@ -297,7 +301,7 @@ def run_ours(args, rank, world, local_rank):
             indptr.copy_(indptr_h, non_blocking=True)
             indices.copy_(indices_h, non_blocking=True)
         hpa.decode_step(ws, q, k, v, lens, indptr, indices, out, out_lse, ks, vs, tile=b.tile,
-                        stream=stream)
+                        stream=stream, tc=tc)
         with torch.cuda.stream(stream):
             out_h.copy_(out, non_blocking=True)
             lse_h.copy_(out_lse, non_blocking=True)
@@ -424,6 +428,9 @@ def main():
                     help="tile budgets (the pages' method) or the token-weighted variant")
     ap.add_argument("--num-ctas", type=int, default=None,
                     help="partitions per KV head (default: the device default)")
+    ap.add_argument("--attn", default="mma", choices=["mma", "tc"],
+                    help="attention kernel: mma.sync (hpa_decode_attn) or tcgen05 "
+                         "(hpa_decode_attn_tc)")
     ap.add_argument("--no-static", action="store_true", help="skip the static comparators")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-feeder", action="store_true", help="skip the KV-store feeder timing")
@@ -454,7 +461,8 @@ def main():
     achieved = kv_bytes / (attn_ms * 1e-3) / 1e9
     us_batch = per_batch_us(r["ms"], world)
     traffic = None
-    if TRAFFIC_PROFILE["source_sha256"] == kernel_sha() and TRAFFIC_PROFILE["bytes_per_kv_byte"]:
+    if (args.attn == "mma" and TRAFFIC_PROFILE["source_sha256"] == kernel_sha()
+            and TRAFFIC_PROFILE["bytes_per_kv_byte"]):
         traffic = int(TRAFFIC_PROFILE["bytes_per_kv_byte"] * kv_bytes)
     cpu = None
     if not args.no_cpu_baseline:
@@ -472,6 +480,7 @@ def main():
                    "kv_tokens": int(b.seq_lens.sum()), "q_len": b.q_len, "heads": "64q/8kv",
                    "head_dim": 128, "page": 64, "tile": b.tile, "num_ctas": int(r["C"]),
                    "kv_dtype": b.kv_dtype, "kv_bytes": int(kv_bytes), "plan": args.plan,
+                   "attention_kernel": "tcgen05" if args.attn == "tc" else "mma.sync",
                    "l2": "inputs larger than L2 (%.2f GB KV), no flush" % (kv_bytes / 1e9),
                    "parallelism": "dp%d replicas" % world, "seed": args.seed},
         "kv_gbs": round(kv_bytes / (r["ms"] * 1e-3) / 1e9, 1),
@@ -481,12 +490,14 @@ def main():
                          "combine": round(statistics.mean(r["comb"]) * 1e3, 2)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "decode_attn_kernel", "peak_kind": peak_kind + " (hbm_gbs)"},
+                     "kernel": "decode_attn_kernel" if args.attn == "mma" else "decode_attn_tc_kernel",
+                     "peak_kind": peak_kind + " (hbm_gbs)"},
         "step_us_distribution": step_distribution(r["step_ms"]),
         "tail": r["tail"],
         "kv_store_feeder": r["feeder"],
-        "fused_combine": {"us_per_batch": round(per_batch_us(r["fused_ms"], world), 2),
-                          "speedup_vs_three_calls": round(r["ms"] / r["fused_ms"], 3)},
+        "fused_combine": None if r["fused_ms"] is None else {
+            "us_per_batch": round(per_batch_us(r["fused_ms"], world), 2),
+            "speedup_vs_three_calls": round(r["ms"] / r["fused_ms"], 3)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(per_batch_us(r["e2e_ms"], world), 2), "unit": UNIT,
                 "h2d_bytes_per_step": int(r["h2d"]), "d2h_bytes_per_step": int(r["d2h"])},

@@ -182,6 +182,31 @@ int hpa_decode_attn(const void *q_dev, const void *k_pool_dev, const void *v_poo
                     float *partial_lse_dev, hpa_stream_t stream);
 
 /*
+ * hpa_decode_attn_tc -- the same split-KV attention step ([Notes §3.1] steps
+ * 4-5), computed by a kernel that runs both products on the 5th-generation
+ * tensor cores (tcgen05.mma with accumulators in tensor memory).  Grid
+ * num_ctas x Hkv: one CTA covers all G * q_len query rows of its KV head
+ * (up to 64) in a single pass over the keys, where hpa_decode_attn makes one
+ * pass per group of 16 rows.  It pays for MTP with more than 16 rows per KV
+ * head; up to 16 rows hpa_decode_attn is as fast or faster.
+ * Arguments, layouts, supported shapes, outputs and errors are exactly those
+ * of hpa_decode_attn; the partials feed hpa_combine unchanged.  E4M3 pages
+ * enter the MMA as 8-bit operands; the query rows and the probabilities are
+ * each carried as two E4M3 terms (about 8 significant bits, as bf16).
+ */
+int hpa_decode_attn_tc(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
+                       int32_t kv_dtype, const float *k_scale_dev, const float *v_scale_dev,
+                       int64_t num_pages, const int32_t *page_indptr_dev,
+                       const int32_t *page_indices_dev, int32_t page_size, int32_t B,
+                       int32_t q_len, int32_t Hq, int32_t Hkv, int32_t d, float sm_scale,
+                       void *taskmap_dev, int32_t num_ctas, float *partial_o_dev,
+                       float *partial_lse_dev, hpa_stream_t stream);
+
+/* Partitions per KV head that fill the current device once with
+ * hpa_decode_attn_tc CTAs (SMs x resident CTAs per SM / Hkv), or -1. */
+int32_t hpa_default_num_ctas_tc(int32_t Hq, int32_t Hkv, int32_t q_len, int32_t kv_dtype);
+
+/*
  * hpa_decode_attn_traced -- hpa_decode_attn that also records, for every CTA,
  * four uint64 words at trace_dev[4 * (h * num_ctas + c)]: the %globaltimer (ns)
  * at kernel entry, after the task map was read, after the CTA's last segment

@@ -1,0 +1,843 @@
+// Split-KV GQA decode attention on the 5th-generation tensor cores (tcgen05),
+// driven by the same task map and writing the same partials as decode_attn.cu.
+//
+// "Hy3 Preview AI Infra 推理优化精读笔记", §3.1 方案 steps 4-5: each CTA takes the
+// tiles of its partition from the task map and writes split-KV partial
+// results for the combine.  One CTA is (partition c, KV head h) and covers all
+// G * q_len query rows of h (up to 64) in one pass over the KV, where the
+// mma.sync kernel needs one pass per group of 16 rows.  This matters for MTP
+// with several draft tokens, where the warp-level MMAs become the bound.
+//
+// Work per step = two pages (128 keys) of one KV head:
+//   S^T[128 keys][rows]  = K[128 keys][128 dims] . Q^T          (tcgen05.mma, TMEM)
+//   P^T = exp2(S^T - m)  by 128 threads, one key each            (registers -> smem)
+//   O^T[128 dims][rows] += V^T[128 dims][128 keys] . P^T         (tcgen05.mma, TMEM)
+// Keys sit on the TMEM lanes for the softmax, so all four compute warps share
+// it; output dims sit on the lanes for O, so each compute thread owns one dim
+// at the segment end and O needs no cross-warp merge.  The row sums l are
+// accumulated in fp32 from the unrounded probabilities, per thread (its key
+// slot) across the steps, and reduced once per segment.
+//
+// E4M3 pages feed the MMA as they are (kind::f8f6f4).  The query rows and the
+// probabilities are each split into two E4M3 terms, hi = e4m3(x) and
+// lo = e4m3(x - hi), accumulated into the same D: their sum carries about
+// 8 significant bits, the precision of bf16, so no widening pass is needed.
+// Queries are scaled per row by a power of two into the E4M3 range (folded
+// into the score scale), so a bf16 query row is carried exactly.  Probabilities are 2^(s - m + 4) with a reference max m that
+// moves only when a score exceeds it by more than 4 (base 2), so P <= 256.
+// bf16 pages use kind::f16 with bf16 Q and P.
+//
+// Roles (192 threads): warps 0-3 compute (softmax, epilogue), warp 4 TMA
+// producer, warp 5 one elected thread issuing every MMA.  S is double-buffered
+// in TMEM so Q K^T of step i+1 overlaps the softmax of step i.  Every wait is
+// bounded in time; a role that gives up flags the task map's status word and
+// raises the CTA's abort flag, the MMA thread waits for its MMAs in flight and
+// the producer for its copies, and the CTA frees its TMEM and returns.
+#include <math_constants.h>
+
+#include <climits>
+
+#include "hpa_internal.cuh"
+
+namespace hpa {
+namespace {
+
+constexpr int kTcComputeWarps = 4;
+constexpr int kTcThreads = (kTcComputeWarps + 2) * 32;
+constexpr uint32_t kFull = 0xffffffffu;
+
+template <int KV>
+struct TcCfg;
+template <>
+struct TcCfg<HPA_KV_BF16> {
+  static constexpr int kPageBytes = 16384;  // one page-head of K (or V)
+  static constexpr float kSlack = 8.f;      // P <= 2^8 in bf16
+  static constexpr float kPOff = 0.f;
+};
+template <>
+struct TcCfg<HPA_KV_E4M3> {
+  static constexpr int kPageBytes = 8192;
+  static constexpr float kSlack = 4.f;      // P = 2^(s - m + 4) <= 2^8 = 256 < 448
+  static constexpr float kPOff = 4.f;
+};
+
+// Shared memory of one CTA; NC = row chunks of 16 (Rp = 16 NC padded rows).
+template <int KV, int NC>
+struct TcSmem {
+  static constexpr int kRp = 16 * NC;
+  static constexpr int kKPair = 2 * TcCfg<KV>::kPageBytes;     // K of 128 keys
+  static constexpr int kStageBytes = 2 * kKPair;               // K then V
+  static constexpr int kOperand = 256 * kRp;                   // a Q slot or a P buffer
+  // as many page-pair stages as fit beside the operands (one CTA per SM): DRAM
+  // latency is hidden by the bytes in flight, up to 6 x 32 KB (E4M3) / 3 x 64 KB
+  static constexpr int kStages0 = (226 * 1024 - 4 * kOperand - 6 * 1024) / kStageBytes;
+  static constexpr int kStages = kStages0 > 6 ? 6 : kStages0;
+  static constexpr int kQ = kStages * kStageBytes;             // 2 query slots
+  static constexpr int kP = kQ + 2 * kOperand;                 // 2 probability buffers
+  static constexpr int kRowC = kP + 2 * kOperand;              // float[2][64] score scales
+  static constexpr int kStepMax = kRowC + 2 * 64 * 4;          // float[2][4][64]
+  static constexpr int kFlags = kStepMax + 2 * 4 * 64 * 4;     // int[2][4]
+  static constexpr int kLRed = kFlags + 32;                    // float[4][64] row-sum parts
+  static constexpr int kJRow = kLRed + 4 * 64 * 4;             // int[64]: token j of row r
+  static constexpr int kInfo = kJRow + 64 * 4;                 // int4[2]
+  static constexpr int kBars = kInfo + 32;
+  // q_full[2] q_empty[2] s_full[2] s_free[2] p_full[2] pv_done[2] o_free drain flag[2]
+  // smax lred kv_full[kStages] kv_empty[kStages]
+  static constexpr int kNumBars = 18 + 2 * kStages;
+  static constexpr int kKvEmpty = 18 + kStages;  // first kv_empty barrier (after kv_full)
+  static constexpr int kTmem = kBars + kNumBars * 8;           // TMEM base address
+  static constexpr int kAbort = kTmem + 4;
+  static constexpr int kBytes = kAbort + 4;
+  static constexpr int kAlloc = kBytes + 1024;                 // room to align the base
+  // TMEM columns: S[0], S[1], O (Rp each), rounded up to a power of two >= 32
+  static constexpr int kTmemCols = 3 * kRp <= 32 ? 32 : 3 * kRp <= 64 ? 64 : 3 * kRp <= 128 ? 128 : 256;
+};
+
+enum TcBar : int {
+  B_Q_FULL = 0, B_Q_EMPTY = 2, B_S_FULL = 4, B_S_FREE = 6, B_P_FULL = 8, B_PV_DONE = 10,
+  B_O_FREE = 12, B_DRAIN = 13, B_FLAG = 14, B_SMAX = 16, B_LRED = 17, B_KV_FULL = 18
+};
+
+
+// ---- tcgen05 wrappers ---------------------------------------------------------------
+// Shared-memory matrix descriptor (sm_100 family): start, leading and stride byte
+// offsets in 16-byte units, version 1, 128-byte swizzle.
+__device__ __forceinline__ uint64_t tc_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+  return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) |
+         (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+}
+
+// Instruction descriptor: fp32 accumulate, M = 128, N = n; A/B formats (bf16 = 1 for
+// kind::f16, E4M3 = 0 for kind::f8f6f4) and major-ness (0 = K-major, 1 = MN-major).
+__device__ __forceinline__ uint32_t tc_idesc(int fmt, int n, int a_mn, int b_mn) {
+  return (1u << 4) | (static_cast<uint32_t>(fmt) << 7) | (static_cast<uint32_t>(fmt) << 10) |
+         (static_cast<uint32_t>(a_mn) << 15) | (static_cast<uint32_t>(b_mn) << 16) |
+         (static_cast<uint32_t>(n >> 3) << 17) | (static_cast<uint32_t>(128 >> 4) << 24);
+}
+
+template <int KV>
+__device__ __forceinline__ void tc_mma(uint32_t d, uint64_t a, uint64_t b, uint32_t idesc,
+                                       uint32_t acc) {
+  if (KV == HPA_KV_BF16)
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+  else
+    asm volatile(
+        "{\n\t.reg .pred p;\n\tsetp.ne.b32 p, %4, 0;\n\t"
+        "tcgen05.mma.cta_group::1.kind::f8f6f4 [%0], %1, %2, %3, p;\n\t}" ::"r"(d),
+        "l"(a), "l"(b), "r"(idesc), "r"(acc)
+        : "memory");
+}
+
+// Arrive on `bar` once every MMA this thread has issued so far has completed.
+__device__ __forceinline__ void tc_commit(uint32_t bar) {
+  asm volatile(
+      "tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// 16 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
+      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
+        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
+        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
+      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
+      : "memory");
+}
+
+__device__ __forceinline__ void tc_wait_ld() {
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void tc_wait_st() {
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ float warp_max(float x) {
+  float r;
+  asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
+  return r;
+}
+
+// Byte offset of (row r, byte kb) in a K-major operand with 128-byte swizzle:
+// 8-row atoms of 8 x 128 B, 16-byte chunk index XOR (row % 8).  Rows beyond the
+// first 128-byte column block live in the next block, `blk` bytes further on.
+__device__ __forceinline__ uint32_t kmaj(int r, int kb, uint32_t blk) {
+  return (kb >> 7) * blk + (r >> 3) * 1024 + (r & 7) * 128 + ((((kb & 127) >> 4) ^ (r & 7)) << 4) +
+         (kb & 15);
+}
+
+// ----------------------------------------------------------------------------- roles
+template <int KV, int NC>
+struct Tc {
+  using S = TcSmem<KV, NC>;
+  static constexpr int kRp = S::kRp;
+
+  // ---- warp 4: query staging and TMA copies
+  static __device__ void producer(const AttnParams &p, const CUtensorMap *tmk,
+                                  const CUtensorMap *tmv, uint8_t *smem, int s_begin,
+                                  int s_end, int tile, int h) {
+    const int lane = threadIdx.x & 31;
+    const uint32_t base = smem_u32(smem), bars = base + S::kBars;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kAbort);
+    uint64_t pol = 0;
+    if (lane == 0) {
+      pol = l2_policy_evict_first();
+      prefetch_tmap(tmk);
+      prefetch_tmap(tmv);
+    }
+    const int G = p.G, R = p.rows;
+    float ksc = 1.f;
+    if (KV == HPA_KV_E4M3) ksc = p.k_scale[h];
+    int st = 0;
+    uint32_t phase = 0, issued = 0, parity_bits = 0;
+    bool ok = true;
+    for (int s = s_begin; s < s_end && ok; ++s) {
+      const int k = s - s_begin, slot = k & 1;
+      const int4 sg = reinterpret_cast<const int4 *>(p.tm + p.lay.segs)[s];
+      const int r = sg.x, L = p.tm[p.lay.lens + r];
+      const int klo = sg.y * tile, khi = min(sg.z * tile, L);
+      const int pg0 = klo / PAGE, pg1 = (khi + PAGE - 1) / PAGE;
+      int good = 1;
+      if (lane == 0)
+        good = !*abort_flag && mbar_wait_bounded(bars + 8 * (B_Q_EMPTY + slot), ((k >> 1) & 1) ^ 1);
+      if (!__shfl_sync(kFull, good, 0)) {
+        ok = false;
+        break;
+      }
+      // query rows -> operand slot (K-major, 128-byte swizzle); lane l holds dims 4l..4l+3
+      uint8_t *qs = smem + S::kQ + slot * S::kOperand;
+      float *rowc = reinterpret_cast<float *>(smem + S::kRowC) + slot * 64;
+      for (int row = 0; row < kRp; ++row) {
+        float x[4] = {0.f, 0.f, 0.f, 0.f};
+        if (row < R) {
+          const int j = row / G, g = row % G;
+          const uint2 raw = reinterpret_cast<const uint2 *>(
+              p.q + ((static_cast<int64_t>(r) * p.q_len + j) * p.Hq + h * G + g) * HEAD_DIM)[lane];
+          const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
+          const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
+          x[0] = a.x, x[1] = a.y, x[2] = b.x, x[3] = b.y;
+        }
+        if (KV == HPA_KV_BF16) {
+          uint2 w;
+          w.x = pack_bf16(x[0], x[1]);
+          w.y = pack_bf16(x[2], x[3]);
+          *reinterpret_cast<uint2 *>(qs + kmaj(row, 8 * lane, kRp * 128)) = w;
+          if (lane == 0) rowc[row] = p.scale_log2;
+        } else {
+          float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+          amax = warp_max(amax);
+          // A power-of-two row scale keeps q * sq a bf16 value (8 significant bits), which
+          // hi + lo (4 + 4 bits) then carry exactly: amax * sq lands in [128, 256).
+          int ea = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127;
+          ea = min(max(ea, -119), 126);
+          const float sq = amax > 0.f ? __uint_as_float(static_cast<uint32_t>(127 + 7 - ea) << 23)
+                                      : 1.f;
+          uint32_t hi = 0, lo = 0;
+#pragma unroll
+          for (int e = 0; e < 4; e += 2) {
+            const float v0 = x[e] * sq, v1 = x[e + 1] * sq;
+            const uint16_t h2 = f32x2_to_e4m3x2(v0, v1);
+            const uint32_t hh = e4m3x2_to_f16x2(h2);
+            const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hh));
+            const uint16_t l2 = f32x2_to_e4m3x2(v0 - hf.x, v1 - hf.y);
+            hi |= static_cast<uint32_t>(h2) << (8 * e);
+            lo |= static_cast<uint32_t>(l2) << (8 * e);
+          }
+          *reinterpret_cast<uint32_t *>(qs + kmaj(row, 4 * lane, 0)) = hi;
+          *reinterpret_cast<uint32_t *>(qs + kRp * 128 + kmaj(row, 4 * lane, 0)) = lo;
+          if (lane == 0) rowc[row] = p.scale_log2 * ksc / sq;
+        }
+      }
+      if (lane == 0)
+        reinterpret_cast<int4 *>(smem + S::kInfo)[slot] = make_int4(r, L, klo, khi);
+      fence_proxy_async_smem();  // the MMA reads the slot through the async proxy
+      mbar_arrive(bars + 8 * (B_Q_FULL + slot));
+
+      // KV pages, two per stage
+      const int pstart = p.page_indptr[r];
+      const int pcount = p.page_indptr[r + 1] - pstart;
+      const int32_t *pidx = p.page_indices + pstart;
+      for (int pb = pg0; pb < pg1 && ok; pb += 64) {
+        int id[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+          const int pg = pb + 2 * lane + u;
+          id[u] = 0;
+          if (pg < pg1) {
+            id[u] = pg < pcount ? pidx[pg] : -1;
+            if (id[u] < 0 || id[u] >= p.num_pages) {
+              status_or(p.tm, HPA_STATUS_BAD_PAGE);
+              id[u] = 0;
+            }
+          }
+        }
+        const int npair = min(32, (pg1 - pb + 1) / 2);
+        for (int i = 0; i < npair; ++i) {
+          const int n = min(2, pg1 - (pb + 2 * i));
+          const int id0 = __shfl_sync(kFull, id[0], i), id1 = __shfl_sync(kFull, id[1], i);
+          int g2 = 1;
+          if (lane == 0) {
+            if (*abort_flag ||
+                !mbar_wait_bounded(bars + 8 * (S::kKvEmpty + st), phase ^ 1)) {
+              g2 = 0;
+            } else {
+              const uint32_t fb = bars + 8 * (B_KV_FULL + st);
+              const uint32_t dst = base + st * S::kStageBytes;
+              mbar_arrive_expect_tx(fb, n * 2 * TcCfg<KV>::kPageBytes);
+              for (int u = 0; u < n; ++u) {
+                const int z = (u ? id1 : id0) * p.Hkv + h;
+                if (KV == HPA_KV_BF16) {
+                  // [dim block][128 keys][128 B] for K, then the same for V
+                  tma_load_3d(dst + u * 8192, tmk, fb, 0, 0, z, pol);
+                  tma_load_3d(dst + 16384 + u * 8192, tmk, fb, 64, 0, z, pol);
+                  tma_load_3d(dst + S::kKPair + u * 8192, tmv, fb, 0, 0, z, pol);
+                  tma_load_3d(dst + S::kKPair + 16384 + u * 8192, tmv, fb, 64, 0, z, pol);
+                } else {
+                  tma_load_3d(dst + u * 8192, tmk, fb, 0, 0, z, pol);
+                  tma_load_3d(dst + S::kKPair + u * 8192, tmv, fb, 0, 0, z, pol);
+                }
+              }
+              issued |= 1u << st;
+              parity_bits = (parity_bits & ~(1u << st)) | (phase << st);
+            }
+          }
+          ok = __shfl_sync(kFull, g2, 0) != 0;
+          if (!ok) break;
+          if (++st == S::kStages) {
+            st = 0;
+            phase ^= 1;
+          }
+        }
+      }
+    }
+    if (!ok && lane == 0) {
+      status_or(p.tm, HPA_STATUS_TIMEOUT);
+      *abort_flag = 1;
+      for (int i = 0; i < S::kStages; ++i)  // never leave copies landing in shared memory
+        if (issued & (1u << i))
+          mbar_wait_bounded(bars + 8 * (B_KV_FULL + i), (parity_bits >> i) & 1u, 1000000000ull);
+    }
+  }
+
+  // ---- warp 5, one thread: every MMA
+  struct PvStep {
+    int i, st, first, k;
+  };
+
+  static __device__ bool issue_pv(const PvStep &v, uint8_t *smem, uint32_t tmem) {
+    const uint32_t base = smem_u32(smem), bars = base + S::kBars;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kAbort);
+    const int b = v.i & 1;
+    if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_P_FULL + b), (v.i >> 1) & 1)) return false;
+    if (v.first && v.k > 0 &&
+        (*abort_flag || !mbar_wait_bounded(bars + 8 * B_O_FREE, (v.k - 1) & 1)))
+      return false;
+    tc_fence_after();
+    const uint32_t vbase = base + v.st * S::kStageBytes + S::kKPair;
+    const uint32_t pbase = base + S::kP + b * S::kOperand;
+    const uint32_t o_t = tmem + 2 * kRp;
+    if (KV == HPA_KV_BF16) {
+      const uint32_t idv = tc_idesc(1, kRp, 1, 0);
+#pragma unroll
+      for (int kk = 0; kk < 8; ++kk)  // 16 keys per MMA
+        tc_mma<KV>(o_t, tc_desc(vbase + kk * 2048, 16384, 1024),
+                   tc_desc(pbase + (kk >> 2) * (kRp * 128) + (kk & 3) * 32, 16, 1024), idv,
+                   !v.first || kk > 0);
+    } else {
+      const uint32_t idv = tc_idesc(0, kRp, 1, 0);
+#pragma unroll
+      for (int part = 0; part < 2; ++part)  // P = hi + lo
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk)  // 32 keys per MMA
+          tc_mma<KV>(o_t, tc_desc(vbase + kk * 4096, 8192, 1024),
+                     tc_desc(pbase + part * (kRp * 128) + kk * 32, 16, 1024), idv,
+                     !v.first || part > 0 || kk > 0);
+    }
+    tc_commit(bars + 8 * (S::kKvEmpty + v.st));  // the page pair may be refilled
+    tc_commit(bars + 8 * (B_PV_DONE + b));      // P[b] is free; O is current
+    return true;
+  }
+
+  static __device__ void mma_issuer(const AttnParams &p, uint8_t *smem, int s_begin, int s_end,
+                                    int tile, uint32_t tmem) {
+    const uint32_t base = smem_u32(smem), bars = base + S::kBars;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kAbort);
+    int i = 0, st = 0;
+    uint32_t phase = 0;
+    bool ok = true, have = false;
+    PvStep prev{0, 0, 0, 0};
+    for (int s = s_begin; s < s_end && ok; ++s) {
+      const int k = s - s_begin, slot = k & 1;
+      const int4 sg = reinterpret_cast<const int4 *>(p.tm + p.lay.segs)[s];
+      const int L = p.tm[p.lay.lens + sg.x];
+      const int pg0 = sg.y * tile / PAGE, pg1 = (min(sg.z * tile, L) + PAGE - 1) / PAGE;
+      const int npairs = (pg1 - pg0 + 1) / 2;
+      if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_Q_FULL + slot), (k >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      const uint32_t qbase = base + S::kQ + slot * S::kOperand;
+      for (int j = 0; j < npairs; ++j) {
+        const int b = i & 1;
+        if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_KV_FULL + st), phase) ||
+            !mbar_wait_bounded(bars + 8 * (B_S_FREE + b), ((i >> 1) & 1) ^ 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t kbase = base + st * S::kStageBytes;
+        const uint32_t s_t = tmem + b * kRp;
+        if (KV == HPA_KV_BF16) {
+          const uint32_t id = tc_idesc(1, kRp, 0, 0);
+#pragma unroll
+          for (int kk = 0; kk < 8; ++kk)  // 16 dims per MMA
+            tc_mma<KV>(s_t, tc_desc(kbase + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
+                       tc_desc(qbase + (kk >> 2) * (kRp * 128) + (kk & 3) * 32, 16, 1024), id,
+                       kk > 0);
+        } else {
+          const uint32_t id = tc_idesc(0, kRp, 0, 0);
+#pragma unroll
+          for (int part = 0; part < 2; ++part)  // Q = hi + lo
+#pragma unroll
+            for (int kk = 0; kk < 4; ++kk)  // 32 dims per MMA
+              tc_mma<KV>(s_t, tc_desc(kbase + kk * 32, 16, 1024),
+                         tc_desc(qbase + part * (kRp * 128) + kk * 32, 16, 1024), id,
+                         part > 0 || kk > 0);
+        }
+        tc_commit(bars + 8 * (B_S_FULL + b));
+        if (j == npairs - 1) tc_commit(bars + 8 * (B_Q_EMPTY + slot));
+        if (have && !issue_pv(prev, smem, tmem)) {
+          ok = false;
+          break;
+        }
+        prev = PvStep{i, st, j == 0, k};
+        have = true;
+        ++i;
+        if (++st == S::kStages) {
+          st = 0;
+          phase ^= 1;
+        }
+      }
+    }
+    if (ok && have) ok = issue_pv(prev, smem, tmem);
+    if (!ok) {
+      status_or(p.tm, HPA_STATUS_TIMEOUT);
+      *abort_flag = 1;
+    }
+    // every MMA complete before the CTA frees its TMEM
+    tc_commit(bars + 8 * B_DRAIN);
+    mbar_wait_bounded(bars + 8 * B_DRAIN, 0, 1000000000ull);
+  }
+
+  // ---- warps 0-3: softmax and the segment epilogue
+  static __device__ void compute(const AttnParams &p, uint8_t *smem, int s_begin, int s_end,
+                                 uint32_t tmem, int h) {
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31;
+    const uint32_t base = smem_u32(smem), bars = base + S::kBars;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kAbort);
+    const uint32_t lane_t = tmem + (static_cast<uint32_t>(32 * w) << 16);
+    const int G = p.G, R = p.rows, q_len = p.q_len;
+    const float vsc = KV == HPA_KV_E4M3 ? p.v_scale[h] : 1.f;
+    constexpr float kSlack = TcCfg<KV>::kSlack, kPOff = TcCfg<KV>::kPOff;
+    float *stepmax = reinterpret_cast<float *>(smem + S::kStepMax);
+    int *flags = reinterpret_cast<int *>(smem + S::kFlags);
+    int i = 0, n_moved = 0, n_seg = 0;
+    bool ok = true;
+    for (int s = s_begin; s < s_end && ok; ++s) {
+      const int k = s - s_begin, slot = k & 1;
+      if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_Q_FULL + slot), (k >> 1) & 1)) {
+        ok = false;
+        break;
+      }
+      const int4 inf = reinterpret_cast<const int4 *>(smem + S::kInfo)[slot];
+      const int L = inf.y, klo = inf.z, khi = inf.w;
+      const int pg0 = klo / PAGE, pg1 = (khi + PAGE - 1) / PAGE;
+      const int npairs = (pg1 - pg0 + 1) / 2;
+      if (L < q_len && t == 0) status_or(p.tm, HPA_STATUS_BAD_SEQLEN);
+      const float *rowc = reinterpret_cast<const float *>(smem + S::kRowC) + slot * 64;
+      const int *jrow = reinterpret_cast<const int *>(smem + S::kJRow);
+      float mref[kRp], lsum[kRp];  // reference max per row; this key slot's share of l
+#pragma unroll
+      for (int r = 0; r < kRp; ++r) {
+        mref[r] = -CUDART_INF_F;
+        lsum[r] = 0.f;
+      }
+
+      for (int jp = 0; jp < npairs; ++jp) {
+        const int b = i & 1, st = i % S::kStages;
+        if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_S_FULL + b), (i >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        float x[kRp];
+#pragma unroll
+        for (int c = 0; c < NC; ++c) {
+          float v[16];
+          tc_ld16(lane_t + b * kRp + 16 * c, v);
+#pragma unroll
+          for (int e = 0; e < 16; ++e) x[16 * c + e] = v[e];
+        }
+        tc_wait_ld();
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + 8 * (B_S_FREE + b));
+
+        const int pg = pg0 + 2 * jp, key = pg * PAGE + t;
+        const bool present = key < pg1 * PAGE;  // the pair's second page may be missing
+        // row r (token j = r / G) sees keys < L - q_len + 1 + j
+        const int d0 = present ? key - (L - q_len + 1) : INT_MAX;
+        bool flag = false;
+#pragma unroll
+        for (int r = 0; r < kRp; ++r) {
+          const bool live = r < R && d0 < jrow[r];
+          x[r] = live ? x[r] * rowc[r] : -CUDART_INF_F;
+          flag |= x[r] > mref[r] + kSlack;
+        }
+        // A reference max moves only when some score exceeds it by more than the slack.
+        // The four warps agree through mbarriers (bounded waits), never named barriers:
+        // a warp that gives up must not leave the others waiting without a limit.
+        {
+          const bool any = __any_sync(kFull, flag);
+          if (lane == 0) {
+            flags[b * 4 + w] = any;
+            mbar_arrive(bars + 8 * (B_FLAG + b));
+          }
+        }
+        if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_FLAG + b), (i >> 1) & 1)) {
+          ok = false;
+          break;
+        }
+        const bool moved = flags[b * 4] | flags[b * 4 + 1] | flags[b * 4 + 2] | flags[b * 4 + 3];
+        if (moved) {
+          float *sm = stepmax + (n_moved & 1) * 4 * 64;
+#pragma unroll
+          for (int r = 0; r < kRp; ++r) {
+            const float mx = warp_max(x[r]);
+            if (lane == 0) sm[w * 64 + r] = mx;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars + 8 * B_SMAX);
+          if (*abort_flag || !mbar_wait_bounded(bars + 8 * B_SMAX, n_moved & 1)) {
+            ok = false;
+            break;
+          }
+          ++n_moved;
+          float alpha[kRp];
+          bool rescale = false;
+#pragma unroll
+          for (int r = 0; r < kRp; ++r) {
+            const float mn = fmaxf(fmaxf(fmaxf(sm[r], sm[64 + r]), fmaxf(sm[128 + r], sm[192 + r])),
+                                   mref[r]);
+            alpha[r] = mn == mref[r] ? 1.f : exp2f(mref[r] - mn);  // 0 from -inf
+            rescale |= alpha[r] != 1.f;
+            mref[r] = mn;
+            lsum[r] *= alpha[r];
+          }
+          if (jp > 0 && rescale) {
+            // O holds the earlier pairs of this segment: wait for the last P V, then
+            // rescale it in TMEM (this thread's lane = output dim t)
+            const int pi = i - 1;
+            if (*abort_flag ||
+                !mbar_wait_bounded(bars + 8 * (B_PV_DONE + (pi & 1)), (pi >> 1) & 1)) {
+              ok = false;
+              break;
+            }
+            tc_fence_after();
+#pragma unroll
+            for (int c = 0; c < NC; ++c) {
+              float o[16];
+              tc_ld16(lane_t + 2 * kRp + 16 * c, o);
+              tc_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 16; ++e) o[e] *= alpha[16 * c + e];
+              tc_st16(lane_t + 2 * kRp + 16 * c, o);
+            }
+            tc_wait_st();
+            tc_fence_before();
+          }
+        }
+        // P[b] is free once the P V of two steps back has completed
+        if (i >= 2 && (*abort_flag ||
+                       !mbar_wait_bounded(bars + 8 * (B_PV_DONE + b), ((i - 2) >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+        uint8_t *pb = smem + S::kP + b * S::kOperand;
+        if (KV == HPA_KV_BF16) {
+#pragma unroll
+          for (int r = 0; r < kRp; r += 2) {
+            const float b0 = mref[r] == -CUDART_INF_F ? 0.f : mref[r];
+            const float b1 = mref[r + 1] == -CUDART_INF_F ? 0.f : mref[r + 1];
+            const float p0 = exp2f(x[r] - b0), p1 = exp2f(x[r + 1] - b1);
+            lsum[r] += p0;
+            lsum[r + 1] += p1;
+            const uint32_t pk = pack_bf16(p0, p1);
+            *reinterpret_cast<uint16_t *>(pb + kmaj(r, 2 * t, kRp * 128)) =
+                static_cast<uint16_t>(pk & 0xffffu);
+            *reinterpret_cast<uint16_t *>(pb + kmaj(r + 1, 2 * t, kRp * 128)) =
+                static_cast<uint16_t>(pk >> 16);
+          }
+        } else {
+#pragma unroll
+          for (int r = 0; r < kRp; r += 2) {
+            const float b0 = mref[r] == -CUDART_INF_F ? 0.f : mref[r];
+            const float b1 = mref[r + 1] == -CUDART_INF_F ? 0.f : mref[r + 1];
+            const float p0 = exp2f(x[r] - b0 + kPOff), p1 = exp2f(x[r + 1] - b1 + kPOff);
+            lsum[r] += p0;
+            lsum[r + 1] += p1;
+            const uint16_t h2 = f32x2_to_e4m3x2(p0, p1);
+            const uint32_t hh = e4m3x2_to_f16x2(h2);
+            const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hh));
+            const uint16_t l2 = f32x2_to_e4m3x2(p0 - hf.x, p1 - hf.y);
+            pb[kmaj(r, t, 0)] = static_cast<uint8_t>(h2 & 0xff);
+            pb[kmaj(r + 1, t, 0)] = static_cast<uint8_t>(h2 >> 8);
+            pb[kRp * 128 + kmaj(r, t, 0)] = static_cast<uint8_t>(l2 & 0xff);
+            pb[kRp * 128 + kmaj(r + 1, t, 0)] = static_cast<uint8_t>(l2 >> 8);
+          }
+        }
+        // V rows of keys past the request (or of a missing page) must be finite: zero them
+        if (!present || key >= L) {
+          uint8_t *vr = smem + st * S::kStageBytes + S::kKPair + (t >> 3) * 1024 + (t & 7) * 128;
+          const int4 z = make_int4(0, 0, 0, 0);
+#pragma unroll
+          for (int c = 0; c < 8; ++c) {
+            reinterpret_cast<int4 *>(vr)[c] = z;
+            if (KV == HPA_KV_BF16) reinterpret_cast<int4 *>(vr + 16384)[c] = z;
+          }
+        }
+        fence_proxy_async_smem();  // generic writes before the MMA reads them
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + 8 * (B_P_FULL + b));
+
+        if (jp == npairs - 1) {
+          // ---- segment end: l per row (sum over the 128 key slots), then O / l for
+          // every row, this thread's dim t
+          float *lred = reinterpret_cast<float *>(smem + S::kLRed);
+#pragma unroll
+          for (int r = 0; r < kRp; ++r) {
+            float v = lsum[r];
+#pragma unroll
+            for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
+            if (lane == 0) lred[w * 64 + r] = v;
+          }
+          __syncwarp();
+          if (lane == 0) mbar_arrive(bars + 8 * B_LRED);
+          if (*abort_flag || !mbar_wait_bounded(bars + 8 * B_LRED, n_seg & 1) ||
+              !mbar_wait_bounded(bars + 8 * (B_PV_DONE + b), (i >> 1) & 1)) {
+            ok = false;
+            break;
+          }
+          ++n_seg;
+          tc_fence_after();
+#pragma unroll
+          for (int c = 0; c < NC; ++c) {
+            float o[16];
+            tc_ld16(lane_t + 2 * kRp + 16 * c, o);
+            tc_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 16; ++e) {
+              const int r = 16 * c + e;
+              const float l = lred[r] + lred[64 + r] + lred[128 + r] + lred[192 + r];
+              if (r < R) {
+                const int j = jrow[r], g = r - j * G;
+                const int64_t row = (static_cast<int64_t>(s) * q_len + j) * p.Hq + h * G + g;
+                p.partial_o[row * HEAD_DIM + t] = l > 0.f ? o[e] / l * vsc : 0.f;
+              }
+              if (r == t && t < R) {  // thread r writes row r's lse
+                const int j = jrow[r], g = r - j * G;
+                const int64_t row = (static_cast<int64_t>(s) * q_len + j) * p.Hq + h * G + g;
+                p.partial_lse[row] = l > 0.f
+                                         ? (mref[r] - kPOff + log2f(l)) * 0.69314718055994531f
+                                         : -CUDART_INF_F;
+              }
+            }
+          }
+          tc_fence_before();
+          __syncwarp();
+          if (lane == 0) {
+            mbar_arrive(bars + 8 * B_O_FREE);              // O may be overwritten
+            mbar_arrive(bars + 8 * (B_Q_EMPTY + slot));    // the query slot may be refilled
+          }
+        }
+        ++i;
+      }
+    }
+    if (!ok && t == 0) {
+      status_or(p.tm, HPA_STATUS_TIMEOUT);
+      *abort_flag = 1;
+    }
+  }
+};
+
+template <int KV, int NC>
+__global__ void __launch_bounds__(kTcThreads, 1)
+    decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tmk,
+                          const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
+  using S = TcSmem<KV, NC>;
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t *smem = reinterpret_cast<uint8_t *>(
+      (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
+  const int c = blockIdx.x, h = blockIdx.y;
+  __shared__ int hdr[4];  // go, tile, s_begin, s_end
+  const uint32_t base = smem_u32(smem), bars = base + S::kBars;
+  pdl_wait();
+  if (threadIdx.x == 0) {
+    const int32_t *tm = p.tm;
+    const int tile = tm[TM_TILE];
+    int go = tm[TM_STATUS] == 0;
+    if (go && (tm[TM_B] != p.B || tm[TM_C] != p.C || tile <= 0 || tile % PAGE != 0)) {
+      if (c == 0 && h == 0) status_or(p.tm, HPA_STATUS_MISMATCH);
+      go = 0;
+    }
+    hdr[1] = tile;
+    hdr[2] = go ? tm[p.lay.cta_seg + c] : 0;
+    hdr[3] = go ? tm[p.lay.cta_seg + c + 1] : 0;
+    hdr[0] = go && hdr[2] < hdr[3];
+    // q_full q_empty s_full s_free p_full pv_done o_free drain flag smax lred
+    const int counts[18] = {32, 32, 1 + kTcComputeWarps, 1 + kTcComputeWarps, 1, 1,
+                            kTcComputeWarps, kTcComputeWarps, kTcComputeWarps, kTcComputeWarps,
+                            1, 1, kTcComputeWarps, 1, kTcComputeWarps, kTcComputeWarps,
+                            kTcComputeWarps, kTcComputeWarps};
+    for (int i = 0; i < 18; ++i) mbar_init(bars + 8 * i, counts[i]);
+    for (int i = 0; i < S::kStages; ++i) {
+      mbar_init(bars + 8 * (B_KV_FULL + i), 1);                 // TMA bytes
+      mbar_init(bars + 8 * (S::kKvEmpty + i), 1);      // MMA commit
+    }
+    for (int r = 0; r < 64; ++r) reinterpret_cast<int *>(smem + S::kJRow)[r] = r / p.G;
+    *reinterpret_cast<int *>(smem + S::kAbort) = 0;
+    fence_barrier_init();
+  }
+  __syncthreads();
+  pdl_launch_dependents();
+  if (!hdr[0]) return;  // bad map, or a partition with no tiles
+  if (threadIdx.x < 32) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
+                     base + S::kTmem),
+                 "r"(S::kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + S::kTmem);
+  const int tile = hdr[1], s_begin = hdr[2], s_end = hdr[3];
+  const int warp = threadIdx.x >> 5;
+  if (warp < kTcComputeWarps)
+    Tc<KV, NC>::compute(p, smem, s_begin, s_end, tmem, h);
+  else if (warp == kTcComputeWarps)
+    Tc<KV, NC>::producer(p, &tmk, &tmv, smem, s_begin, s_end, tile, h);
+  else if ((threadIdx.x & 31) == 0)
+    Tc<KV, NC>::mma_issuer(p, smem, s_begin, s_end, tile, tmem);
+  tc_fence_before();
+  __syncthreads();
+  if (threadIdx.x < 32) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
+                 "r"(S::kTmemCols)
+                 : "memory");
+  }
+}
+
+template <int KV, int NC>
+cudaError_t launch_tc(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                      cudaStream_t s) {
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(decode_attn_tc_kernel<KV, NC>,
+                             cudaFuncAttributeMaxDynamicSharedMemorySize, TcSmem<KV, NC>::kAlloc);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.C, p.Hkv, 1);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = TcSmem<KV, NC>::kAlloc;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, decode_attn_tc_kernel<KV, NC>, tmk, tmv, p);
+}
+
+template <int KV>
+cudaError_t launch_tc_kv(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
+                         cudaStream_t s) {
+  switch ((p.rows + 15) / 16) {
+    case 1: return launch_tc<KV, 1>(p, tmk, tmv, s);
+    case 2: return launch_tc<KV, 2>(p, tmk, tmv, s);
+    case 3: return launch_tc<KV, 3>(p, tmk, tmv, s);
+    default: return launch_tc<KV, 4>(p, tmk, tmv, s);
+  }
+}
+
+template <int KV, int NC>
+int occupancy_tc(int *ctas) {
+  cudaError_t e = cudaFuncSetAttribute(decode_attn_tc_kernel<KV, NC>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       TcSmem<KV, NC>::kAlloc);
+  if (e != cudaSuccess) return -1;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, decode_attn_tc_kernel<KV, NC>,
+                                                    kTcThreads, TcSmem<KV, NC>::kAlloc);
+  return e == cudaSuccess ? 0 : -1;
+}
+
+template <int KV>
+int occupancy_tc_kv(int rows, int *ctas) {
+  switch ((rows + 15) / 16) {
+    case 1: return occupancy_tc<KV, 1>(ctas);
+    case 2: return occupancy_tc<KV, 2>(ctas);
+    case 3: return occupancy_tc<KV, 3>(ctas);
+    default: return occupancy_tc<KV, 4>(ctas);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_decode_attn_tc(const AttnParams &p, const CUtensorMap &tmk,
+                                  const CUtensorMap &tmv, int kv_dtype, cudaStream_t s) {
+  return kv_dtype == HPA_KV_BF16 ? launch_tc_kv<HPA_KV_BF16>(p, tmk, tmv, s)
+                                 : launch_tc_kv<HPA_KV_E4M3>(p, tmk, tmv, s);
+}
+
+int attn_tc_ctas_per_sm(int kv_dtype, int rows, int *ctas) {
+  return kv_dtype == HPA_KV_BF16 ? occupancy_tc_kv<HPA_KV_BF16>(rows, ctas)
+                                 : occupancy_tc_kv<HPA_KV_E4M3>(rows, ctas);
+}
+
+}  // namespace hpa

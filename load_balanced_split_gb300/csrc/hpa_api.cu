@@ -191,7 +191,7 @@ static int decode_attn_impl(const void *q_dev, const void *k_pool_dev, const voi
                             int32_t d, float sm_scale, void *taskmap_dev, int32_t num_ctas,
                             float *partial_o_dev, float *partial_lse_dev, uint64_t *trace_dev,
                             void *out_dev, float *out_lse_dev, int32_t *arrivals_dev,
-                            hpa_stream_t stream) {
+                            hpa_stream_t stream, bool tc = false) {
   if (!q_dev || !k_pool_dev || !v_pool_dev || !page_indptr_dev || !page_indices_dev ||
       !taskmap_dev || !partial_o_dev || !partial_lse_dev)
     return HPA_ERR_INVALID;
@@ -234,9 +234,41 @@ static int decode_attn_impl(const void *q_dev, const void *k_pool_dev, const voi
   p.G = Hq / Hkv;
   p.rows = p.G * q_len;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
-  cudaError_t e = hpa::launch_decode_attn(p, tmk, tmv, kv_dtype,
-                                          reinterpret_cast<cudaStream_t>(stream));
+  cudaError_t e =
+      tc ? hpa::launch_decode_attn_tc(p, tmk, tmv, kv_dtype, reinterpret_cast<cudaStream_t>(stream))
+         : hpa::launch_decode_attn(p, tmk, tmv, kv_dtype, reinterpret_cast<cudaStream_t>(stream));
   return e == cudaSuccess ? HPA_OK : cuda_fail(e);
+}
+
+int hpa_decode_attn_tc(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
+                       int32_t kv_dtype, const float *k_scale_dev, const float *v_scale_dev,
+                       int64_t num_pages, const int32_t *page_indptr_dev,
+                       const int32_t *page_indices_dev, int32_t page_size, int32_t B,
+                       int32_t q_len, int32_t Hq, int32_t Hkv, int32_t d, float sm_scale,
+                       void *taskmap_dev, int32_t num_ctas, float *partial_o_dev,
+                       float *partial_lse_dev, hpa_stream_t stream) {
+  return decode_attn_impl(q_dev, k_pool_dev, v_pool_dev, kv_dtype, k_scale_dev, v_scale_dev,
+                          num_pages, page_indptr_dev, page_indices_dev, page_size, B, q_len, Hq,
+                          Hkv, d, sm_scale, taskmap_dev, num_ctas, partial_o_dev,
+                          partial_lse_dev, nullptr, nullptr, nullptr, nullptr, stream, true);
+}
+
+int32_t hpa_default_num_ctas_tc(int32_t Hq, int32_t Hkv, int32_t q_len, int32_t kv_dtype) {
+  if (Hkv < 1 || Hq < Hkv || Hq % Hkv != 0 || q_len < 1 ||
+      int64_t(Hq / Hkv) * q_len > hpa::MAX_ROWS_TOTAL ||
+      (kv_dtype != HPA_KV_BF16 && kv_dtype != HPA_KV_E4M3))
+    return -1;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    g_last_cuda_error = static_cast<int>(e);
+    return -1;
+  }
+  if (hpa::attn_tc_ctas_per_sm(kv_dtype, (Hq / Hkv) * q_len, &per_sm) != 0 || per_sm < 1)
+    return -1;
+  const int c = sms * per_sm / Hkv;
+  return c < 1 ? 1 : c;
 }
 
 int hpa_decode_attn(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,

@@ -67,6 +67,9 @@ cudaError_t launch_combine(const float *po, const float *plse, int32_t *tm, int 
 cudaError_t launch_decode_attn(const AttnParams &p, const CUtensorMap &tmk,
                                const CUtensorMap &tmv, int kv_dtype, cudaStream_t s);
 int attn_ctas_per_sm(int kv_dtype, int q_len, int *ctas);  // occupancy query (host)
+cudaError_t launch_decode_attn_tc(const AttnParams &p, const CUtensorMap &tmk,
+                                  const CUtensorMap &tmv, int kv_dtype, cudaStream_t s);
+int attn_tc_ctas_per_sm(int kv_dtype, int rows, int *ctas);  // occupancy query (host)
 cudaError_t launch_selftest_wait(int32_t *status, long long limit_ns, cudaStream_t s);
 
 struct StoreKvParams {

@@ -54,6 +54,9 @@ def lib():
                 "hpa_plan_weighted": ([P, I32, I32, I32, P, SZ, P], ctypes.c_int),
                 "hpa_decode_attn": ([P, P, P, I32, P, P, I64, P, P, I32, I32, I32, I32, I32,
                                      I32, F, P, I32, P, P, P], ctypes.c_int),
+                "hpa_decode_attn_tc": ([P, P, P, I32, P, P, I64, P, P, I32, I32, I32, I32, I32,
+                                        I32, F, P, I32, P, P, P], ctypes.c_int),
+                "hpa_default_num_ctas_tc": ([I32, I32, I32, I32], I32),
                 "hpa_decode_attn_traced": ([P, P, P, I32, P, P, I64, P, P, I32, I32, I32, I32,
                                             I32, I32, F, P, I32, P, P, P, P], ctypes.c_int),
                 "hpa_combine": ([P, P, P, I32, I32, I32, I32, I32, P, P, P], ctypes.c_int),
@@ -129,6 +132,14 @@ def hpa_default_num_ctas(Hkv: int, q_len: int, kv_dtype: int, Hq: int = 64) -> i
     return c
 
 
+def hpa_default_num_ctas_tc(Hkv: int, q_len: int, kv_dtype: int, Hq: int = 64) -> int:
+    c = int(lib().hpa_default_num_ctas_tc(Hq, Hkv, q_len, kv_dtype))
+    if c <= 0:
+        raise HpaError("hpa_default_num_ctas_tc failed (cudaError %d)" %
+                       lib().hpa_last_cuda_error())
+    return c
+
+
 # ----------------------------------------------------------------------------- the three calls
 def hpa_plan(seq_lens, tile: int, num_ctas: int, taskmap, stream=None):
     _dev(seq_lens, "seq_lens", torch.int32)
@@ -155,8 +166,10 @@ def hpa_plan_static(seq_lens, tile: int, splits: int, taskmap, stream=None):
 
 def hpa_decode_attn(q, k_pool, v_pool, page_indptr, page_indices, taskmap, num_ctas: int,
                     partial_o, partial_lse, k_scale=None, v_scale=None,
-                    sm_scale: float | None = None, stream=None):
-    """q bf16 [B][q_len][Hq][d]; k/v pools bf16 or uint8 (E4M3) [P][Hkv][page][d]."""
+                    sm_scale: float | None = None, stream=None, tc: bool = False):
+    """q bf16 [B][q_len][Hq][d]; k/v pools bf16 or uint8 (E4M3) [P][Hkv][page][d].
+
+    tc=True calls hpa_decode_attn_tc (the tcgen05 kernel) with the same arguments."""
     _dev(q, "q", torch.bfloat16)
     _dev(k_pool, "k_pool")
     _dev(v_pool, "v_pool")
@@ -184,11 +197,19 @@ def hpa_decode_attn(q, k_pool, v_pool, page_indptr, page_indices, taskmap, num_c
         raise HpaError("partial buffers too small: need (B + num_ctas - 1) segments")
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(d)
-    _check(lib().hpa_decode_attn(
+    name = "hpa_decode_attn_tc" if tc else "hpa_decode_attn"
+    _check(getattr(lib(), name)(
         _ptr(q), _ptr(k_pool), _ptr(v_pool), kv, _ptr(k_scale), _ptr(v_scale), P,
         _ptr(page_indptr), _ptr(page_indices), page, B, q_len, Hq, Hkv, d, float(sm_scale),
-        _ptr(taskmap), num_ctas, _ptr(partial_o), _ptr(partial_lse), _stream(stream)),
-        "hpa_decode_attn")
+        _ptr(taskmap), num_ctas, _ptr(partial_o), _ptr(partial_lse), _stream(stream)), name)
+
+
+def hpa_decode_attn_tc(q, k_pool, v_pool, page_indptr, page_indices, taskmap, num_ctas: int,
+                       partial_o, partial_lse, k_scale=None, v_scale=None,
+                       sm_scale: float | None = None, stream=None):
+    """hpa_decode_attn computed on the tcgen05 tensor cores (one pass for up to 64 rows)."""
+    hpa_decode_attn(q, k_pool, v_pool, page_indptr, page_indices, taskmap, num_ctas, partial_o,
+                    partial_lse, k_scale, v_scale, sm_scale, stream, tc=True)
 
 
 def hpa_decode_attn_traced(q, k_pool, v_pool, page_indptr, page_indices, taskmap, num_ctas: int,
@@ -393,10 +414,14 @@ class Workspace:
 
 def decode_step(ws: Workspace, q, k_pool, v_pool, seq_lens, page_indptr, page_indices, out,
                 out_lse=None, k_scale=None, v_scale=None, tile=512, plan=True, stream=None,
-                fused=False):
+                fused=False, tc=False):
     """plan (optional) -> split-KV attention -> combine, all enqueued on one stream.
 
-    fused=True runs the attention kernel with the combine folded in (one launch)."""
+    fused=True runs the attention kernel with the combine folded in (one launch);
+    tc=True runs the tcgen05 attention kernel (size the workspace with
+    hpa_default_num_ctas_tc)."""
+    if fused and tc:
+        raise HpaError("the tcgen05 kernel has no fused-combine variant")
     if plan:
         ws.plan(seq_lens, tile, stream)
     if fused:
@@ -405,5 +430,5 @@ def decode_step(ws: Workspace, q, k_pool, v_pool, seq_lens, page_indptr, page_in
                               out_lse, k_scale, v_scale, stream=stream)
         return
     hpa_decode_attn(q, k_pool, v_pool, page_indptr, page_indices, ws.taskmap, ws.num_ctas,
-                    ws.partial_o, ws.partial_lse, k_scale, v_scale, stream=stream)
+                    ws.partial_o, ws.partial_lse, k_scale, v_scale, stream=stream, tc=tc)
     hpa_combine(ws.partial_o, ws.partial_lse, ws.taskmap, ws.num_ctas, out, out_lse, stream)

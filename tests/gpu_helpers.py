@@ -71,19 +71,20 @@ class DeviceBatch:
         self.indices = torch.from_numpy(b.page_indices).to(device)
 
 
-def num_ctas_for(b) -> int:
+def num_ctas_for(b, tc=False) -> int:
     if b.num_ctas is not None:
         return b.num_ctas
-    return hpa.hpa_default_num_ctas(b.Hkv, b.q_len, hpa.KV_BF16 if b.kv_dtype == "bf16"
-                                    else hpa.KV_E4M3, b.Hq)
+    fn = hpa.hpa_default_num_ctas_tc if tc else hpa.hpa_default_num_ctas
+    return fn(b.Hkv, b.q_len, hpa.KV_BF16 if b.kv_dtype == "bf16" else hpa.KV_E4M3, b.Hq)
 
 
-def run_gpu(b, num_ctas=None, splits=None, tile=512, db=None, fused=False, weighted=False):
+def run_gpu(b, num_ctas=None, splits=None, tile=512, db=None, fused=False, weighted=False,
+            tc=False):
     """plan -> attention -> combine on the GPU (fused: one attention launch with the
-    combine folded in).  Returns host numpy results."""
+    combine folded in; tc: the tcgen05 attention kernel).  Returns host numpy results."""
     db = db or DeviceBatch(b)
     if splits is None and num_ctas is None:
-        num_ctas = num_ctas_for(b)
+        num_ctas = num_ctas_for(b, tc)
     ws = hpa.Workspace(b.B, b.q_len, b.Hq, b.d, num_ctas=num_ctas, splits=splits,
                        weighted=weighted)
     ws.partial_o.fill_(float("nan"))
@@ -91,7 +92,7 @@ def run_gpu(b, num_ctas=None, splits=None, tile=512, db=None, fused=False, weigh
     out = torch.empty((b.B, b.q_len, b.Hq, b.d), dtype=torch.bfloat16, device="cuda")
     out_lse = torch.empty((b.B, b.q_len, b.Hq), dtype=torch.float32, device="cuda")
     hpa.decode_step(ws, db.q, db.k, db.v, db.lens, db.indptr, db.indices, out, out_lse,
-                    db.ks, db.vs, tile=tile, fused=fused)
+                    db.ks, db.vs, tile=tile, fused=fused, tc=tc)
     torch.cuda.synchronize()
     if fused:
         assert int(ws.arrivals.abs().sum().item()) == 0, "arrival counters not reset"

@@ -1,0 +1,109 @@
+"""The tcgen05 attention kernel (hpa_decode_attn_tc) against the fp64 oracle.
+
+Same checks as the mma.sync kernel's tests: the task map bit-exactly, every
+segment's partial (o, lse) against the oracle over that segment's keys, and
+the combined output and lse against unsplit attention.  The cases cover
+what is particular to this kernel: two pages per step (odd page counts, a
+missing second page), all G * q_len rows (up to 64) in one CTA, query rows
+and probabilities carried as two E4M3 terms, and the reference-max moves
+that rescale O and L in tensor memory."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+import workloads as W
+from gpu_helpers import assert_close, assert_lse_close, expect_taskmap_equal, run_gpu
+
+pytestmark = pytest.mark.gpu
+
+
+def check(b, num_ctas=None, splits=None, tile=512):
+    g = run_gpu(b, num_ctas=num_ctas, splits=splits, tile=tile, tc=True)
+    ref_plan = (oracle.plan(b.seq_lens, tile, g["num_ctas"]) if splits is None
+                else oracle.plan_static(b.seq_lens, tile, splits))
+    expect_taskmap_equal(g["tm"], ref_plan, g["capacity"])
+    po, pl = oracle.split_attention(b, ref_plan)
+    assert_close(g["po"], po, b.kv_dtype, "partial_o")
+    assert_lse_close(g["pl"], pl, "partial_lse")
+    out, lse = oracle.attention(b)
+    err = assert_close(g["out"], out, b.kv_dtype, "out")
+    assert_lse_close(g["lse"], lse, "out_lse")
+    return g, err
+
+
+def test_worked_example():
+    check(W.make_config(1))
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+@pytest.mark.parametrize("q_len", [1, 2, 3, 4, 8])
+def test_ragged_batch(kv, q_len):
+    lens = [q_len, 63, 64, 65, 128, 129, 511, 513, 1000, 3333, 4096 + 17]
+    b = W.make_batch(lens, q_len=q_len, kv_dtype=kv, seed=200 + q_len)
+    check(b, num_ctas=7)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+@pytest.mark.parametrize("C", [1, 3, 40])
+def test_partition_counts(kv, C):
+    b = W.make_batch([100, 700, 30, 5000], q_len=2, kv_dtype=kv, seed=C)
+    check(b, num_ctas=C)
+
+
+@pytest.mark.parametrize("tile", [64, 192, 1024])
+def test_odd_page_segments(tile):
+    """Tiles of 1 or 3 pages give segments with a missing second page mid-request."""
+    b = W.make_batch([100, 2000, 9000, 64 * 7], q_len=2, kv_dtype="e4m3", seed=tile)
+    check(b, num_ctas=9, tile=tile)
+
+
+@pytest.mark.parametrize("splits", [1, 3, 16])
+def test_static_plan(splits):
+    b = W.make_batch([100, 2000, 9000, 4], q_len=4, kv_dtype="e4m3", seed=splits)
+    check(b, splits=splits)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_poisoned_tail_slots_are_ignored(kv):
+    """Pool slots past each request's length hold NaN; they must not reach the output."""
+    lens = [70, 130, 1000, 5]
+    b = W.make_batch(lens, q_len=2, kv_dtype=kv, seed=5)
+    nan_code = 0x7FC0 if kv == "bf16" else 0x7F
+    for r, L in enumerate(lens):
+        last = b.page_indices[b.page_indptr[r + 1] - 1]
+        used = L - (b.page_indptr[r + 1] - b.page_indptr[r] - 1) * b.page_size
+        for pool in (b.k_pool, b.v_pool):
+            raw = pool.view(torch.int16) if kv == "bf16" else pool
+            raw[last, :, used:, :] = nan_code
+    check(b, num_ctas=6)
+
+
+def test_rows_not_a_multiple_of_16():
+    b = W.make_batch([100, 2000], q_len=3, Hq=24, Hkv=4, kv_dtype="e4m3", seed=7)  # 18 rows
+    check(b, num_ctas=4)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_late_dominant_key_moves_the_reference(kv):
+    """A key far above everything before it (late in a long segment) forces the
+    reference max up by more than the slack, so O and L are rescaled in TMEM."""
+    b = W.make_batch([6000, 3000], q_len=2, kv_dtype=kv, seed=77)
+    hot = 5000                                         # key 5000 of request 0
+    page = b.page_indices[b.page_indptr[0] + hot // b.page_size]
+    slot = hot % b.page_size
+    q0 = b.q[0, 0].float()                             # [Hq][d]
+    G = b.Hq // b.Hkv
+    for h in range(b.Hkv):
+        direction = torch.sign(q0[h * G])              # aligned with head h*G's query
+        if kv == "bf16":
+            b.k_pool[page, h, slot] = (direction * 3.0).to(torch.bfloat16)
+        else:
+            b.k_pool[page, h, slot] = W.encode_e4m3(direction * 3.0 / float(b.k_scale[h]))
+    check(b, num_ctas=2)
+
+
+def test_mtp_workload_sample():
+    """The first 3 requests of the MTP E4M3 workload at q_len 4 (32 rows per KV head)."""
+    b = W.make_config(5, max_requests=3, q_len=4)
+    check(b)
