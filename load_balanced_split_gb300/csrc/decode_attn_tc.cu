@@ -8,10 +8,11 @@
 // mma.sync kernel needs one pass per group of 16 rows.  This matters for MTP
 // with several draft tokens, where the warp-level MMAs become the bound.
 //
-// Work per step = two pages (128 keys) of one KV head:
+// Work per step = PPS pages (64 PPS keys) of one KV head, PPS = 4 for the 8-bit
+// path with up to 32 rows (TMEM allowing) and 2 otherwise; per 128-key tile:
 //   S^T[128 keys][rows]  = K[128 keys][128 dims] . Q^T          (tcgen05.mma, TMEM)
 //   P^T = exp2(S^T - m)  by 128 threads, one key each            (registers -> smem)
-//   O^T[128 dims][rows] += V^T[128 dims][128 keys] . P^T         (tcgen05.mma, TMEM)
+//   O^T[128 dims][rows] += V^T[128 dims][64 PPS keys] . P^T      (tcgen05.mma, TMEM)
 // Keys sit on the TMEM lanes for the softmax, so all four compute warps share
 // it; output dims sit on the lanes for O, so each compute thread owns one dim
 // at the segment end and O needs no cross-warp merge.  The row sums l are
@@ -27,9 +28,14 @@
 // moves only when a score exceeds it by more than 4 (base 2), so P <= 256.
 // bf16 pages use kind::f16 with bf16 Q and P.
 //
-// Roles (192 threads): warps 0-3 compute (softmax, epilogue), warp 4 TMA
-// producer, warp 5 one elected thread issuing every MMA.  S is double-buffered
-// in TMEM so Q K^T of step i+1 overlaps the softmax of step i.  Every wait is
+// Roles (352 threads): warps 0-7 compute (softmax, epilogue; warps w and w + 4
+// share TMEM lane quarter w % 4 -- the same keys, and the same output dims --
+// and split the query rows), warp 8 TMA producer, warp 9 one thread issuing
+// Q K^T, warp 10 one thread issuing P V.
+// A tcgen05.mma costs its issuing thread about 100 cycles whatever N is, so the
+// two products are issued from two threads and each step issues few, wide
+// MMAs.  S is double-buffered in TMEM so Q K^T of step i+1 overlaps the
+// softmax of step i.  Every wait is
 // bounded in time; a role that gives up flags the task map's status word and
 // raises the CTA's abort flag, the MMA thread waits for its MMAs in flight and
 // the producer for its copies, and the CTA frees its TMEM and returns.
@@ -42,8 +48,8 @@
 namespace hpa {
 namespace {
 
-constexpr int kTcComputeWarps = 4;
-constexpr int kTcThreads = (kTcComputeWarps + 2) * 32;
+constexpr int kTcComputeWarps = 8;  // two per TMEM lane quarter, splitting the rows
+constexpr int kTcThreads = (kTcComputeWarps + 3) * 32;  // + producer, QK issuer, PV issuer
 constexpr uint32_t kFull = 0xffffffffu;
 
 template <int KV>
@@ -65,19 +71,32 @@ struct TcCfg<HPA_KV_E4M3> {
 template <int KV, int NC>
 struct TcSmem {
   static constexpr int kRp = 16 * NC;
-  static constexpr int kKPair = 2 * TcCfg<KV>::kPageBytes;     // K of 128 keys
-  static constexpr int kStageBytes = 2 * kKPair;               // K then V
-  static constexpr int kOperand = 256 * kRp;                   // a Q slot or a P buffer
-  // as many page-pair stages as fit beside the operands (one CTA per SM): DRAM
-  // latency is hidden by the bytes in flight, up to 6 x 32 KB (E4M3) / 3 x 64 KB
-  static constexpr int kStages0 = (226 * 1024 - 4 * kOperand - 6 * 1024) / kStageBytes;
+  // Columns of S and of O: the hi and lo terms of the 8-bit path sit side by side
+  // (one MMA with N = 2 Rp instead of two with N = Rp: MMA issue, not tensor math,
+  // is what a step of narrow MMAs costs).
+  static constexpr int kNS = KV == HPA_KV_E4M3 ? 2 * kRp : kRp;
+  // Pages per step: every step pays a fixed chain of waits (S ready, the reference-max
+  // vote, P V done), so the 8-bit path takes four pages when S fits twice in TMEM.
+  static constexpr int kPPS = KV == HPA_KV_E4M3 && NC <= 2 ? 4 : 2;
+  static constexpr int kMT = kPPS / 2;                         // 128-key tiles per step
+  static constexpr int kStepKeys = PAGE * kPPS;
+  static constexpr int kKStep = kPPS * TcCfg<KV>::kPageBytes;  // K of one step
+  static constexpr int kStageBytes = 2 * kKStep;               // K then V
+  static constexpr int kOperand = 256 * kRp;                   // a Q slot
+  static constexpr int kPRows = KV == HPA_KV_E4M3 ? 2 * kRp : kRp;  // P^T rows (hi, lo)
+  static constexpr int kPBlk = kPRows * 128;                   // one 128-byte column block
+  static constexpr int kPBuf = kPBlk * (kStepKeys * (KV == HPA_KV_E4M3 ? 1 : 2) / 128);
+  // as many stages as fit beside the operands (one CTA per SM): DRAM latency is
+  // hidden by the bytes in flight
+  static constexpr int kStages0 =
+      (226 * 1024 - 2 * kOperand - 2 * kPBuf - 6 * 1024) / kStageBytes;
   static constexpr int kStages = kStages0 > 6 ? 6 : kStages0;
   static constexpr int kQ = kStages * kStageBytes;             // 2 query slots
   static constexpr int kP = kQ + 2 * kOperand;                 // 2 probability buffers
-  static constexpr int kRowC = kP + 2 * kOperand;              // float[2][64] score scales
+  static constexpr int kRowC = kP + 2 * kPBuf;                 // float[2][64] score scales
   static constexpr int kStepMax = kRowC + 2 * 64 * 4;          // float[2][4][64]
-  static constexpr int kFlags = kStepMax + 2 * 4 * 64 * 4;     // int[2][4]
-  static constexpr int kLRed = kFlags + 32;                    // float[4][64] row-sum parts
+  static constexpr int kFlags = kStepMax + 2 * 4 * 64 * 4;     // int[2][8]
+  static constexpr int kLRed = kFlags + 64;                    // float[4][64] row-sum parts
   static constexpr int kJRow = kLRed + 4 * 64 * 4;             // int[64]: token j of row r
   static constexpr int kInfo = kJRow + 64 * 4;                 // int4[2]
   static constexpr int kBars = kInfo + 32;
@@ -89,8 +108,14 @@ struct TcSmem {
   static constexpr int kAbort = kTmem + 4;
   static constexpr int kBytes = kAbort + 4;
   static constexpr int kAlloc = kBytes + 1024;                 // room to align the base
-  // TMEM columns: S[0], S[1], O (Rp each), rounded up to a power of two >= 32
-  static constexpr int kTmemCols = 3 * kRp <= 32 ? 32 : 3 * kRp <= 64 ? 64 : 3 * kRp <= 128 ? 128 : 256;
+  // TMEM columns: S[0], S[1] (kMT tiles of kNS each), O (kNS), rounded up to a power
+  // of two >= 32
+  static constexpr int kCols = (2 * kMT + 1) * kNS;
+  static constexpr int kTmemCols =
+      kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
+  static constexpr int kOCol = 2 * kMT * kNS;  // first column of O
+  static_assert(kCols <= 512, "TMEM");
+  static_assert(kStages >= 2, "shared memory");
 };
 
 enum TcBar : int {
@@ -147,31 +172,23 @@ __device__ __forceinline__ void tc_fence_after() {
   asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
 }
 
-// 16 consecutive 32-bit TMEM columns of this thread's lane.
-__device__ __forceinline__ void tc_ld16(uint32_t taddr, float (&v)[16]) {
-  uint32_t r[16];
-  asm volatile(
-      "tcgen05.ld.sync.aligned.32x32b.x16.b32 "
-      "{%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
-      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]),
-        "=r"(r[7]), "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]),
-        "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
-      : "r"(taddr));
+// 8 consecutive 32-bit TMEM columns of this thread's lane.
+__device__ __forceinline__ void tc_ld8(uint32_t taddr, float (&v)[8]) {
+  uint32_t r[8];
+  asm volatile("tcgen05.ld.sync.aligned.32x32b.x8.b32 {%0,%1,%2,%3,%4,%5,%6,%7}, [%8];"
+               : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]),
+                 "=r"(r[6]), "=r"(r[7])
+               : "r"(taddr));
 #pragma unroll
-  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+  for (int i = 0; i < 8; ++i) v[i] = __uint_as_float(r[i]);
 }
 
-__device__ __forceinline__ void tc_st16(uint32_t taddr, const float (&v)[16]) {
-  asm volatile(
-      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
-      "{%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
-      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
-      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
-      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
-      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
-      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
-      "r"(__float_as_uint(v[15]))
-      : "memory");
+__device__ __forceinline__ void tc_st8(uint32_t taddr, const float (&v)[8]) {
+  asm volatile("tcgen05.st.sync.aligned.32x32b.x8.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8};" ::"r"(taddr),
+               "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+               "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+               "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7]))
+               : "memory");
 }
 
 __device__ __forceinline__ void tc_wait_ld() {
@@ -179,6 +196,10 @@ __device__ __forceinline__ void tc_wait_ld() {
 }
 __device__ __forceinline__ void tc_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
+  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
 
 __device__ __forceinline__ float warp_max(float x) {
@@ -282,15 +303,16 @@ struct Tc {
       fence_proxy_async_smem();  // the MMA reads the slot through the async proxy
       mbar_arrive(bars + 8 * (B_Q_FULL + slot));
 
-      // KV pages, two per stage
+      // KV pages, kPPS per stage
+      constexpr int PPS = S::kPPS;
       const int pstart = p.page_indptr[r];
       const int pcount = p.page_indptr[r + 1] - pstart;
       const int32_t *pidx = p.page_indices + pstart;
-      for (int pb = pg0; pb < pg1 && ok; pb += 64) {
-        int id[2];
+      for (int pb = pg0; pb < pg1 && ok; pb += 32 * PPS) {
+        int id[PPS];
 #pragma unroll
-        for (int u = 0; u < 2; ++u) {
-          const int pg = pb + 2 * lane + u;
+        for (int u = 0; u < PPS; ++u) {
+          const int pg = pb + PPS * lane + u;
           id[u] = 0;
           if (pg < pg1) {
             id[u] = pg < pcount ? pidx[pg] : -1;
@@ -300,10 +322,12 @@ struct Tc {
             }
           }
         }
-        const int npair = min(32, (pg1 - pb + 1) / 2);
-        for (int i = 0; i < npair; ++i) {
-          const int n = min(2, pg1 - (pb + 2 * i));
-          const int id0 = __shfl_sync(kFull, id[0], i), id1 = __shfl_sync(kFull, id[1], i);
+        const int nstep = min(32, (pg1 - pb + PPS - 1) / PPS);
+        for (int i = 0; i < nstep; ++i) {
+          const int n = min(PPS, pg1 - (pb + PPS * i));
+          int ids[PPS];
+#pragma unroll
+          for (int u = 0; u < PPS; ++u) ids[u] = __shfl_sync(kFull, id[u], i);
           int g2 = 1;
           if (lane == 0) {
             if (*abort_flag ||
@@ -313,17 +337,20 @@ struct Tc {
               const uint32_t fb = bars + 8 * (B_KV_FULL + st);
               const uint32_t dst = base + st * S::kStageBytes;
               mbar_arrive_expect_tx(fb, n * 2 * TcCfg<KV>::kPageBytes);
-              for (int u = 0; u < n; ++u) {
-                const int z = (u ? id1 : id0) * p.Hkv + h;
+#pragma unroll
+              for (int u = 0; u < PPS; ++u) {
+                if (u >= n) break;
+                const int z = ids[u] * p.Hkv + h;
                 if (KV == HPA_KV_BF16) {
-                  // [dim block][128 keys][128 B] for K, then the same for V
+                  // [dim block][64 PPS keys][128 B] for K, then the same for V
+                  constexpr int blk = PPS * 8192;
                   tma_load_3d(dst + u * 8192, tmk, fb, 0, 0, z, pol);
-                  tma_load_3d(dst + 16384 + u * 8192, tmk, fb, 64, 0, z, pol);
-                  tma_load_3d(dst + S::kKPair + u * 8192, tmv, fb, 0, 0, z, pol);
-                  tma_load_3d(dst + S::kKPair + 16384 + u * 8192, tmv, fb, 64, 0, z, pol);
+                  tma_load_3d(dst + blk + u * 8192, tmk, fb, 64, 0, z, pol);
+                  tma_load_3d(dst + S::kKStep + u * 8192, tmv, fb, 0, 0, z, pol);
+                  tma_load_3d(dst + S::kKStep + blk + u * 8192, tmv, fb, 64, 0, z, pol);
                 } else {
                   tma_load_3d(dst + u * 8192, tmk, fb, 0, 0, z, pol);
-                  tma_load_3d(dst + S::kKPair + u * 8192, tmv, fb, 0, 0, z, pol);
+                  tma_load_3d(dst + S::kKStep + u * 8192, tmv, fb, 0, 0, z, pol);
                 }
               }
               issued |= 1u << st;
@@ -348,59 +375,32 @@ struct Tc {
     }
   }
 
-  // ---- warp 5, one thread: every MMA
-  struct PvStep {
-    int i, st, first, k;
-  };
-
-  static __device__ bool issue_pv(const PvStep &v, uint8_t *smem, uint32_t tmem) {
-    const uint32_t base = smem_u32(smem), bars = base + S::kBars;
+  // ---- warps 5 and 6, one thread each: the MMAs.  Both walk the same segments
+  // and page pairs as the producer; st / i / phase follow the same sequence.
+  static __device__ void mma_done(const AttnParams &p, uint8_t *smem, bool ok) {
+    const uint32_t bars = smem_u32(smem) + S::kBars;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kAbort);
-    const int b = v.i & 1;
-    if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_P_FULL + b), (v.i >> 1) & 1)) return false;
-    if (v.first && v.k > 0 &&
-        (*abort_flag || !mbar_wait_bounded(bars + 8 * B_O_FREE, (v.k - 1) & 1)))
-      return false;
-    tc_fence_after();
-    const uint32_t vbase = base + v.st * S::kStageBytes + S::kKPair;
-    const uint32_t pbase = base + S::kP + b * S::kOperand;
-    const uint32_t o_t = tmem + 2 * kRp;
-    if (KV == HPA_KV_BF16) {
-      const uint32_t idv = tc_idesc(1, kRp, 1, 0);
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk)  // 16 keys per MMA
-        tc_mma<KV>(o_t, tc_desc(vbase + kk * 2048, 16384, 1024),
-                   tc_desc(pbase + (kk >> 2) * (kRp * 128) + (kk & 3) * 32, 16, 1024), idv,
-                   !v.first || kk > 0);
-    } else {
-      const uint32_t idv = tc_idesc(0, kRp, 1, 0);
-#pragma unroll
-      for (int part = 0; part < 2; ++part)  // P = hi + lo
-#pragma unroll
-        for (int kk = 0; kk < 4; ++kk)  // 32 keys per MMA
-          tc_mma<KV>(o_t, tc_desc(vbase + kk * 4096, 8192, 1024),
-                     tc_desc(pbase + part * (kRp * 128) + kk * 32, 16, 1024), idv,
-                     !v.first || part > 0 || kk > 0);
+    if (!ok) {
+      status_or(p.tm, HPA_STATUS_TIMEOUT);
+      *abort_flag = 1;
     }
-    tc_commit(bars + 8 * (S::kKvEmpty + v.st));  // the page pair may be refilled
-    tc_commit(bars + 8 * (B_PV_DONE + b));      // P[b] is free; O is current
-    return true;
+    // every MMA this thread issued completes before the CTA frees its TMEM
+    tc_commit(bars + 8 * B_DRAIN);
   }
 
-  static __device__ void mma_issuer(const AttnParams &p, uint8_t *smem, int s_begin, int s_end,
-                                    int tile, uint32_t tmem) {
+  static __device__ void qk_issuer(const AttnParams &p, uint8_t *smem, int s_begin, int s_end,
+                                   int tile, uint32_t tmem) {
     const uint32_t base = smem_u32(smem), bars = base + S::kBars;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kAbort);
     int i = 0, st = 0;
     uint32_t phase = 0;
-    bool ok = true, have = false;
-    PvStep prev{0, 0, 0, 0};
+    bool ok = true;
     for (int s = s_begin; s < s_end && ok; ++s) {
       const int k = s - s_begin, slot = k & 1;
       const int4 sg = reinterpret_cast<const int4 *>(p.tm + p.lay.segs)[s];
       const int L = p.tm[p.lay.lens + sg.x];
       const int pg0 = sg.y * tile / PAGE, pg1 = (min(sg.z * tile, L) + PAGE - 1) / PAGE;
-      const int npairs = (pg1 - pg0 + 1) / 2;
+      const int npairs = (pg1 - pg0 + S::kPPS - 1) / S::kPPS;  // steps
       if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_Q_FULL + slot), (k >> 1) & 1)) {
         ok = false;
         break;
@@ -415,32 +415,29 @@ struct Tc {
         }
         tc_fence_after();
         const uint32_t kbase = base + st * S::kStageBytes;
-        const uint32_t s_t = tmem + b * kRp;
-        if (KV == HPA_KV_BF16) {
-          const uint32_t id = tc_idesc(1, kRp, 0, 0);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk)  // 16 dims per MMA
-            tc_mma<KV>(s_t, tc_desc(kbase + (kk >> 2) * 16384 + (kk & 3) * 32, 16, 1024),
-                       tc_desc(qbase + (kk >> 2) * (kRp * 128) + (kk & 3) * 32, 16, 1024), id,
-                       kk > 0);
-        } else {
-          const uint32_t id = tc_idesc(0, kRp, 0, 0);
+        for (int mt = 0; mt < S::kMT; ++mt) {  // keys [128 mt, 128 mt + 128) of the step
+          const uint32_t s_t = tmem + (b * S::kMT + mt) * S::kNS;
+          if (KV == HPA_KV_BF16) {
+            const uint32_t id = tc_idesc(1, kRp, 0, 0);
 #pragma unroll
-          for (int part = 0; part < 2; ++part)  // Q = hi + lo
+            for (int kk = 0; kk < 8; ++kk)  // 16 dims per MMA
+              tc_mma<KV>(s_t,
+                         tc_desc(kbase + (kk >> 2) * (S::kPPS * 8192) + mt * 16384 + (kk & 3) * 32,
+                                 16, 1024),
+                         tc_desc(qbase + (kk >> 2) * (kRp * 128) + (kk & 3) * 32, 16, 1024), id,
+                         kk > 0);
+          } else {
+            // B = [Q hi rows; Q lo rows] (2 Rp rows): S hi in columns [0, Rp), lo in [Rp, 2 Rp)
+            const uint32_t id = tc_idesc(0, 2 * kRp, 0, 0);
 #pragma unroll
             for (int kk = 0; kk < 4; ++kk)  // 32 dims per MMA
-              tc_mma<KV>(s_t, tc_desc(kbase + kk * 32, 16, 1024),
-                         tc_desc(qbase + part * (kRp * 128) + kk * 32, 16, 1024), id,
-                         part > 0 || kk > 0);
+              tc_mma<KV>(s_t, tc_desc(kbase + mt * 16384 + kk * 32, 16, 1024),
+                         tc_desc(qbase + kk * 32, 16, 1024), id, kk > 0);
+          }
         }
         tc_commit(bars + 8 * (B_S_FULL + b));
         if (j == npairs - 1) tc_commit(bars + 8 * (B_Q_EMPTY + slot));
-        if (have && !issue_pv(prev, smem, tmem)) {
-          ok = false;
-          break;
-        }
-        prev = PvStep{i, st, j == 0, k};
-        have = true;
         ++i;
         if (++st == S::kStages) {
           st = 0;
@@ -448,28 +445,79 @@ struct Tc {
         }
       }
     }
-    if (ok && have) ok = issue_pv(prev, smem, tmem);
-    if (!ok) {
-      status_or(p.tm, HPA_STATUS_TIMEOUT);
-      *abort_flag = 1;
-    }
-    // every MMA complete before the CTA frees its TMEM
-    tc_commit(bars + 8 * B_DRAIN);
-    mbar_wait_bounded(bars + 8 * B_DRAIN, 0, 1000000000ull);
+    mma_done(p, smem, ok);
   }
 
-  // ---- warps 0-3: softmax and the segment epilogue
-  static __device__ void compute(const AttnParams &p, uint8_t *smem, int s_begin, int s_end,
-                                 uint32_t tmem, int h) {
-    const int t = threadIdx.x, w = t >> 5, lane = t & 31;
+  static __device__ void pv_issuer(const AttnParams &p, uint8_t *smem, int s_begin, int s_end,
+                                   int tile, uint32_t tmem) {
     const uint32_t base = smem_u32(smem), bars = base + S::kBars;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kAbort);
-    const uint32_t lane_t = tmem + (static_cast<uint32_t>(32 * w) << 16);
+    const uint32_t o_t = tmem + 2 * S::kMT * S::kNS;
+    int i = 0, st = 0;
+    bool ok = true;
+    for (int s = s_begin; s < s_end && ok; ++s) {
+      const int k = s - s_begin;
+      const int4 sg = reinterpret_cast<const int4 *>(p.tm + p.lay.segs)[s];
+      const int L = p.tm[p.lay.lens + sg.x];
+      const int pg0 = sg.y * tile / PAGE, pg1 = (min(sg.z * tile, L) + PAGE - 1) / PAGE;
+      const int npairs = (pg1 - pg0 + S::kPPS - 1) / S::kPPS;  // steps
+      for (int j = 0; j < npairs; ++j) {
+        const int b = i & 1;
+        // P of this step written; at a segment start, the previous segment's O read out
+        if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_P_FULL + b), (i >> 1) & 1) ||
+            (j == 0 && k > 0 && !mbar_wait_bounded(bars + 8 * B_O_FREE, (k - 1) & 1))) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        const uint32_t vbase = base + st * S::kStageBytes + S::kKStep;
+        const uint32_t pbase = base + S::kP + b * S::kPBuf;
+        if (KV == HPA_KV_BF16) {
+          const uint32_t idv = tc_idesc(1, kRp, 1, 0);
+#pragma unroll
+          for (int kk = 0; kk < 4 * S::kPPS; ++kk)  // 16 keys per MMA
+            tc_mma<KV>(o_t, tc_desc(vbase + kk * 2048, S::kPPS * 8192, 1024),
+                       tc_desc(pbase + (kk >> 2) * S::kPBlk + (kk & 3) * 32, 16, 1024), idv,
+                       j > 0 || kk > 0);
+        } else {
+          // B = [P hi rows; P lo rows]: O hi in columns [0, Rp), lo in [Rp, 2 Rp)
+          const uint32_t idv = tc_idesc(0, 2 * kRp, 1, 0);
+#pragma unroll
+          for (int kk = 0; kk < 2 * S::kPPS; ++kk)  // 32 keys per MMA
+            tc_mma<KV>(o_t, tc_desc(vbase + kk * 4096, 8192, 1024),
+                       tc_desc(pbase + (kk >> 2) * S::kPBlk + (kk & 3) * 32, 16, 1024), idv,
+                       j > 0 || kk > 0);
+        }
+        // Q K^T of this step completed before its P was written, so this commit
+        // frees the whole K/V stage
+        tc_commit(bars + 8 * (S::kKvEmpty + st));
+        tc_commit(bars + 8 * (B_PV_DONE + b));  // P[b] is free; O is current
+        ++i;
+        if (++st == S::kStages) st = 0;
+      }
+    }
+    mma_done(p, smem, ok);
+  }
+
+  // ---- warps 0-7: softmax and the segment epilogue.  Thread t: key slots
+  // kt + 128 m of the step (m < kMT) and output dim kt = t % 128 (its TMEM lane),
+  // rows [hf RH, hf RH + RH) with hf = t / 128.
+  static __device__ void compute(const AttnParams &p, uint8_t *smem, int s_begin, int s_end,
+                                 uint32_t tmem, int h) {
+    constexpr int RH = kRp / 2;  // rows per warp
+    constexpr int MT = S::kMT;
+    const int t = threadIdx.x, w = t >> 5, lane = t & 31, qd = w & 3, hf = w >> 2;
+    const int kt = t & 127, r0 = hf * RH;
+    const uint32_t base = smem_u32(smem), bars = base + S::kBars;
+    volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kAbort);
+    const uint32_t lane_t = tmem + (static_cast<uint32_t>(32 * qd) << 16);
     const int G = p.G, R = p.rows, q_len = p.q_len;
     const float vsc = KV == HPA_KV_E4M3 ? p.v_scale[h] : 1.f;
     constexpr float kSlack = TcCfg<KV>::kSlack, kPOff = TcCfg<KV>::kPOff;
-    float *stepmax = reinterpret_cast<float *>(smem + S::kStepMax);
-    int *flags = reinterpret_cast<int *>(smem + S::kFlags);
+    float *stepmax = reinterpret_cast<float *>(smem + S::kStepMax);  // [2][4 quarters][64]
+    int *flags = reinterpret_cast<int *>(smem + S::kFlags);           // [2][8 warps]
+    float *lred = reinterpret_cast<float *>(smem + S::kLRed);         // [4 quarters][64]
+    const int *jrow = reinterpret_cast<const int *>(smem + S::kJRow);
     int i = 0, n_moved = 0, n_seg = 0;
     bool ok = true;
     for (int s = s_begin; s < s_end && ok; ++s) {
@@ -481,15 +529,15 @@ struct Tc {
       const int4 inf = reinterpret_cast<const int4 *>(smem + S::kInfo)[slot];
       const int L = inf.y, klo = inf.z, khi = inf.w;
       const int pg0 = klo / PAGE, pg1 = (khi + PAGE - 1) / PAGE;
-      const int npairs = (pg1 - pg0 + 1) / 2;
+      const int npairs = (pg1 - pg0 + S::kPPS - 1) / S::kPPS;  // steps
       if (L < q_len && t == 0) status_or(p.tm, HPA_STATUS_BAD_SEQLEN);
-      const float *rowc = reinterpret_cast<const float *>(smem + S::kRowC) + slot * 64;
-      const int *jrow = reinterpret_cast<const int *>(smem + S::kJRow);
-      float mref[kRp], lsum[kRp];  // reference max per row; this key slot's share of l
+      const uint32_t rowc_s = base + S::kRowC + (slot * 64 + r0) * 4;
+      const float c_all = p.scale_log2;  // bf16: one score scale for every row
+      float mref[RH], lsum[RH];  // reference max per row; this key slot's share of l
 #pragma unroll
-      for (int r = 0; r < kRp; ++r) {
-        mref[r] = -CUDART_INF_F;
-        lsum[r] = 0.f;
+      for (int e = 0; e < RH; ++e) {
+        mref[e] = -CUDART_INF_F;
+        lsum[e] = 0.f;
       }
 
       for (int jp = 0; jp < npairs; ++jp) {
@@ -499,37 +547,71 @@ struct Tc {
           break;
         }
         tc_fence_after();
-        float x[kRp];
+        float x[MT][RH];
 #pragma unroll
-        for (int c = 0; c < NC; ++c) {
-          float v[16];
-          tc_ld16(lane_t + b * kRp + 16 * c, v);
+        for (int m = 0; m < MT; ++m)
 #pragma unroll
-          for (int e = 0; e < 16; ++e) x[16 * c + e] = v[e];
-        }
+          for (int c = 0; c < RH / 8; ++c) {
+            const uint32_t col = lane_t + (b * MT + m) * S::kNS + r0 + 8 * c;
+            float v[8];
+            tc_ld8(col, v);
+            if (KV == HPA_KV_E4M3) {  // S = S(Q hi) + S(Q lo)
+              float u[8];
+              tc_ld8(col + kRp, u);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v[e] += u[e];
+            }
+#pragma unroll
+            for (int e = 0; e < 8; ++e) x[m][8 * c + e] = v[e];
+          }
         tc_wait_ld();
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars + 8 * (B_S_FREE + b));
 
-        const int pg = pg0 + 2 * jp, key = pg * PAGE + t;
-        const bool present = key < pg1 * PAGE;  // the pair's second page may be missing
-        // row r (token j = r / G) sees keys < L - q_len + 1 + j
-        const int d0 = present ? key - (L - q_len + 1) : INT_MAX;
+        const int key0 = (pg0 + S::kPPS * jp) * PAGE + kt;  // key of slot m: key0 + 128 m
+        int d0[MT];
+        bool present[MT];
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          present[m] = key0 + 128 * m < pg1 * PAGE;  // the step's last pages may be missing
+          // row r (token j = r / G) sees keys < L - q_len + 1 + j
+          d0[m] = present[m] ? key0 + 128 * m - (L - q_len + 1) : INT_MAX;
+        }
+#pragma unroll
+        for (int e4 = 0; e4 < RH; e4 += 4) {
+          float c4[4] = {c_all, c_all, c_all, c_all};
+          if (KV == HPA_KV_E4M3) {  // per-row scale (the query rows' own power of two)
+            uint32_t w0, w1, w2, w3;
+            lds128(rowc_s + 4 * e4, w0, w1, w2, w3);
+            c4[0] = __uint_as_float(w0), c4[1] = __uint_as_float(w1);
+            c4[2] = __uint_as_float(w2), c4[3] = __uint_as_float(w3);
+          }
+#pragma unroll
+          for (int m = 0; m < MT; ++m)
+#pragma unroll
+            for (int e = 0; e < 4; ++e)
+              x[m][e4 + e] = r0 + e4 + e < R ? x[m][e4 + e] * c4[e] : -CUDART_INF_F;
+        }
+#pragma unroll
+        for (int m = 0; m < MT; ++m)
+          if (__any_sync(kFull, d0[m] >= 0)) {  // near the request's end, or a missing page
+#pragma unroll
+            for (int e = 0; e < RH; ++e)
+              if (d0[m] >= jrow[r0 + e]) x[m][e] = -CUDART_INF_F;
+          }
         bool flag = false;
 #pragma unroll
-        for (int r = 0; r < kRp; ++r) {
-          const bool live = r < R && d0 < jrow[r];
-          x[r] = live ? x[r] * rowc[r] : -CUDART_INF_F;
-          flag |= x[r] > mref[r] + kSlack;
-        }
+        for (int m = 0; m < MT; ++m)
+#pragma unroll
+          for (int e = 0; e < RH; ++e) flag |= x[m][e] > mref[e] + kSlack;
         // A reference max moves only when some score exceeds it by more than the slack.
-        // The four warps agree through mbarriers (bounded waits), never named barriers:
-        // a warp that gives up must not leave the others waiting without a limit.
+        // The warps agree through mbarriers (bounded waits), never named barriers: a
+        // warp that gives up must not leave the others waiting without a limit.
         {
           const bool any = __any_sync(kFull, flag);
           if (lane == 0) {
-            flags[b * 4 + w] = any;
+            flags[b * 8 + w] = any;
             mbar_arrive(bars + 8 * (B_FLAG + b));
           }
         }
@@ -537,13 +619,18 @@ struct Tc {
           ok = false;
           break;
         }
-        const bool moved = flags[b * 4] | flags[b * 4 + 1] | flags[b * 4 + 2] | flags[b * 4 + 3];
+        int moved = 0;
+#pragma unroll
+        for (int x8 = 0; x8 < 8; ++x8) moved |= flags[b * 8 + x8];
         if (moved) {
           float *sm = stepmax + (n_moved & 1) * 4 * 64;
 #pragma unroll
-          for (int r = 0; r < kRp; ++r) {
-            const float mx = warp_max(x[r]);
-            if (lane == 0) sm[w * 64 + r] = mx;
+          for (int e = 0; e < RH; ++e) {
+            float v = x[0][e];
+#pragma unroll
+            for (int m = 1; m < MT; ++m) v = fmaxf(v, x[m][e]);
+            const float mx = warp_max(v);
+            if (lane == 0) sm[qd * 64 + r0 + e] = mx;
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(bars + 8 * B_SMAX);
@@ -552,20 +639,21 @@ struct Tc {
             break;
           }
           ++n_moved;
-          float alpha[kRp];
+          float alpha[RH];
           bool rescale = false;
 #pragma unroll
-          for (int r = 0; r < kRp; ++r) {
+          for (int e = 0; e < RH; ++e) {
+            const int r = r0 + e;
             const float mn = fmaxf(fmaxf(fmaxf(sm[r], sm[64 + r]), fmaxf(sm[128 + r], sm[192 + r])),
-                                   mref[r]);
-            alpha[r] = mn == mref[r] ? 1.f : exp2f(mref[r] - mn);  // 0 from -inf
-            rescale |= alpha[r] != 1.f;
-            mref[r] = mn;
-            lsum[r] *= alpha[r];
+                                   mref[e]);
+            alpha[e] = mn == mref[e] ? 1.f : exp2f(mref[e] - mn);  // 0 from -inf
+            rescale |= alpha[e] != 1.f;
+            mref[e] = mn;
+            lsum[e] *= alpha[e];
           }
-          if (jp > 0 && rescale) {
+          if (jp > 0 && __any_sync(kFull, rescale)) {
             // O holds the earlier pairs of this segment: wait for the last P V, then
-            // rescale it in TMEM (this thread's lane = output dim t)
+            // rescale this warp's rows of it in TMEM (lane = output dim kt)
             const int pi = i - 1;
             if (*abort_flag ||
                 !mbar_wait_bounded(bars + 8 * (B_PV_DONE + (pi & 1)), (pi >> 1) & 1)) {
@@ -574,14 +662,17 @@ struct Tc {
             }
             tc_fence_after();
 #pragma unroll
-            for (int c = 0; c < NC; ++c) {
-              float o[16];
-              tc_ld16(lane_t + 2 * kRp + 16 * c, o);
-              tc_wait_ld();
+            for (int part = 0; part < S::kNS / kRp; ++part)  // O (and its lo half)
 #pragma unroll
-              for (int e = 0; e < 16; ++e) o[e] *= alpha[16 * c + e];
-              tc_st16(lane_t + 2 * kRp + 16 * c, o);
-            }
+              for (int c = 0; c < RH / 8; ++c) {
+                const uint32_t col = lane_t + S::kOCol + part * kRp + r0 + 8 * c;
+                float o[8];
+                tc_ld8(col, o);
+                tc_wait_ld();
+#pragma unroll
+                for (int e = 0; e < 8; ++e) o[e] *= alpha[8 * c + e];
+                tc_st8(col, o);
+              }
             tc_wait_st();
             tc_fence_before();
           }
@@ -592,47 +683,68 @@ struct Tc {
           ok = false;
           break;
         }
-        uint8_t *pb = smem + S::kP + b * S::kOperand;
-        if (KV == HPA_KV_BF16) {
+        // P^T rows go to shared memory as 32-bit words: lanes exchange values so that
+        // each thread holds consecutive keys of one row (quad byte transpose for
+        // E4M3, a pair swap for bf16)
+        const uint32_t pb = base + S::kP + b * S::kPBuf;
 #pragma unroll
-          for (int r = 0; r < kRp; r += 2) {
-            const float b0 = mref[r] == -CUDART_INF_F ? 0.f : mref[r];
-            const float b1 = mref[r + 1] == -CUDART_INF_F ? 0.f : mref[r + 1];
-            const float p0 = exp2f(x[r] - b0), p1 = exp2f(x[r + 1] - b1);
-            lsum[r] += p0;
-            lsum[r + 1] += p1;
-            const uint32_t pk = pack_bf16(p0, p1);
-            *reinterpret_cast<uint16_t *>(pb + kmaj(r, 2 * t, kRp * 128)) =
-                static_cast<uint16_t>(pk & 0xffffu);
-            *reinterpret_cast<uint16_t *>(pb + kmaj(r + 1, 2 * t, kRp * 128)) =
-                static_cast<uint16_t>(pk >> 16);
+        for (int m = 0; m < MT; ++m) {
+          const int kk = kt + 128 * m;  // key within the step
+          if (KV == HPA_KV_BF16) {
+#pragma unroll
+            for (int e = 0; e < RH; e += 2) {
+              const float b0 = mref[e] == -CUDART_INF_F ? 0.f : mref[e];
+              const float b1 = mref[e + 1] == -CUDART_INF_F ? 0.f : mref[e + 1];
+              const float p0 = exp2f(x[m][e] - b0), p1 = exp2f(x[m][e + 1] - b1);
+              lsum[e] += p0;
+              lsum[e + 1] += p1;
+              const uint32_t a = pack_bf16(p0, p1);  // (row r, row r + 1) of key kk
+              const uint32_t o = __shfl_xor_sync(kFull, a, 1);
+              // even lane: row r, keys kk, kk + 1; odd lane: row r + 1, keys kk - 1, kk
+              const uint32_t wv = __byte_perm(a, o, (lane & 1) ? 0x3276u : 0x5410u);
+              sts32(pb + kmaj(r0 + e + (lane & 1), 2 * (kk & ~1), S::kPBlk), wv);
+            }
+          } else {
+            const uint32_t sel1 = (lane & 1) ? 0x3715u : 0x6240u;
+            const uint32_t sel2 = (lane & 2) ? 0x3276u : 0x5410u;
+            auto quad_transpose = [&](uint32_t a) {  // byte e of lane q -> byte q of lane e
+              const uint32_t y = __byte_perm(a, __shfl_xor_sync(kFull, a, 1), sel1);
+              return __byte_perm(y, __shfl_xor_sync(kFull, y, 2), sel2);
+            };
+#pragma unroll
+            for (int e4 = 0; e4 < RH; e4 += 4) {
+              uint32_t hi = 0, lo = 0;
+#pragma unroll
+              for (int e = 0; e < 4; e += 2) {
+                const int a0 = e4 + e;
+                const float b0 = mref[a0] == -CUDART_INF_F ? 0.f : mref[a0];
+                const float b1 = mref[a0 + 1] == -CUDART_INF_F ? 0.f : mref[a0 + 1];
+                const float p0 = exp2f(x[m][a0] - b0 + kPOff);
+                const float p1 = exp2f(x[m][a0 + 1] - b1 + kPOff);
+                lsum[a0] += p0;
+                lsum[a0 + 1] += p1;
+                const uint16_t h2 = f32x2_to_e4m3x2(p0, p1);
+                const uint32_t hh = e4m3x2_to_f16x2(h2);
+                const float2 hv = __half22float2(*reinterpret_cast<const __half2 *>(&hh));
+                const uint16_t l2 = f32x2_to_e4m3x2(p0 - hv.x, p1 - hv.y);
+                hi |= static_cast<uint32_t>(h2) << (8 * e);
+                lo |= static_cast<uint32_t>(l2) << (8 * e);
+              }
+              // lane q of each quad now writes row r0 + e4 + q for the quad's 4 keys
+              const int rr = r0 + e4 + (lane & 3);
+              sts32(pb + kmaj(rr, kk & ~3, S::kPBlk), quad_transpose(hi));
+              sts32(pb + kmaj(kRp + rr, kk & ~3, S::kPBlk), quad_transpose(lo));
+            }
           }
-        } else {
+          // V rows of keys past the request (or of a missing page) must be finite: zero them
+          if (hf == 0 && (!present[m] || key0 + 128 * m >= L)) {
+            uint8_t *vr = smem + st * S::kStageBytes + S::kKStep + (kk >> 3) * 1024 + (kk & 7) * 128;
+            const int4 z = make_int4(0, 0, 0, 0);
 #pragma unroll
-          for (int r = 0; r < kRp; r += 2) {
-            const float b0 = mref[r] == -CUDART_INF_F ? 0.f : mref[r];
-            const float b1 = mref[r + 1] == -CUDART_INF_F ? 0.f : mref[r + 1];
-            const float p0 = exp2f(x[r] - b0 + kPOff), p1 = exp2f(x[r + 1] - b1 + kPOff);
-            lsum[r] += p0;
-            lsum[r + 1] += p1;
-            const uint16_t h2 = f32x2_to_e4m3x2(p0, p1);
-            const uint32_t hh = e4m3x2_to_f16x2(h2);
-            const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hh));
-            const uint16_t l2 = f32x2_to_e4m3x2(p0 - hf.x, p1 - hf.y);
-            pb[kmaj(r, t, 0)] = static_cast<uint8_t>(h2 & 0xff);
-            pb[kmaj(r + 1, t, 0)] = static_cast<uint8_t>(h2 >> 8);
-            pb[kRp * 128 + kmaj(r, t, 0)] = static_cast<uint8_t>(l2 & 0xff);
-            pb[kRp * 128 + kmaj(r + 1, t, 0)] = static_cast<uint8_t>(l2 >> 8);
-          }
-        }
-        // V rows of keys past the request (or of a missing page) must be finite: zero them
-        if (!present || key >= L) {
-          uint8_t *vr = smem + st * S::kStageBytes + S::kKPair + (t >> 3) * 1024 + (t & 7) * 128;
-          const int4 z = make_int4(0, 0, 0, 0);
-#pragma unroll
-          for (int c = 0; c < 8; ++c) {
-            reinterpret_cast<int4 *>(vr)[c] = z;
-            if (KV == HPA_KV_BF16) reinterpret_cast<int4 *>(vr + 16384)[c] = z;
+            for (int c = 0; c < 8; ++c) {
+              reinterpret_cast<int4 *>(vr)[c] = z;
+              if (KV == HPA_KV_BF16) reinterpret_cast<int4 *>(vr + S::kPPS * 8192)[c] = z;
+            }
           }
         }
         fence_proxy_async_smem();  // generic writes before the MMA reads them
@@ -641,14 +753,13 @@ struct Tc {
 
         if (jp == npairs - 1) {
           // ---- segment end: l per row (sum over the 128 key slots), then O / l for
-          // every row, this thread's dim t
-          float *lred = reinterpret_cast<float *>(smem + S::kLRed);
+          // this warp's rows, this thread's dim kt
 #pragma unroll
-          for (int r = 0; r < kRp; ++r) {
-            float v = lsum[r];
+          for (int e = 0; e < RH; ++e) {
+            float v = lsum[e];
 #pragma unroll
             for (int o = 16; o > 0; o >>= 1) v += __shfl_xor_sync(kFull, v, o);
-            if (lane == 0) lred[w * 64 + r] = v;
+            if (lane == 0) lred[qd * 64 + r0 + e] = v;
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(bars + 8 * B_LRED);
@@ -660,25 +771,30 @@ struct Tc {
           ++n_seg;
           tc_fence_after();
 #pragma unroll
-          for (int c = 0; c < NC; ++c) {
-            float o[16];
-            tc_ld16(lane_t + 2 * kRp + 16 * c, o);
+          for (int c = 0; c < RH / 8; ++c) {
+            float o[8];
+            tc_ld8(lane_t + S::kOCol + r0 + 8 * c, o);
+            if (KV == HPA_KV_E4M3) {  // O = O(P hi) + O(P lo)
+              float u[8];
+              tc_ld8(lane_t + S::kOCol + kRp + r0 + 8 * c, u);
+              tc_wait_ld();
+#pragma unroll
+              for (int e = 0; e < 8; ++e) o[e] += u[e];
+            }
             tc_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 16; ++e) {
-              const int r = 16 * c + e;
+            for (int e = 0; e < 8; ++e) {
+              const int r = r0 + 8 * c + e;
               const float l = lred[r] + lred[64 + r] + lred[128 + r] + lred[192 + r];
               if (r < R) {
                 const int j = jrow[r], g = r - j * G;
                 const int64_t row = (static_cast<int64_t>(s) * q_len + j) * p.Hq + h * G + g;
-                p.partial_o[row * HEAD_DIM + t] = l > 0.f ? o[e] / l * vsc : 0.f;
-              }
-              if (r == t && t < R) {  // thread r writes row r's lse
-                const int j = jrow[r], g = r - j * G;
-                const int64_t row = (static_cast<int64_t>(s) * q_len + j) * p.Hq + h * G + g;
-                p.partial_lse[row] = l > 0.f
-                                         ? (mref[r] - kPOff + log2f(l)) * 0.69314718055994531f
-                                         : -CUDART_INF_F;
+                p.partial_o[row * HEAD_DIM + kt] = l > 0.f ? o[e] / l * vsc : 0.f;
+                if (kt == 8 * c + e) {  // one thread per row writes its lse
+                  p.partial_lse[row] =
+                      l > 0.f ? (mref[8 * c + e] - kPOff + log2f(l)) * 0.69314718055994531f
+                              : -CUDART_INF_F;
+                }
               }
             }
           }
@@ -726,7 +842,7 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     // q_full q_empty s_full s_free p_full pv_done o_free drain flag smax lred
     const int counts[18] = {32, 32, 1 + kTcComputeWarps, 1 + kTcComputeWarps, 1, 1,
                             kTcComputeWarps, kTcComputeWarps, kTcComputeWarps, kTcComputeWarps,
-                            1, 1, kTcComputeWarps, 1, kTcComputeWarps, kTcComputeWarps,
+                            1, 1, kTcComputeWarps, 2, kTcComputeWarps, kTcComputeWarps,
                             kTcComputeWarps, kTcComputeWarps};
     for (int i = 0; i < 18; ++i) mbar_init(bars + 8 * i, counts[i]);
     for (int i = 0; i < S::kStages; ++i) {
@@ -757,10 +873,14 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     Tc<KV, NC>::compute(p, smem, s_begin, s_end, tmem, h);
   else if (warp == kTcComputeWarps)
     Tc<KV, NC>::producer(p, &tmk, &tmv, smem, s_begin, s_end, tile, h);
-  else if ((threadIdx.x & 31) == 0)
-    Tc<KV, NC>::mma_issuer(p, smem, s_begin, s_end, tile, tmem);
+  else if (warp == kTcComputeWarps + 1 && (threadIdx.x & 31) == 0)
+    Tc<KV, NC>::qk_issuer(p, smem, s_begin, s_end, tile, tmem);
+  else if (warp == kTcComputeWarps + 2 && (threadIdx.x & 31) == 0)
+    Tc<KV, NC>::pv_issuer(p, smem, s_begin, s_end, tile, tmem);
   tc_fence_before();
   __syncthreads();
+  // both issuers have committed to the drain barrier: wait (bounded) for their MMAs
+  mbar_wait_bounded(bars + 8 * B_DRAIN, 0, 1000000000ull);
   if (threadIdx.x < 32) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
