@@ -11,9 +11,11 @@ import numpy as np
 import pytest
 import torch
 
+import load_balanced_split_gb300 as hpa
 import oracle
 import workloads as W
-from gpu_helpers import assert_close, assert_lse_close, expect_taskmap_equal, run_gpu
+from gpu_helpers import (DeviceBatch, assert_close, assert_lse_close, expect_taskmap_equal,
+                         run_gpu)
 
 pytestmark = pytest.mark.gpu
 
@@ -107,3 +109,62 @@ def test_mtp_workload_sample():
     """The first 3 requests of the MTP E4M3 workload at q_len 4 (32 rows per KV head)."""
     b = W.make_config(5, max_requests=3, q_len=4)
     check(b)
+
+
+def test_bad_page_id_is_flagged():
+    b = W.make_batch([200, 300], q_len=2, kv_dtype="e4m3", seed=6)
+    b.page_indices = b.page_indices.copy()
+    b.page_indices[2] = b.num_pages + 5
+    db = DeviceBatch(b)
+    ws = hpa.Workspace(b.B, 2, 64, 128, num_ctas=4)
+    out = torch.empty((2, 2, 64, 128), dtype=torch.bfloat16, device="cuda")
+    hpa.decode_step(ws, db.q, db.k, db.v, db.lens, db.indptr, db.indices, out, None, db.ks,
+                    db.vs, tc=True)
+    torch.cuda.synchronize()
+    assert ws.status() & 4
+    assert torch.isnan(out.float()).all()
+
+
+def test_mismatched_partition_count_is_flagged():
+    b = W.make_batch([200, 3000], q_len=4, seed=7)
+    db = DeviceBatch(b)
+    ws = hpa.Workspace(b.B, 4, 64, 128, num_ctas=4)
+    ws.plan(db.lens)
+    big = hpa.Workspace(b.B, 4, 64, 128, num_ctas=9)
+    out = torch.empty((2, 4, 64, 128), dtype=torch.bfloat16, device="cuda")
+    hpa.hpa_decode_attn_tc(db.q, db.k, db.v, db.indptr, db.indices, ws.taskmap, 9,
+                           big.partial_o, big.partial_lse)
+    hpa.hpa_combine(big.partial_o, big.partial_lse, ws.taskmap, 9, out)
+    torch.cuda.synchronize()
+    assert ws.status() & 2
+    assert torch.isnan(out.float()).all()
+
+
+def test_three_calls_capture_in_a_cuda_graph():
+    """plan -> tcgen05 attention -> combine recorded once in a CUDA graph and replayed on
+    new lengths."""
+    lens0 = np.array([3000, 40, 12000, 700], dtype=np.int32)
+    b = W.make_batch(lens0, q_len=4, kv_dtype="e4m3", seed=90)
+    db = DeviceBatch(b)
+    ws = hpa.Workspace(b.B, 4, 64, 128, num_ctas=11)
+    out = torch.empty((b.B, 4, 64, 128), dtype=torch.bfloat16, device="cuda")
+    lse = torch.empty((b.B, 4, 64), dtype=torch.float32, device="cuda")
+    lens = db.lens.clone()
+    s = torch.cuda.Stream()
+    with torch.cuda.stream(s):                       # warm up (resolves TMA descriptors etc.)
+        hpa.decode_step(ws, db.q, db.k, db.v, lens, db.indptr, db.indices, out, lse, db.ks,
+                        db.vs, stream=s, tc=True)
+    torch.cuda.synchronize()
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g, stream=s):
+        hpa.decode_step(ws, db.q, db.k, db.v, lens, db.indptr, db.indices, out, lse, db.ks,
+                        db.vs, stream=s, tc=True)
+    for shorten in (0, 17):                          # replay; the second time with new lengths
+        b.seq_lens = lens0 - shorten
+        lens.copy_(torch.from_numpy(b.seq_lens))
+        out.zero_()
+        g.replay()
+        torch.cuda.synchronize()
+        ref, ref_lse = oracle.attention(b)
+        assert_close(out.float().cpu().numpy(), ref, "e4m3")
+        assert_lse_close(lse.cpu().numpy(), ref_lse)
