@@ -11,34 +11,35 @@
 // Work per step = PPS pages (64 PPS keys) of one KV head, PPS = 4 for the 8-bit
 // path with up to 32 rows (TMEM allowing) and 2 otherwise; per 128-key tile:
 //   S^T[128 keys][rows]  = K[128 keys][128 dims] . Q^T          (tcgen05.mma, TMEM)
-//   P^T = exp2(S^T - m)  by 128 threads, one key each            (registers -> smem)
+//   P^T = 2^(S^T - m)    by the compute threads, one key each    (registers -> smem)
 //   O^T[128 dims][rows] += V^T[128 dims][64 PPS keys] . P^T      (tcgen05.mma, TMEM)
-// Keys sit on the TMEM lanes for the softmax, so all four compute warps share
-// it; output dims sit on the lanes for O, so each compute thread owns one dim
-// at the segment end and O needs no cross-warp merge.  The row sums l are
+// Keys sit on the TMEM lanes for the softmax, so all compute warps share it;
+// output dims sit on the lanes for O, so each compute thread owns one dim at
+// the segment end and O needs no cross-warp merge.  The row sums l are
 // accumulated in fp32 from the unrounded probabilities, per thread (its key
 // slot) across the steps, and reduced once per segment.
 //
 // E4M3 pages feed the MMA as they are (kind::f8f6f4).  The query rows and the
 // probabilities are each split into two E4M3 terms, hi = e4m3(x) and
-// lo = e4m3(x - hi), accumulated into the same D: their sum carries about
-// 8 significant bits, the precision of bf16, so no widening pass is needed.
-// Queries are scaled per row by a power of two into the E4M3 range (folded
-// into the score scale), so a bf16 query row is carried exactly.  Probabilities are 2^(s - m + 4) with a reference max m that
-// moves only when a score exceeds it by more than 4 (base 2), so P <= 256.
-// bf16 pages use kind::f16 with bf16 Q and P.
+// lo = e4m3(x - hi), side by side in N: their sum carries about 8 significant
+// bits, the precision of bf16, so no widening pass is needed.  Queries are
+// scaled per row by a power of two into the E4M3 range (folded into the score
+// scale), so a bf16 query row is carried exactly.  Probabilities are
+// 2^(s - m + 4) with a reference max m that moves only when a score exceeds it
+// by more than 4 (base 2), so P <= 256.  bf16 pages use kind::f16 with bf16 Q
+// and P.
 //
 // Roles (352 threads): warps 0-7 compute (softmax, epilogue; warps w and w + 4
 // share TMEM lane quarter w % 4 -- the same keys, and the same output dims --
 // and split the query rows), warp 8 TMA producer, warp 9 one thread issuing
-// Q K^T, warp 10 one thread issuing P V.
-// A tcgen05.mma costs its issuing thread about 100 cycles whatever N is, so the
-// two products are issued from two threads and each step issues few, wide
-// MMAs.  S is double-buffered in TMEM so Q K^T of step i+1 overlaps the
-// softmax of step i.  Every wait is
+// Q K^T, warp 10 one thread issuing P V.  A tcgen05.mma costs its issuing
+// thread about 100 cycles whatever N is, so the two products are issued from
+// two threads and each step issues few, wide MMAs.  S is double-buffered in
+// TMEM so Q K^T of step i+1 overlaps the softmax of step i.  Every wait is
 // bounded in time; a role that gives up flags the task map's status word and
-// raises the CTA's abort flag, the MMA thread waits for its MMAs in flight and
-// the producer for its copies, and the CTA frees its TMEM and returns.
+// raises the CTA's abort flag, each MMA thread commits its MMAs to a drain
+// barrier that the CTA waits on, the producer waits for its copies, and the
+// CTA frees its TMEM and returns.
 #include <math_constants.h>
 
 #include <climits>
