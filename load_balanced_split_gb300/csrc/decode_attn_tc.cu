@@ -29,10 +29,10 @@
 // by more than 4 (base 2), so P <= 256.  bf16 pages use kind::f16 with bf16 Q
 // and P.
 //
-// Roles (352 threads): warps 0-7 compute (softmax, epilogue; warps w and w + 4
-// share TMEM lane quarter w % 4 -- the same keys, and the same output dims --
-// and split the query rows), warp 8 TMA producer, warp 9 one thread issuing
-// Q K^T, warp 10 one thread issuing P V.  A tcgen05.mma costs its issuing
+// Roles: CW = 8, 12 or 16 compute warps (softmax, epilogue; the warps with
+// w % 4 equal share TMEM lane quarter w % 4 -- the same keys, and the same
+// output dims -- and split the query rows, at most 16 rows each), then one TMA
+// producer warp, one warp whose thread issues Q K^T and one issuing P V.  A tcgen05.mma costs its issuing
 // thread about 100 cycles whatever N is, so the two products are issued from
 // two threads and each step issues few, wide MMAs.  S is double-buffered in
 // TMEM so Q K^T of step i+1 overlaps the softmax of step i.  Every wait is
@@ -49,8 +49,6 @@
 namespace hpa {
 namespace {
 
-constexpr int kTcComputeWarps = 8;  // two per TMEM lane quarter, splitting the rows
-constexpr int kTcThreads = (kTcComputeWarps + 3) * 32;  // + producer, QK issuer, PV issuer
 constexpr uint32_t kFull = 0xffffffffu;
 
 template <int KV>
@@ -72,6 +70,11 @@ struct TcCfg<HPA_KV_E4M3> {
 template <int KV, int NC>
 struct TcSmem {
   static constexpr int kRp = 16 * NC;
+  // Compute warps: 4 per group of rows, one group per TMEM lane quarter each; a
+  // warp takes at most 16 rows (8 warps up to 32 rows, 12 for 48, 16 for 64).
+  static constexpr int kCW = NC <= 2 ? 8 : 4 * NC;
+  static constexpr int kRH = kRp / (kCW / 4);                  // rows per compute warp
+  static constexpr int kThreads = (kCW + 3) * 32;              // + producer, QK, PV issuers
   // Columns of S and of O: the hi and lo terms of the 8-bit path sit side by side
   // (one MMA with N = 2 Rp instead of two with N = Rp: MMA issue, not tensor math,
   // is what a step of narrow MMAs costs).
@@ -96,8 +99,8 @@ struct TcSmem {
   static constexpr int kP = kQ + 2 * kOperand;                 // 2 probability buffers
   static constexpr int kRowC = kP + 2 * kPBuf;                 // float[2][64] score scales
   static constexpr int kStepMax = kRowC + 2 * 64 * 4;          // float[2][4][64]
-  static constexpr int kFlags = kStepMax + 2 * 4 * 64 * 4;     // int[2][8]
-  static constexpr int kLRed = kFlags + 64;                    // float[4][64] row-sum parts
+  static constexpr int kFlags = kStepMax + 2 * 4 * 64 * 4;     // int[2][16]
+  static constexpr int kLRed = kFlags + 128;                   // float[4][64] row-sum parts
   static constexpr int kJRow = kLRed + 4 * 64 * 4;             // int[64]: token j of row r
   static constexpr int kInfo = kJRow + 64 * 4;                 // int4[2]
   static constexpr int kBars = kInfo + 32;
@@ -505,10 +508,11 @@ struct Tc {
   // rows [hf RH, hf RH + RH) with hf = t / 128.
   static __device__ void compute(const AttnParams &p, uint8_t *smem, int s_begin, int s_end,
                                  uint32_t tmem, int h) {
-    constexpr int RH = kRp / 2;  // rows per warp
+    constexpr int RH = S::kRH;  // rows per warp
+    constexpr int CW = S::kCW;
     constexpr int MT = S::kMT;
     const int t = threadIdx.x, w = t >> 5, lane = t & 31, qd = w & 3, hf = w >> 2;
-    const int kt = t & 127, r0 = hf * RH;
+    const int kt = t & 127, r0 = hf * RH;  // hf: this warp's group of rows
     const uint32_t base = smem_u32(smem), bars = base + S::kBars;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kAbort);
     const uint32_t lane_t = tmem + (static_cast<uint32_t>(32 * qd) << 16);
@@ -612,7 +616,7 @@ struct Tc {
         {
           const bool any = __any_sync(kFull, flag);
           if (lane == 0) {
-            flags[b * 8 + w] = any;
+            flags[b * 16 + w] = any;
             mbar_arrive(bars + 8 * (B_FLAG + b));
           }
         }
@@ -622,7 +626,7 @@ struct Tc {
         }
         int moved = 0;
 #pragma unroll
-        for (int x8 = 0; x8 < 8; ++x8) moved |= flags[b * 8 + x8];
+        for (int x8 = 0; x8 < CW; ++x8) moved |= flags[b * 16 + x8];
         if (moved) {
           float *sm = stepmax + (n_moved & 1) * 4 * 64;
 #pragma unroll
@@ -817,7 +821,7 @@ struct Tc {
 };
 
 template <int KV, int NC>
-__global__ void __launch_bounds__(kTcThreads, 1)
+__global__ void __launch_bounds__(TcSmem<KV, NC>::kThreads, 1)
     decode_attn_tc_kernel(const __grid_constant__ CUtensorMap tmk,
                           const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
   using S = TcSmem<KV, NC>;
@@ -841,10 +845,9 @@ __global__ void __launch_bounds__(kTcThreads, 1)
     hdr[3] = go ? tm[p.lay.cta_seg + c + 1] : 0;
     hdr[0] = go && hdr[2] < hdr[3];
     // q_full q_empty s_full s_free p_full pv_done o_free drain flag smax lred
-    const int counts[18] = {32, 32, 1 + kTcComputeWarps, 1 + kTcComputeWarps, 1, 1,
-                            kTcComputeWarps, kTcComputeWarps, kTcComputeWarps, kTcComputeWarps,
-                            1, 1, kTcComputeWarps, 2, kTcComputeWarps, kTcComputeWarps,
-                            kTcComputeWarps, kTcComputeWarps};
+    constexpr int CW = S::kCW;
+    const int counts[18] = {32, 32, 1 + CW, 1 + CW, 1, 1, CW, CW, CW, CW, 1, 1, CW, 2, CW, CW,
+                            CW, CW};
     for (int i = 0; i < 18; ++i) mbar_init(bars + 8 * i, counts[i]);
     for (int i = 0; i < S::kStages; ++i) {
       mbar_init(bars + 8 * (B_KV_FULL + i), 1);                 // TMA bytes
@@ -870,13 +873,13 @@ __global__ void __launch_bounds__(kTcThreads, 1)
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t *>(smem + S::kTmem);
   const int tile = hdr[1], s_begin = hdr[2], s_end = hdr[3];
   const int warp = threadIdx.x >> 5;
-  if (warp < kTcComputeWarps)
+  if (warp < S::kCW)
     Tc<KV, NC>::compute(p, smem, s_begin, s_end, tmem, h);
-  else if (warp == kTcComputeWarps)
+  else if (warp == S::kCW)
     Tc<KV, NC>::producer(p, &tmk, &tmv, smem, s_begin, s_end, tile, h);
-  else if (warp == kTcComputeWarps + 1 && (threadIdx.x & 31) == 0)
+  else if (warp == S::kCW + 1 && (threadIdx.x & 31) == 0)
     Tc<KV, NC>::qk_issuer(p, smem, s_begin, s_end, tile, tmem);
-  else if (warp == kTcComputeWarps + 2 && (threadIdx.x & 31) == 0)
+  else if (warp == S::kCW + 2 && (threadIdx.x & 31) == 0)
     Tc<KV, NC>::pv_issuer(p, smem, s_begin, s_end, tile, tmem);
   tc_fence_before();
   __syncthreads();
@@ -905,7 +908,7 @@ cudaError_t launch_tc(const AttnParams &p, const CUtensorMap &tmk, const CUtenso
   }
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.C, p.Hkv, 1);
-  cfg.blockDim = dim3(kTcThreads);
+  cfg.blockDim = dim3(TcSmem<KV, NC>::kThreads);
   cfg.dynamicSmemBytes = TcSmem<KV, NC>::kAlloc;
   cfg.stream = s;
   cudaLaunchAttribute attr[1];
@@ -934,7 +937,8 @@ int occupancy_tc(int *ctas) {
                                        TcSmem<KV, NC>::kAlloc);
   if (e != cudaSuccess) return -1;
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, decode_attn_tc_kernel<KV, NC>,
-                                                    kTcThreads, TcSmem<KV, NC>::kAlloc);
+                                                    TcSmem<KV, NC>::kThreads,
+                                                    TcSmem<KV, NC>::kAlloc);
   return e == cudaSuccess ? 0 : -1;
 }
 
