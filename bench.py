@@ -282,29 +282,41 @@ def run_ours(args, rank, world, local_rank):
             "speedup_vs_static_best": round(res[best] / ms, 3),
         }
 
-    # end to end through the public API with host buffers
-    pin = lambda t: t.pin_memory()
-    q_h, lens_h, indptr_h, indices_h = (pin(b.q), pin(torch.from_numpy(b.seq_lens)),
-                                        pin(torch.from_numpy(b.page_indptr)),
-                                        pin(torch.from_numpy(b.page_indices)))
-    out_h = torch.empty(out.shape, dtype=out.dtype).pin_memory()
-    lse_h = torch.empty(out_lse.shape, dtype=out_lse.dtype).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (q_h, lens_h, indptr_h, indices_h))
-    d2h = out_h.numel() * out_h.element_size() + lse_h.numel() * lse_h.element_size()
+    # End to end through the public API with host buffers.  A step's inputs (q,
+    # lengths, page table) sit back to back in one pinned host buffer and one device
+    # buffer, and its outputs (out, lse) likewise, so a step moves them with one copy
+    # each way; the device tensors the calls take are views into those buffers.
+    def packed(tensors, device):
+        offs, total = [], 0
+        for t in tensors:
+            offs.append(total)
+            total += (t.numel() * t.element_size() + 255) // 256 * 256
+        buf = (torch.empty(total, dtype=torch.uint8, device=device) if device is not None
+               else torch.empty(total, dtype=torch.uint8).pin_memory())
+        views = [buf[o:o + t.numel() * t.element_size()].view(t.dtype).view(t.shape)
+                 for o, t in zip(offs, tensors)]
+        return buf, views
+
+    inputs = [b.q, torch.from_numpy(b.seq_lens), torch.from_numpy(b.page_indptr),
+              torch.from_numpy(b.page_indices)]
+    in_h, in_h_views = packed(inputs, None)
+    for dst, src in zip(in_h_views, inputs):
+        dst.copy_(src)
+    in_d, (q_e, lens_e, indptr_e, indices_e) = packed(inputs, dev)
+    out_d, (out_e, lse_e) = packed([out, out_lse], dev)
+    out_h, _ = packed([out, out_lse], None)
+    h2d = in_h.numel()
+    d2h = out_h.numel()
 
     def e2e_step(ev=None):
         if ev is not None:
             ev[0].record(stream)
         with torch.cuda.stream(stream):
-            q.copy_(q_h, non_blocking=True)
-            lens.copy_(lens_h, non_blocking=True)
-            indptr.copy_(indptr_h, non_blocking=True)
-            indices.copy_(indices_h, non_blocking=True)
-        hpa.decode_step(ws, q, k, v, lens, indptr, indices, out, out_lse, ks, vs, tile=b.tile,
-                        stream=stream, tc=tc)
+            in_d.copy_(in_h, non_blocking=True)
+        hpa.decode_step(ws, q_e, k, v, lens_e, indptr_e, indices_e, out_e, lse_e, ks, vs,
+                        tile=b.tile, stream=stream, tc=tc)
         with torch.cuda.stream(stream):
-            out_h.copy_(out, non_blocking=True)
-            lse_h.copy_(out_lse, non_blocking=True)
+            out_h.copy_(out_d, non_blocking=True)
         if ev is not None:
             for e in ev[1:]:
                 e.record(stream)
