@@ -75,7 +75,8 @@ def test_plan_argument_checks():
     assert L.hpa_plan_static(FAKE, 3, 512, 0, FAKE, nb, None) == -1
 
 
-def test_attention_argument_checks():
+@pytest.mark.parametrize("entry", ["hpa_decode_attn", "hpa_decode_attn_tc"])
+def test_attention_argument_checks(entry):
     L = hpa.lib()
     args = dict(q=FAKE, k=FAKE, v=FAKE, kv=0, ks=None, vs=None, P=100, indptr=FAKE,
                 indices=FAKE, page=64, B=3, q_len=1, Hq=64, Hkv=8, d=128, scale=0.088,
@@ -83,7 +84,7 @@ def test_attention_argument_checks():
 
     def call(**kw):
         a = dict(args, **kw)
-        return L.hpa_decode_attn(a["q"], a["k"], a["v"], a["kv"], a["ks"], a["vs"], a["P"],
+        return getattr(L, entry)(a["q"], a["k"], a["v"], a["kv"], a["ks"], a["vs"], a["P"],
                                  a["indptr"], a["indices"], a["page"], a["B"], a["q_len"],
                                  a["Hq"], a["Hkv"], a["d"], a["scale"], a["tm"], a["C"],
                                  a["po"], a["pl"], None)
