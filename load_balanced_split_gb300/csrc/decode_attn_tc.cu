@@ -379,8 +379,8 @@ struct Tc {
     }
   }
 
-  // ---- warps 5 and 6, one thread each: the MMAs.  Both walk the same segments
-  // and page pairs as the producer; st / i / phase follow the same sequence.
+  // ---- the two MMA warps, one thread each.  Both walk the same segments
+  // and steps as the producer; st / i / phase follow the same sequence.
   static __device__ void mma_done(const AttnParams &p, uint8_t *smem, bool ok) {
     const uint32_t bars = smem_u32(smem) + S::kBars;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kAbort);
@@ -404,13 +404,13 @@ struct Tc {
       const int4 sg = reinterpret_cast<const int4 *>(p.tm + p.lay.segs)[s];
       const int L = p.tm[p.lay.lens + sg.x];
       const int pg0 = sg.y * tile / PAGE, pg1 = (min(sg.z * tile, L) + PAGE - 1) / PAGE;
-      const int npairs = (pg1 - pg0 + S::kPPS - 1) / S::kPPS;  // steps
+      const int nsteps = (pg1 - pg0 + S::kPPS - 1) / S::kPPS;
       if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_Q_FULL + slot), (k >> 1) & 1)) {
         ok = false;
         break;
       }
       const uint32_t qbase = base + S::kQ + slot * S::kOperand;
-      for (int j = 0; j < npairs; ++j) {
+      for (int j = 0; j < nsteps; ++j) {
         const int b = i & 1;
         if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_KV_FULL + st), phase) ||
             !mbar_wait_bounded(bars + 8 * (B_S_FREE + b), ((i >> 1) & 1) ^ 1)) {
@@ -441,7 +441,7 @@ struct Tc {
           }
         }
         tc_commit(bars + 8 * (B_S_FULL + b));
-        if (j == npairs - 1) tc_commit(bars + 8 * (B_Q_EMPTY + slot));
+        if (j == nsteps - 1) tc_commit(bars + 8 * (B_Q_EMPTY + slot));
         ++i;
         if (++st == S::kStages) {
           st = 0;
@@ -464,8 +464,8 @@ struct Tc {
       const int4 sg = reinterpret_cast<const int4 *>(p.tm + p.lay.segs)[s];
       const int L = p.tm[p.lay.lens + sg.x];
       const int pg0 = sg.y * tile / PAGE, pg1 = (min(sg.z * tile, L) + PAGE - 1) / PAGE;
-      const int npairs = (pg1 - pg0 + S::kPPS - 1) / S::kPPS;  // steps
-      for (int j = 0; j < npairs; ++j) {
+      const int nsteps = (pg1 - pg0 + S::kPPS - 1) / S::kPPS;
+      for (int j = 0; j < nsteps; ++j) {
         const int b = i & 1;
         // P of this step written; at a segment start, the previous segment's O read out
         if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_P_FULL + b), (i >> 1) & 1) ||
@@ -534,7 +534,7 @@ struct Tc {
       const int4 inf = reinterpret_cast<const int4 *>(smem + S::kInfo)[slot];
       const int L = inf.y, klo = inf.z, khi = inf.w;
       const int pg0 = klo / PAGE, pg1 = (khi + PAGE - 1) / PAGE;
-      const int npairs = (pg1 - pg0 + S::kPPS - 1) / S::kPPS;  // steps
+      const int nsteps = (pg1 - pg0 + S::kPPS - 1) / S::kPPS;
       if (L < q_len && t == 0) status_or(p.tm, HPA_STATUS_BAD_SEQLEN);
       const uint32_t rowc_s = base + S::kRowC + (slot * 64 + r0) * 4;
       const float c_all = p.scale_log2;  // bf16: one score scale for every row
@@ -545,7 +545,7 @@ struct Tc {
         lsum[e] = 0.f;
       }
 
-      for (int jp = 0; jp < npairs; ++jp) {
+      for (int jp = 0; jp < nsteps; ++jp) {
         const int b = i & 1, st = i % S::kStages;
         if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_S_FULL + b), (i >> 1) & 1)) {
           ok = false;
@@ -657,7 +657,7 @@ struct Tc {
             lsum[e] *= alpha[e];
           }
           if (jp > 0 && __any_sync(kFull, rescale)) {
-            // O holds the earlier pairs of this segment: wait for the last P V, then
+            // O holds the earlier steps of this segment: wait for the last P V, then
             // rescale this warp's rows of it in TMEM (lane = output dim kt)
             const int pi = i - 1;
             if (*abort_flag ||
@@ -756,7 +756,7 @@ struct Tc {
         __syncwarp();
         if (lane == 0) mbar_arrive(bars + 8 * (B_P_FULL + b));
 
-        if (jp == npairs - 1) {
+        if (jp == nsteps - 1) {
           // ---- segment end: l per row (sum over the 128 key slots), then O / l for
           // this warp's rows, this thread's dim kt
 #pragma unroll
