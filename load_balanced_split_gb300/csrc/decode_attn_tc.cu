@@ -226,7 +226,7 @@ struct Tc {
   using S = TcSmem<KV, NC>;
   static constexpr int kRp = S::kRp;
 
-  // ---- warp 4: query staging and TMA copies
+  // ---- the TMA warp (after the compute warps): query staging and the K/V copies
   static __device__ void producer(const AttnParams &p, const CUtensorMap *tmk,
                                   const CUtensorMap *tmv, uint8_t *smem, int s_begin,
                                   int s_end, int tile, int h) {
@@ -503,7 +503,7 @@ struct Tc {
     mma_done(p, smem, ok);
   }
 
-  // ---- warps 0-7: softmax and the segment epilogue.  Thread t: key slots
+  // ---- the compute warps: softmax and the segment epilogue.  Thread t: key slots
   // kt + 128 m of the step (m < kMT) and output dim kt = t % 128 (its TMEM lane),
   // rows [hf RH, hf RH + RH) with hf = t / 128.
   static __device__ void compute(const AttnParams &p, uint8_t *smem, int s_begin, int s_end,
