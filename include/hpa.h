@@ -189,7 +189,8 @@ int hpa_decode_attn(const void *q_dev, const void *k_pool_dev, const void *v_poo
  * (up to 64) in a single pass over the keys, where hpa_decode_attn makes one
  * pass per group of 16 rows.  It pays for MTP with more than 16 rows per KV
  * head (on the E4M3 MTP workload at 64/8 heads: 1.3x at q_len 3-4, 1.5x at
- * q_len 6, about even at q_len 8); with up to 16 rows hpa_decode_attn is as
+ * q_len 6, about even at q_len 8).  With up to 16 rows, or with many short
+ * segments per partition (hundreds of short requests), hpa_decode_attn is as
  * fast or faster.
  * Arguments, layouts, supported shapes, outputs and errors are exactly those
  * of hpa_decode_attn; the partials feed hpa_combine unchanged.  E4M3 pages
