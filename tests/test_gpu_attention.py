@@ -277,3 +277,13 @@ def test_mtp_more_draft_tokens(q_len, kv):
 def test_mtp_rows_not_a_multiple_of_16():
     b = W.make_batch([100, 2000], q_len=3, Hq=24, Hkv=4, seed=7)    # 6 heads x 3 tokens = 18 rows
     check(b, num_ctas=4)
+
+
+@pytest.mark.parametrize("Hq,Hkv,q_len,kv", [(8, 8, 1, "bf16"), (8, 8, 2, "e4m3"),
+                                             (64, 1, 1, "e4m3"), (32, 2, 2, "bf16")])
+def test_head_layouts(Hq, Hkv, q_len, kv):
+    """MHA (one query row per KV head), MQA (one KV head for 64 query heads: 64 rows)
+    and 16 query heads per KV head with two tokens."""
+    b = W.make_batch([q_len, 70, 1000, 5000], q_len=q_len, kv_dtype=kv, Hq=Hq, Hkv=Hkv,
+                     seed=Hq + Hkv + q_len)
+    check(b, num_ctas=5)

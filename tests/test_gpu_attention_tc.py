@@ -168,3 +168,13 @@ def test_three_calls_capture_in_a_cuda_graph():
         ref, ref_lse = oracle.attention(b)
         assert_close(out.float().cpu().numpy(), ref, "e4m3")
         assert_lse_close(lse.cpu().numpy(), ref_lse)
+
+
+@pytest.mark.parametrize("Hq,Hkv,q_len,kv", [(8, 8, 1, "bf16"), (8, 8, 2, "e4m3"),
+                                             (64, 1, 1, "e4m3"), (32, 2, 2, "bf16")])
+def test_head_layouts(Hq, Hkv, q_len, kv):
+    """MHA (one query row per KV head), MQA (one KV head for 64 query heads: 64 rows)
+    and 16 query heads per KV head with two tokens."""
+    b = W.make_batch([q_len, 70, 1000, 5000], q_len=q_len, kv_dtype=kv, Hq=Hq, Hkv=Hkv,
+                     seed=Hq + Hkv + q_len)
+    check(b, num_ctas=5)
