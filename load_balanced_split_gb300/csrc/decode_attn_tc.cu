@@ -202,6 +202,14 @@ __device__ __forceinline__ void tc_wait_st() {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// Two f16 (element 0 in the low half) -> two E4M3 codes, round to nearest even,
+// saturating.
+__device__ __forceinline__ uint16_t f16x2_to_e4m3x2(uint32_t v) {
+  uint16_t r;
+  asm("cvt.rn.satfinite.e4m3x2.f16x2 %0, %1;" : "=h"(r) : "r"(v));
+  return r;
+}
+
 __device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
   asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
@@ -728,10 +736,13 @@ struct Tc {
                 const float p1 = exp2f(x[m][a0 + 1] - b1 + kPOff);
                 lsum[a0] += p0;
                 lsum[a0 + 1] += p1;
-                const uint16_t h2 = f32x2_to_e4m3x2(p0, p1);
+                // hi = e4m3(p), lo = e4m3(p - hi), the residual taken in f16 (exact there)
+                const uint32_t pf = pack_f16(p0, p1);
+                const uint16_t h2 = f16x2_to_e4m3x2(pf);
                 const uint32_t hh = e4m3x2_to_f16x2(h2);
-                const float2 hv = __half22float2(*reinterpret_cast<const __half2 *>(&hh));
-                const uint16_t l2 = f32x2_to_e4m3x2(p0 - hv.x, p1 - hv.y);
+                const __half2 rr2 = __hsub2(*reinterpret_cast<const __half2 *>(&pf),
+                                            *reinterpret_cast<const __half2 *>(&hh));
+                const uint16_t l2 = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t *>(&rr2));
                 hi |= static_cast<uint32_t>(h2) << (8 * e);
                 lo |= static_cast<uint32_t>(l2) << (8 * e);
               }
