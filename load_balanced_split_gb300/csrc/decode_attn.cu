@@ -24,6 +24,8 @@
 //    status word, waits for its own copies in flight and returns.
 #include <math_constants.h>
 
+#include <type_traits>
+
 #include "hpa_internal.cuh"
 
 namespace hpa {
@@ -31,11 +33,18 @@ namespace {
 
 constexpr int kConsumerWarps = 4;
 // Segment-end merge buffers (two): one row of 128 partial-output columns per
-// query row, held in accumulator-fragment order (n-tile i, column n -> i * 8 + n)
-// and padded to 136 floats so a warp's fragment stores hit at most 2 lanes per
-// bank.  Warps 0 / 1 store into buffers A / B, warps 2 / 3 add into them, and
+// query row.  Warps 0 / 1 store into buffers A / B, warps 2 / 3 add into them, and
 // the read-out sums A + B: plain shared-memory traffic, no atomics.
-constexpr int kMergeStride = HEAD_DIM + 8;
+//  * bf16: the accumulators hold dim 8 i + n (n-tile i, column n); rows of 136
+//    floats keep a warp's float2 fragment stores at 2 lanes per bank at most;
+//  * E4M3: a thread holds the 32 contiguous dims [32 qd, 32 qd + 32) of its two
+//    rows (the output-column permutation of the 8-bit V path), so it stores them
+//    as float4s in dim order; each 32-dim chunk is padded by 4 floats (rows of
+//    144) so those stores take the minimum 4 wavefronts, and the read-out loads
+//    float4s.
+template <int KV>
+constexpr int kMergeStrideOf = KV == HPA_KV_E4M3 ? HEAD_DIM + 16 : HEAD_DIM + 8;
+__host__ __device__ constexpr int merge_phys(int dd) { return dd + 4 * (dd >> 5); }
 // Largest score excess (log2 units) over the running reference max before the
 // accumulators are rescaled: P values stay <= 256, well inside bf16/f16 range.
 constexpr float kRescaleSlack = 8.f;
@@ -68,6 +77,7 @@ template <int KV>
 struct Smem {
   static constexpr int kStageBytes = 2 * Cfg<KV>::kKBytes;
   static constexpr int kStages = Cfg<KV>::kStages;
+  static constexpr int kMergeStride = kMergeStrideOf<KV>;
   static constexpr int kMerge = kStages * kStageBytes;  // float[2][16][kMergeStride]
   static constexpr int kStats = kMerge + 2 * MAX_ROWS * kMergeStride * 4;  // m[4][16], l[4][16]
   static constexpr int kQ = kStats + 2 * kConsumerWarps * MAX_ROWS * 4;  // 2 query slots
@@ -313,15 +323,6 @@ __device__ __forceinline__ void pv(float (&o)[16][4], const uint32_t (&pa)[4], u
       }
     }
   }
-}
-
-// Merge-buffer position of head dim dd.  The bf16 accumulators hold dim 8 i + n in
-// n-tile i, column n; the E4M3 ones hold dim 16 n + i (the output-column permutation
-// of the 8-bit V path).  The buffer is in fragment order i * 8 + n either way.
-template <int KV>
-__device__ __forceinline__ int merge_pos(int dd) {
-  if (KV == HPA_KV_BF16) return dd;
-  return (dd & 15) * 8 + (dd >> 4);
 }
 
 __device__ __forceinline__ void store_bf16x4(__nv_bfloat16 *dst, float4 v) {
@@ -592,36 +593,59 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
     row_stats(row1, M1, L1);
     const float f0 = L0 > 0.f ? exp2f(m0 - M0) / L0 * vsc : 0.f;
     const float f1 = L1 > 0.f ? exp2f(m1 - M1) / L1 * vsc : 0.f;
-    float *mine = mbuf + (w & 1) * (MAX_ROWS * kMergeStride);
-    if (w < 2) {
+    constexpr int MS = S::kMergeStride;
+    float *mine = mbuf + (w & 1) * (MAX_ROWS * MS);
+    // one merge pass: warps 0 / 1 store (ADD = false), then warps 2 / 3 add
+    auto merge = [&](auto add_tag) {
+      constexpr bool ADD = decltype(add_tag)::value;
+      if (KV == HPA_KV_BF16) {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int pos = i * 8 + 2 * qd;
-        if (v0)
-          *reinterpret_cast<float2 *>(mine + row0 * kMergeStride + pos) =
-              make_float2(o[i][0] * f0, o[i][1] * f0);
-        if (v1)
-          *reinterpret_cast<float2 *>(mine + row1 * kMergeStride + pos) =
-              make_float2(o[i][2] * f1, o[i][3] * f1);
+        for (int i = 0; i < 16; ++i) {
+          const int pos = i * 8 + 2 * qd;
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) {
+            if (hr == 0 ? !v0 : !v1) continue;
+            float2 *d = reinterpret_cast<float2 *>(mine + (hr ? row1 : row0) * MS + pos);
+            const float fs = hr ? f1 : f0;
+            float2 nv = make_float2(o[i][2 * hr] * fs, o[i][2 * hr + 1] * fs);
+            if (ADD) {
+              const float2 t = *d;
+              nv.x += t.x;
+              nv.y += t.y;
+            }
+            *d = nv;
+          }
+        }
+      } else {
+        // o[i][c] of row hr holds dim 32 qd + 16 (c & 1) + i
+#pragma unroll
+        for (int hr = 0; hr < 2; ++hr) {
+          if (hr == 0 ? !v0 : !v1) continue;
+          const float fs = hr ? f1 : f0;
+          float *rowp = mine + (hr ? row1 : row0) * MS;
+#pragma unroll
+          for (int half = 0; half < 2; ++half)
+#pragma unroll
+            for (int k = 0; k < 4; ++k) {
+              float4 *d = reinterpret_cast<float4 *>(rowp + merge_phys(32 * qd + 16 * half + 4 * k));
+              const int c = 2 * hr + half;
+              float4 nv = make_float4(o[4 * k][c] * fs, o[4 * k + 1][c] * fs,
+                                      o[4 * k + 2][c] * fs, o[4 * k + 3][c] * fs);
+              if (ADD) {
+                const float4 t = *d;
+                nv.x += t.x;
+                nv.y += t.y;
+                nv.z += t.z;
+                nv.w += t.w;
+              }
+              *d = nv;
+            }
+        }
       }
-    }
+    };
+    if (w < 2) merge(std::false_type());
     named_barrier(1, kConsumerWarps * 32);
-    if (w >= 2) {
-#pragma unroll
-      for (int i = 0; i < 16; ++i) {
-        const int pos = i * 8 + 2 * qd;
-        if (v0) {
-          float2 *d = reinterpret_cast<float2 *>(mine + row0 * kMergeStride + pos);
-          const float2 t = *d;
-          *d = make_float2(t.x + o[i][0] * f0, t.y + o[i][1] * f0);
-        }
-        if (v1) {
-          float2 *d = reinterpret_cast<float2 *>(mine + row1 * kMergeStride + pos);
-          const float2 t = *d;
-          *d = make_float2(t.x + o[i][2] * f1, t.y + o[i][3] * f1);
-        }
-      }
-    }
+    if (w >= 2) merge(std::true_type());
     named_barrier(1, kConsumerWarps * 32);
     const int tid = threadIdx.x;
     // fused combine, single-segment request: this segment is the whole result
@@ -631,21 +655,12 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
       const int j = (rb + row) / G, g = (rb + row) % G;
       const int64_t dst = ((static_cast<int64_t>(direct ? f.r : s) * q_len + j) * p.Hq + h * G + g) *
                           HEAD_DIM;
-      const float *ra = mbuf + row * kMergeStride;           // buffer A
-      const float *rb2 = ra + MAX_ROWS * kMergeStride;         // buffer B
-      float4 val;
-      if (KV == HPA_KV_BF16) {
-        const float4 a = *reinterpret_cast<const float4 *>(ra + 4 * c4);
-        const float4 b = *reinterpret_cast<const float4 *>(rb2 + 4 * c4);
-        val = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
-      } else {
-        float *x = &val.x;
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          const int pos = merge_pos<KV>(4 * c4 + k);
-          x[k] = ra[pos] + rb2[pos];
-        }
-      }
+      const float *ra = mbuf + row * MS;           // buffer A
+      const float *rb2 = ra + MAX_ROWS * MS;         // buffer B
+      const int pos = KV == HPA_KV_BF16 ? 4 * c4 : merge_phys(4 * c4);
+      const float4 a = *reinterpret_cast<const float4 *>(ra + pos);
+      const float4 b = *reinterpret_cast<const float4 *>(rb2 + pos);
+      const float4 val = make_float4(a.x + b.x, a.y + b.y, a.z + b.z, a.w + b.w);
       if (direct)
         store_bf16x4(p.out + dst + 4 * c4, val);
       else
