@@ -42,8 +42,8 @@ UNIT = "us/batch"
 # Taken on the uniform 32 x 8192 batch (1.07 GB KV; the mixed batch is too large to capture
 # with every section) and scaled by KV bytes, since traffic grows with the KV read.
 TRAFFIC_PROFILE = {
-    "source_sha256": "7fbf75bf04def951e0f50891049ca26f5aecd991830f10ec5475592e9bba96e9",
-    "bytes_per_kv_byte": (1074363000 + 3833088) / 1073741824,
+    "source_sha256": "80760069db5fb18d6dc788cf74cb81e5f46581dccee0b0709cb6c10db7c142ea",
+    "bytes_per_kv_byte": (1074352384 + 3225856) / 1073741824,
     "workload": "uniform_32x8k_paged (profiles/decode_attn_uniform_32x8k_bf16_full.md)",
 }
 
