@@ -10,7 +10,8 @@ import load_balanced_split_gb300 as hpa
 
 HEADER = 16
 
-# Output tolerance: |d| <= ABS and |d| <= REL * max(|ref|, rms of the ref row of d values).
+# Output tolerance: |d| <= ABS (+ half an ulp of bf16 at ref, for outputs stored as bf16)
+# and |d| <= REL * max(|ref|, rms of the ref row of d values).
 TOL = {"bf16": (1e-2, 2e-2), "e4m3": (5e-2, 5e-2)}
 LSE_REL = 1e-4  # |d lse| <= 1e-4 * max(|ref lse|, 1)
 
@@ -107,6 +108,10 @@ def run_gpu(b, num_ctas=None, splits=None, tile=512, db=None, fused=False, weigh
 
 
 def assert_close(got, ref, kv, what="out"):
+    """Element-wise check against the fp64 reference.  The absolute bound covers the
+    attention arithmetic; outputs stored as bf16 (everything but the fp32 split
+    partials) also carry their own rounding, up to half an ulp of bf16 at the
+    reference value (2^-6 for |ref| in [4, 8), more than 1e-2 on its own)."""
     ab, rel = TOL[kv]
     ref = np.asarray(ref, np.float64)
     got = np.asarray(got, np.float64)
@@ -114,6 +119,11 @@ def assert_close(got, ref, kv, what="out"):
     rms = np.sqrt((ref ** 2).mean(axis=-1, keepdims=True))
     floor = np.maximum(np.abs(ref), rms)
     d = np.abs(got - ref)
+    if not what.startswith("partial"):
+        aref = np.abs(ref)
+        with np.errstate(divide="ignore"):
+            half_ulp = np.where(aref > 0, 2.0 ** (np.floor(np.log2(np.where(aref > 0, aref, 1.0))) - 8), 0.0)
+        ab = ab + half_ulp
     bad = (d > ab) | (d > rel * floor)
     if bad.any():
         i = np.unravel_index(np.argmax(d / np.maximum(floor, 1e-30)), d.shape)

@@ -287,3 +287,11 @@ def test_head_layouts(Hq, Hkv, q_len, kv):
     b = W.make_batch([q_len, 70, 1000, 5000], q_len=q_len, kv_dtype=kv, Hq=Hq, Hkv=Hkv,
                      seed=Hq + Hkv + q_len)
     check(b, num_ctas=5)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_thousands_of_short_requests(kv):
+    """3000 requests of 2-300 keys: thousands of segments, many per partition."""
+    lens = np.random.default_rng(31).integers(2, 301, size=3000)
+    b = W.make_batch(lens, q_len=2, kv_dtype=kv, seed=31)
+    check(b)
