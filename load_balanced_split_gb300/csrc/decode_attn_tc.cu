@@ -106,8 +106,8 @@ struct TcSmem {
   static constexpr int kBars = kInfo + 32;
   // q_full[2] q_empty[2] s_full[2] s_free[2] p_full[2] pv_done[2] o_free drain flag[2]
   // smax lred kv_full[kStages] kv_empty[kStages]
-  static constexpr int kNumBars = 18 + 2 * kStages;
-  static constexpr int kKvEmpty = 18 + kStages;  // first kv_empty barrier (after kv_full)
+  static constexpr int kNumBars = 30 + 2 * kStages;
+  static constexpr int kKvEmpty = 30 + kStages;  // first kv_empty barrier (after kv_full)
   static constexpr int kTmem = kBars + kNumBars * 8;           // TMEM base address
   static constexpr int kAbort = kTmem + 4;
   static constexpr int kBytes = kAbort + 4;
@@ -124,7 +124,8 @@ struct TcSmem {
 
 enum TcBar : int {
   B_Q_FULL = 0, B_Q_EMPTY = 2, B_S_FULL = 4, B_S_FREE = 6, B_P_FULL = 8, B_PV_DONE = 10,
-  B_O_FREE = 12, B_DRAIN = 13, B_FLAG = 14, B_SMAX = 16, B_LRED = 17, B_KV_FULL = 18
+  // per row group g (the 4 warps that share rows): flag[b][g], smax[g], lred[g]
+  B_O_FREE = 12, B_DRAIN = 13, B_FLAG = 14, B_SMAX = 22, B_LRED = 26, B_KV_FULL = 30
 };
 
 
@@ -619,22 +620,23 @@ struct Tc {
 #pragma unroll
           for (int e = 0; e < RH; ++e) flag |= x[m][e] > mref[e] + kSlack;
         // A reference max moves only when some score exceeds it by more than the slack.
-        // The warps agree through mbarriers (bounded waits), never named barriers: a
-        // warp that gives up must not leave the others waiting without a limit.
+        // The 4 warps that share this warp's rows agree through an mbarrier of their own
+        // (bounded waits, never named barriers: a warp that gives up must not leave the
+        // others waiting without a limit).
         {
           const bool any = __any_sync(kFull, flag);
           if (lane == 0) {
-            flags[b * 16 + w] = any;
-            mbar_arrive(bars + 8 * (B_FLAG + b));
+            flags[b * 16 + w] = any;  // w = 4 hf + qd
+            mbar_arrive(bars + 8 * (B_FLAG + 4 * b + hf));
           }
         }
-        if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_FLAG + b), (i >> 1) & 1)) {
+        if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_FLAG + 4 * b + hf), (i >> 1) & 1)) {
           ok = false;
           break;
         }
         int moved = 0;
 #pragma unroll
-        for (int x8 = 0; x8 < CW; ++x8) moved |= flags[b * 16 + x8];
+        for (int x4 = 0; x4 < 4; ++x4) moved |= flags[b * 16 + 4 * hf + x4];
         if (moved) {
           float *sm = stepmax + (n_moved & 1) * 4 * 64;
 #pragma unroll
@@ -646,8 +648,8 @@ struct Tc {
             if (lane == 0) sm[qd * 64 + r0 + e] = mx;
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(bars + 8 * B_SMAX);
-          if (*abort_flag || !mbar_wait_bounded(bars + 8 * B_SMAX, n_moved & 1)) {
+          if (lane == 0) mbar_arrive(bars + 8 * (B_SMAX + hf));
+          if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_SMAX + hf), n_moved & 1)) {
             ok = false;
             break;
           }
@@ -778,8 +780,8 @@ struct Tc {
             if (lane == 0) lred[qd * 64 + r0 + e] = v;
           }
           __syncwarp();
-          if (lane == 0) mbar_arrive(bars + 8 * B_LRED);
-          if (*abort_flag || !mbar_wait_bounded(bars + 8 * B_LRED, n_seg & 1) ||
+          if (lane == 0) mbar_arrive(bars + 8 * (B_LRED + hf));
+          if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_LRED + hf), n_seg & 1) ||
               !mbar_wait_bounded(bars + 8 * (B_PV_DONE + b), (i >> 1) & 1)) {
             ok = false;
             break;
@@ -857,9 +859,11 @@ __global__ void __launch_bounds__(TcSmem<KV, NC>::kThreads, 1)
     hdr[0] = go && hdr[2] < hdr[3];
     // q_full q_empty s_full s_free p_full pv_done o_free drain flag smax lred
     constexpr int CW = S::kCW;
-    const int counts[18] = {32, 32, 1 + CW, 1 + CW, 1, 1, CW, CW, CW, CW, 1, 1, CW, 2, CW, CW,
-                            CW, CW};
-    for (int i = 0; i < 18; ++i) mbar_init(bars + 8 * i, counts[i]);
+    // q_full q_empty s_full s_free p_full pv_done o_free drain; then per row group
+    // (4 warps each) flag[2][4] smax[4] lred[4]
+    const int counts[30] = {32, 32, 1 + CW, 1 + CW, 1, 1, CW, CW, CW, CW, 1, 1, CW, 2,
+                            4, 4, 4, 4, 4, 4, 4, 4, 4, 4, 4, 4, 4, 4, 4, 4};
+    for (int i = 0; i < 30; ++i) mbar_init(bars + 8 * i, counts[i]);
     for (int i = 0; i < S::kStages; ++i) {
       mbar_init(bars + 8 * (B_KV_FULL + i), 1);                 // TMA bytes
       mbar_init(bars + 8 * (S::kKvEmpty + i), 1);      // MMA commit
