@@ -376,7 +376,10 @@ class Workspace:
 
     Sized once for (B, num_ctas, q_len, Hq, d) -- dynamic map by default, or
     the static comparator with `splits`.  Allocation is done with torch; the
-    library itself never allocates.
+    library itself never allocates.  num_ctas (partitions per KV head) is
+    normally hpa_default_num_ctas(...) for the mma.sync attention kernel, or
+    hpa_default_num_ctas_tc(...) when the step runs the tcgen05 kernel
+    (decode_step(..., tc=True)); either kernel accepts any partition count.
     """
 
     def __init__(self, B, q_len, Hq, d, num_ctas=None, splits=None, device="cuda", Hkv=8,
