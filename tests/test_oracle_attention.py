@@ -1,7 +1,9 @@
 """Pins of the oracle's fp64 attention and merge against independent facts.
 
 - bit decoders: every bf16 / E4M3 code against torch's own conversions;
-- closed forms: one key, identical keys, zero query, a dominant key;
+- closed forms: one key, identical keys, zero query, a dominant key, two keys
+  worked by hand (with the first MTP token's causal row);
+- brute force: pure-Python scalar loops on tiny inputs (d <= 4, L <= 8);
 - library routines: torch scaled_dot_product_attention and torch.logsumexp in
   float64 on the explicitly expanded (GQA-repeated, page-gathered) tensors;
 - invariants: causal MTP rows, page-table permutation, GQA grouping;
@@ -127,6 +129,84 @@ def test_dominant_key():
     out, _ = oracle.attention(b)
     v21 = dense_kv(b, "v")[0][21, 0].numpy()
     np.testing.assert_allclose(out[0, 0], np.broadcast_to(v21, (8, 16)), atol=1e-10)
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+def test_two_keys_by_hand(kv):
+    """d = 4 (scale 1/2), q = (1,1,1,1), k0 = 0, k1 = (1,1,0,0): the scores are 0 and 1,
+    so the weights are 1/(1+e) and e/(1+e). With v0 = (1,0,0,0) and v1 = (0,2,0,0)
+    the output is (1/(1+e), 2e/(1+e), 0, 0) and lse = ln(1+e). With two new tokens,
+    the first sits at position 0 and sees only key 0: out = v0, lse = 0."""
+    for q_len in (1, 2):
+        b = small_batch([2], q_len=q_len, kv=kv, Hq=1, Hkv=1, d=4, page=4, shuffle=False)
+        b.q[:] = 1.0
+        if kv == "bf16":
+            b.k_pool.zero_()
+            b.v_pool.zero_()
+            b.k_pool[0, 0, 1, :2] = 1.0
+            b.v_pool[0, 0, 0, 0] = 1.0
+            b.v_pool[0, 0, 1, 1] = 2.0
+        else:
+            # E4M3 codes (bias 7): 0x30 = 0.5, 0x38 = 1.0, 0x40 = 2.0; the per-head
+            # scales bring k1 to (1,1,0,0), v0 to (1,0,0,0) and v1 to (0,2,0,0)
+            b.k_scale[:] = 0.5
+            b.v_scale[:] = 2.0
+            b.k_pool.zero_()
+            b.v_pool.zero_()
+            b.k_pool[0, 0, 1, :2] = 0x40
+            b.v_pool[0, 0, 0, 0] = 0x30
+            b.v_pool[0, 0, 1, 1] = 0x38
+        out, lse = oracle.attention(b)
+        e = math.e
+        last = q_len - 1
+        np.testing.assert_allclose(out[0, last, 0], [1 / (1 + e), 2 * e / (1 + e), 0, 0],
+                                   rtol=1e-14, atol=1e-16)
+        np.testing.assert_allclose(lse[0, last, 0], math.log(1 + e), rtol=1e-14)
+        if q_len == 2:
+            np.testing.assert_array_equal(out[0, 0, 0], [1.0, 0, 0, 0])
+            assert lse[0, 0, 0] == 0.0
+
+
+def scalar_attention(b):
+    """Pure-Python scalar loops over the definition: exp without max-subtraction,
+    sums in visiting order, keys decoded by torch (tiny inputs only)."""
+    G = b.Hq // b.Hkv
+    K, V = dense_kv(b, "k"), dense_kv(b, "v")
+    out = np.zeros((b.B, b.q_len, b.Hq, b.d))
+    lse = np.zeros((b.B, b.q_len, b.Hq))
+    for r, L in enumerate(b.seq_lens):
+        Kr, Vr = K[r].tolist(), V[r].tolist()
+        for j in range(b.q_len):
+            visible = L - b.q_len + 1 + j
+            for g in range(b.Hq):
+                h = g // G
+                q = b.q[r, j, g].to(F64).tolist()
+                w = []
+                for k in range(visible):
+                    dot = 0.0
+                    for i in range(b.d):
+                        dot += q[i] * Kr[k][h][i]
+                    w.append(math.exp(dot / math.sqrt(b.d)))
+                Z = sum(w)
+                for i in range(b.d):
+                    out[r, j, g, i] = sum(w[k] * Vr[k][h][i] for k in range(visible)) / Z
+                lse[r, j, g] = math.log(Z)
+    return out, lse
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_brute_force_tiny(seed):
+    """d <= 4, L <= 8, one or two new tokens, up to 2 KV heads, both KV types."""
+    rng = np.random.default_rng(100 + seed)
+    q_len = 1 + seed % 2
+    lens = rng.integers(q_len, 9, size=int(rng.integers(1, 4)))
+    Hkv = 1 + (seed // 2) % 2
+    b = small_batch(lens, q_len=q_len, kv="e4m3" if seed % 4 >= 2 else "bf16", seed=seed,
+                    Hq=2 * Hkv, Hkv=Hkv, d=int(rng.choice([2, 4])), page=int(rng.choice([1, 2, 4])))
+    out, lse = oracle.attention(b)
+    ref_o, ref_l = scalar_attention(b)
+    np.testing.assert_allclose(out, ref_o, rtol=1e-13, atol=1e-15)
+    np.testing.assert_allclose(lse, ref_l, rtol=1e-13, atol=1e-15)
 
 
 # ----------------------------------------------------------------------------- library routine
