@@ -87,9 +87,13 @@ struct TcSmem {
   static constexpr int kKStep = kPPS * TcCfg<KV>::kPageBytes;  // K of one step
   static constexpr int kStageBytes = 2 * kKStep;               // K then V
   static constexpr int kOperand = 256 * kRp;                   // a Q slot
-  static constexpr int kPRows = KV == HPA_KV_E4M3 ? 2 * kRp : kRp;  // P^T rows (hi, lo)
-  static constexpr int kPBlk = kPRows * 128;                   // one 128-byte column block
-  static constexpr int kPBuf = kPBlk * (kStepKeys * (KV == HPA_KV_E4M3 ? 1 : 2) / 128);
+  // P^T is stored MN-major: one row of 2 Rp bytes per key (E4M3: the hi rows, then
+  // the lo rows; bf16: the rows), padded to a swizzle width of 32, 64 or 128 bytes.
+  // A compute thread owns one key, so it writes its probabilities with vector
+  // stores and no exchange between lanes.
+  static constexpr int kPSW = NC == 1 ? 32 : NC == 2 ? 64 : 128;  // bytes per key row
+  static constexpr int kPSwz = kPSW == 32 ? 6 : kPSW == 64 ? 4 : 2;  // descriptor mode
+  static constexpr int kPBuf = kStepKeys * kPSW;
   // as many stages as fit beside the operands (one CTA per SM): DRAM latency is
   // hidden by the bytes in flight
   static constexpr int kStages0 =
@@ -131,11 +135,14 @@ enum TcBar : int {
 
 // ---- tcgen05 wrappers ---------------------------------------------------------------
 // Shared-memory matrix descriptor (sm_100 family): start, leading and stride byte
-// offsets in 16-byte units, version 1, 128-byte swizzle.
-__device__ __forceinline__ uint64_t tc_desc(uint32_t addr, uint32_t lbo, uint32_t sbo) {
+// offsets in 16-byte units, version 1, swizzle mode (2 = 128-byte, 4 = 64-byte,
+// 6 = 32-byte).
+__device__ __forceinline__ uint64_t tc_desc(uint32_t addr, uint32_t lbo, uint32_t sbo,
+                                            uint32_t swz = 2) {
   return static_cast<uint64_t>((addr >> 4) & 0x3FFFu) |
          (static_cast<uint64_t>((lbo >> 4) & 0x3FFFu) << 16) |
-         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) | (2ull << 61);
+         (static_cast<uint64_t>((sbo >> 4) & 0x3FFFu) << 32) | (1ull << 46) |
+         (static_cast<uint64_t>(swz) << 61);
 }
 
 // Instruction descriptor: fp32 accumulate, M = 128, N = n; A/B formats (bf16 = 1 for
@@ -211,14 +218,28 @@ __device__ __forceinline__ uint16_t f16x2_to_e4m3x2(uint32_t v) {
   return r;
 }
 
-__device__ __forceinline__ void sts32(uint32_t addr, uint32_t v) {
-  asm volatile("st.shared.u32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+__device__ __forceinline__ void sts64(uint32_t addr, uint32_t a, uint32_t b) {
+  asm volatile("st.shared.v2.u32 [%0], {%1,%2};" ::"r"(addr), "r"(a), "r"(b) : "memory");
+}
+__device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, uint32_t c,
+                                       uint32_t d) {
+  asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" ::"r"(addr), "r"(a), "r"(b), "r"(c),
+               "r"(d)
+               : "memory");
 }
 
 __device__ __forceinline__ float warp_max(float x) {
   float r;
   asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
   return r;
+}
+
+// Byte offset of byte n of key k's row in an MN-major operand whose rows are one
+// swizzle width sw (32, 64 or 128 bytes) long, from a 1024-byte aligned base: the
+// 16-byte chunk index XOR address bits 7.. (as many bits as the row has chunks - 1).
+__device__ __forceinline__ uint32_t mnmaj(int k, int n, int sw) {
+  const uint32_t row = static_cast<uint32_t>(k) * sw;
+  return row + ((((n >> 4) ^ (row >> 7)) & (sw / 16 - 1)) << 4) + (n & 15);
 }
 
 // Byte offset of (row r, byte kb) in a K-major operand with 128-byte swizzle:
@@ -485,20 +506,22 @@ struct Tc {
         tc_fence_after();
         const uint32_t vbase = base + st * S::kStageBytes + S::kKStep;
         const uint32_t pbase = base + S::kP + b * S::kPBuf;
+        // A = V^T and B = P^T, both MN-major; B's stride between groups of 8 keys is
+        // 8 key rows
         if (KV == HPA_KV_BF16) {
-          const uint32_t idv = tc_idesc(1, kRp, 1, 0);
+          const uint32_t idv = tc_idesc(1, kRp, 1, 1);
 #pragma unroll
           for (int kk = 0; kk < 4 * S::kPPS; ++kk)  // 16 keys per MMA
             tc_mma<KV>(o_t, tc_desc(vbase + kk * 2048, S::kPPS * 8192, 1024),
-                       tc_desc(pbase + (kk >> 2) * S::kPBlk + (kk & 3) * 32, 16, 1024), idv,
+                       tc_desc(pbase + kk * 16 * S::kPSW, 16, 8 * S::kPSW, S::kPSwz), idv,
                        j > 0 || kk > 0);
         } else {
           // B = [P hi rows; P lo rows]: O hi in columns [0, Rp), lo in [Rp, 2 Rp)
-          const uint32_t idv = tc_idesc(0, 2 * kRp, 1, 0);
+          const uint32_t idv = tc_idesc(0, 2 * kRp, 1, 1);
 #pragma unroll
           for (int kk = 0; kk < 2 * S::kPPS; ++kk)  // 32 keys per MMA
             tc_mma<KV>(o_t, tc_desc(vbase + kk * 4096, 8192, 1024),
-                       tc_desc(pbase + (kk >> 2) * S::kPBlk + (kk & 3) * 32, 16, 1024), idv,
+                       tc_desc(pbase + kk * 32 * S::kPSW, 16, 8 * S::kPSW, S::kPSwz), idv,
                        j > 0 || kk > 0);
         }
         // Q K^T of this step completed before its P was written, so this commit
@@ -518,7 +541,6 @@ struct Tc {
   static __device__ void compute(const AttnParams &p, uint8_t *smem, int s_begin, int s_end,
                                  uint32_t tmem, int h) {
     constexpr int RH = S::kRH;  // rows per warp
-    constexpr int CW = S::kCW;
     constexpr int MT = S::kMT;
     const int t = threadIdx.x, w = t >> 5, lane = t & 31, qd = w & 3, hf = w >> 2;
     const int kt = t & 127, r0 = hf * RH;  // hf: this warp's group of rows
@@ -698,14 +720,16 @@ struct Tc {
           ok = false;
           break;
         }
-        // P^T rows go to shared memory as 32-bit words: lanes exchange values so that
-        // each thread holds consecutive keys of one row (quad byte transpose for
-        // E4M3, a pair swap for bf16)
+        // P^T goes to shared memory MN-major: this thread's key kk holds rows
+        // [r0, r0 + RH) at bytes [r0, r0 + RH) (E4M3 hi; lo at Rp + r0) or [2 r0, 2 r0 + 2 RH)
+        // (bf16) of its row
         const uint32_t pb = base + S::kP + b * S::kPBuf;
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
           const int kk = kt + 128 * m;  // key within the step
+          static_assert(RH == 16 || RH == 8, "rows per compute warp");
           if (KV == HPA_KV_BF16) {
+            uint32_t pw[RH / 2];  // rows (r0 + e, r0 + e + 1) in word e / 2
 #pragma unroll
             for (int e = 0; e < RH; e += 2) {
               const float b0 = mref[e] == -CUDART_INF_F ? 0.f : mref[e];
@@ -713,19 +737,14 @@ struct Tc {
               const float p0 = exp2f(x[m][e] - b0), p1 = exp2f(x[m][e + 1] - b1);
               lsum[e] += p0;
               lsum[e + 1] += p1;
-              const uint32_t a = pack_bf16(p0, p1);  // (row r, row r + 1) of key kk
-              const uint32_t o = __shfl_xor_sync(kFull, a, 1);
-              // even lane: row r, keys kk, kk + 1; odd lane: row r + 1, keys kk - 1, kk
-              const uint32_t wv = __byte_perm(a, o, (lane & 1) ? 0x3276u : 0x5410u);
-              sts32(pb + kmaj(r0 + e + (lane & 1), 2 * (kk & ~1), S::kPBlk), wv);
+              pw[e / 2] = pack_bf16(p0, p1);
             }
+#pragma unroll
+            for (int c = 0; c < RH / 8; ++c)
+              sts128(pb + mnmaj(kk, 2 * r0 + 16 * c, S::kPSW), pw[4 * c], pw[4 * c + 1],
+                     pw[4 * c + 2], pw[4 * c + 3]);
           } else {
-            const uint32_t sel1 = (lane & 1) ? 0x3715u : 0x6240u;
-            const uint32_t sel2 = (lane & 2) ? 0x3276u : 0x5410u;
-            auto quad_transpose = [&](uint32_t a) {  // byte e of lane q -> byte q of lane e
-              const uint32_t y = __byte_perm(a, __shfl_xor_sync(kFull, a, 1), sel1);
-              return __byte_perm(y, __shfl_xor_sync(kFull, y, 2), sel2);
-            };
+            uint32_t hw[RH / 4], lw[RH / 4];  // rows r0 + e4 .. r0 + e4 + 3 in word e4 / 4
 #pragma unroll
             for (int e4 = 0; e4 < RH; e4 += 4) {
               uint32_t hi = 0, lo = 0;
@@ -748,10 +767,15 @@ struct Tc {
                 hi |= static_cast<uint32_t>(h2) << (8 * e);
                 lo |= static_cast<uint32_t>(l2) << (8 * e);
               }
-              // lane q of each quad now writes row r0 + e4 + q for the quad's 4 keys
-              const int rr = r0 + e4 + (lane & 3);
-              sts32(pb + kmaj(rr, kk & ~3, S::kPBlk), quad_transpose(hi));
-              sts32(pb + kmaj(kRp + rr, kk & ~3, S::kPBlk), quad_transpose(lo));
+              hw[e4 / 4] = hi;
+              lw[e4 / 4] = lo;
+            }
+            if constexpr (RH == 16) {
+              sts128(pb + mnmaj(kk, r0, S::kPSW), hw[0], hw[1], hw[2], hw[3]);
+              sts128(pb + mnmaj(kk, kRp + r0, S::kPSW), lw[0], lw[1], lw[2], lw[3]);
+            } else {
+              sts64(pb + mnmaj(kk, r0, S::kPSW), hw[0], hw[1]);
+              sts64(pb + mnmaj(kk, kRp + r0, S::kPSW), lw[0], lw[1]);
             }
           }
           // V rows of keys past the request (or of a missing page) must be finite: zero them

@@ -39,8 +39,9 @@ def test_worked_example():
 
 
 @pytest.mark.parametrize("kv", ["bf16", "e4m3"])
-@pytest.mark.parametrize("q_len", [1, 2, 3, 4, 8])
+@pytest.mark.parametrize("q_len", [1, 2, 3, 4, 5, 6, 7, 8])
 def test_ragged_batch(kv, q_len):
+    """8 to 64 rows per KV head: every P^T row width (32, 64, 96 in 128, 128 bytes)."""
     lens = [q_len, 63, 64, 65, 128, 129, 511, 513, 1000, 3333, 4096 + 17]
     b = W.make_batch(lens, q_len=q_len, kv_dtype=kv, seed=200 + q_len)
     check(b, num_ctas=7)
