@@ -188,8 +188,8 @@ int hpa_decode_attn(const void *q_dev, const void *k_pool_dev, const void *v_poo
  * num_ctas x Hkv: one CTA covers all G * q_len query rows of its KV head
  * (up to 64) in a single pass over the keys, where hpa_decode_attn makes one
  * pass per group of 16 rows.  It pays for MTP with more than 16 rows per KV
- * head (on the E4M3 MTP workload at 64/8 heads: 1.3x at q_len 3-4, 1.55x
- * at q_len 6, 1.15x at q_len 8).  With up to 16 rows, or with many short
+ * head (on the E4M3 MTP workload at 64/8 heads: 1.4x at q_len 3-4, 1.85x
+ * at q_len 6, 1.37x at q_len 8).  With up to 16 rows, or with many short
  * segments per partition (hundreds of short requests), hpa_decode_attn is as
  * fast or faster.
  * Arguments, layouts, supported shapes, outputs and errors are exactly those
