@@ -11,7 +11,8 @@
 // Work per step = PPS pages (64 PPS keys) of one KV head, PPS = 4 for the 8-bit
 // path with up to 32 rows (TMEM allowing) and 2 otherwise; per 128-key tile:
 //   S^T[128 keys][rows]  = K[128 keys][128 dims] . Q^T          (tcgen05.mma, TMEM)
-//   P^T = 2^(S^T - m)    by the compute threads, one key each    (registers -> smem)
+//   P^T = 2^(S^T - m)    by the compute threads, one key each    (registers -> smem,
+//                        MN-major: each thread stores its key's row with 16-byte stores)
 //   O^T[128 dims][rows] += V^T[128 dims][64 PPS keys] . P^T      (tcgen05.mma, TMEM)
 // Keys sit on the TMEM lanes for the softmax, so all compute warps share it;
 // output dims sit on the lanes for O, so each compute thread owns one dim at
@@ -32,8 +33,9 @@
 // Roles: CW = 8, 12 or 16 compute warps (softmax, epilogue; the warps with
 // w % 4 equal share TMEM lane quarter w % 4 -- the same keys, and the same
 // output dims -- and split the query rows, at most 16 rows each), then one TMA
-// producer warp, one warp whose thread issues Q K^T and one issuing P V.  A tcgen05.mma costs its issuing
-// thread about 100 cycles whatever N is, so the two products are issued from
+// producer warp, one warp whose thread issues Q K^T and one issuing P V.  A
+// tcgen05.mma costs its issuing thread about 100 cycles whatever N is, so the
+// two products are issued from
 // two threads and each step issues few, wide MMAs.  S is double-buffered in
 // TMEM so Q K^T of step i+1 overlaps the softmax of step i.  Every wait is
 // bounded in time; a role that gives up flags the task map's status word and
