@@ -38,13 +38,14 @@ METRIC = "mixed-length decode attention: µs/batch, KV-read HBM GB/s and % of pe
 UNIT = "us/batch"
 
 # DRAM traffic of one decode_attn_kernel launch from an ncu capture, valid only
-# for the kernel source it was taken on (sha256 of decode_attn.cu); else null.
-# Taken on the uniform 32 x 8192 batch (1.07 GB KV; the mixed batch is too large to capture
-# with every section) and scaled by KV bytes, since traffic grows with the KV read.
+# for the kernel source it was taken on (sha256 of decode_attn.cu) and for the
+# workload it was taken on; else null.  Expressed per algorithmic KV byte and
+# scaled to the full batch, since traffic grows with the KV read.
 TRAFFIC_PROFILE = {
-    "source_sha256": "80760069db5fb18d6dc788cf74cb81e5f46581dccee0b0709cb6c10db7c142ea",
-    "bytes_per_kv_byte": (1074352384 + 3225856) / 1073741824,
-    "workload": "uniform_32x8k_paged (profiles/decode_attn_uniform_32x8k_bf16_full.md)",
+    "config": 3,
+    "source_sha256": "67e86ff851789597537dc8fc07e83fbc9e8a369d6e98cd1044fef4e76cc1ff91",
+    "bytes_per_kv_byte": (2574309376 + 3269120) / 2572926976,
+    "workload": "mixed_45req_1k_128k_paged, first 12 requests (2.57 GB KV)",
 }
 
 
@@ -158,7 +159,11 @@ def run_ours(args, rank, world, local_rank):
         b.tile = args.tile
     kv = hpa.KV_BF16 if b.kv_dtype == "bf16" else hpa.KV_E4M3
     tc = args.attn == "tc"
-    default_c = hpa.hpa_default_num_ctas_tc if tc else hpa.hpa_default_num_ctas
+    allh = args.attn == "allheads"
+    mma = args.attn == "mma"
+    default_c = (hpa.hpa_default_num_ctas_tc if tc else
+                 hpa.hpa_default_num_ctas_allheads if allh else
+                 hpa.hpa_default_num_ctas_mma if mma else hpa.hpa_default_num_ctas)
     C = args.num_ctas or b.num_ctas or default_c(b.Hkv, b.q_len, kv, b.Hq)
     groups = (b.Hq // b.Hkv * b.q_len + 15) // 16  # query-row groups per (partition, head)
     q = b.q.to(dev)
@@ -182,8 +187,12 @@ def run_ours(args, rank, world, local_rank):
         w.plan(lens, b.tile, stream)
         if ev is not None:
             ev[1].record(stream)
-        hpa.hpa_decode_attn(q, k, v, indptr, indices, w.taskmap, w.num_ctas, w.partial_o,
-                            w.partial_lse, ks, vs, stream=stream, tc=tc)
+        if allh:
+            hpa.hpa_decode_attn_allheads(q, k, v, indptr, indices, w.taskmap, w.num_ctas,
+                                         w.partial_o, w.partial_lse, ks, vs, stream=stream)
+        else:
+            hpa.hpa_decode_attn(q, k, v, indptr, indices, w.taskmap, w.num_ctas, w.partial_o,
+                                w.partial_lse, ks, vs, stream=stream, tc=tc, mma=mma)
         if ev is not None:
             ev[2].record(stream)
         hpa.hpa_combine(w.partial_o, w.partial_lse, w.taskmap, w.num_ctas, out, out_lse, stream)
@@ -238,14 +247,20 @@ def run_ours(args, rank, world, local_rank):
         """Per-CTA timestamps of the attention kernel (outside the timed region)."""
         if tc:
             return None  # the tcgen05 kernel has no traced variant
-        tr = torch.zeros(4 * w.num_ctas * b.Hkv * groups, dtype=torch.int64, device=dev)
+        heads_axis = 1 if allh else b.Hkv  # CTAs per partition and row group
+        tr = torch.zeros(4 * w.num_ctas * heads_axis * groups, dtype=torch.int64, device=dev)
         out_t = None
         for _ in range(reps):
             w.plan(lens, b.tile, stream)
-            hpa.hpa_decode_attn_traced(q, k, v, indptr, indices, w.taskmap, w.num_ctas,
-                                       w.partial_o, w.partial_lse, tr, ks, vs, stream=stream)
+            if allh:
+                hpa.hpa_decode_attn_allheads(q, k, v, indptr, indices, w.taskmap, w.num_ctas,
+                                             w.partial_o, w.partial_lse, ks, vs, trace=tr,
+                                             stream=stream)
+            else:
+                hpa.hpa_decode_attn_traced(q, k, v, indptr, indices, w.taskmap, w.num_ctas,
+                                           w.partial_o, w.partial_lse, tr, ks, vs, stream=stream)
             torch.cuda.synchronize(dev)
-            out_t = hpa.trace_summary(tr, w.num_ctas, b.Hkv, groups)
+            out_t = hpa.trace_summary(tr, w.num_ctas, heads_axis, groups)
         return {k2: round(v2, 3) if isinstance(v2, float) else v2 for k2, v2 in out_t.items()}
 
     tail = traced_tail(ws)
@@ -255,7 +270,7 @@ def run_ours(args, rank, world, local_rank):
         hpa.decode_step(ws, q, k, v, lens, indptr, indices, out, out_lse, ks, vs, tile=b.tile,
                         stream=stream, fused=True)
 
-    fused_ms = None if tc else max_over_ranks(
+    fused_ms = None if (tc or allh) else max_over_ranks(
         timed(fused_step, args.steps, args.warmup, breakdown=False)[0], world, dev)
 
     # static split-KV comparators through the same kernels (heuristic and best of a sweep)
@@ -314,7 +329,7 @@ def run_ours(args, rank, world, local_rank):
         with torch.cuda.stream(stream):
             in_d.copy_(in_h, non_blocking=True)
         hpa.decode_step(ws, q_e, k, v, lens_e, indptr_e, indices_e, out_e, lse_e, ks, vs,
-                        tile=b.tile, stream=stream, tc=tc)
+                        tile=b.tile, stream=stream, tc=tc, allheads=allh, mma=mma)
         with torch.cuda.stream(stream):
             out_h.copy_(out_d, non_blocking=True)
         if ev is not None:
@@ -440,9 +455,11 @@ def main():
                     help="tile budgets (the pages' method) or the token-weighted variant")
     ap.add_argument("--num-ctas", type=int, default=None,
                     help="partitions per KV head (default: the device default)")
-    ap.add_argument("--attn", default="mma", choices=["mma", "tc"],
-                    help="attention kernel: mma.sync (hpa_decode_attn) or tcgen05 "
-                         "(hpa_decode_attn_tc)")
+    ap.add_argument("--attn", default="auto", choices=["auto", "mma", "tc", "allheads"],
+                    help="attention kernel: hpa_decode_attn's own choice by query rows per KV "
+                         "head (auto), mma.sync (hpa_decode_attn_mma), tcgen05 "
+                         "(hpa_decode_attn_tc), or mma.sync with every KV head inside the CTA "
+                         "(hpa_decode_attn_allheads)")
     ap.add_argument("--no-static", action="store_true", help="skip the static comparators")
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-feeder", action="store_true", help="skip the KV-store feeder timing")
@@ -473,7 +490,11 @@ def main():
     achieved = kv_bytes / (attn_ms * 1e-3) / 1e9
     us_batch = per_batch_us(r["ms"], world)
     traffic = None
-    if (args.attn == "mma" and TRAFFIC_PROFILE["source_sha256"] == kernel_sha()
+    rows = b.Hq // b.Hkv * b.q_len
+    on_tc = args.attn == "tc" or (args.attn == "auto" and rows > 16)
+    kernel_name = "decode_attn_tc_kernel" if on_tc else "decode_attn_kernel"
+    if (args.attn in ("auto", "mma") and not on_tc and args.config == TRAFFIC_PROFILE["config"]
+            and TRAFFIC_PROFILE["source_sha256"] == kernel_sha()
             and TRAFFIC_PROFILE["bytes_per_kv_byte"]):
         traffic = int(TRAFFIC_PROFILE["bytes_per_kv_byte"] * kv_bytes)
     cpu = None
@@ -492,7 +513,8 @@ def main():
                    "kv_tokens": int(b.seq_lens.sum()), "q_len": b.q_len, "heads": "64q/8kv",
                    "head_dim": 128, "page": 64, "tile": b.tile, "num_ctas": int(r["C"]),
                    "kv_dtype": b.kv_dtype, "kv_bytes": int(kv_bytes), "plan": args.plan,
-                   "attention_kernel": "tcgen05" if args.attn == "tc" else "mma.sync",
+                   "attention_kernel": ("mma.sync, all KV heads per CTA" if args.attn == "allheads"
+                                        else "tcgen05" if on_tc else "mma.sync"),
                    "l2": "inputs larger than L2 (%.2f GB KV), no flush" % (kv_bytes / 1e9),
                    "parallelism": "dp%d replicas" % world, "seed": args.seed},
         "kv_gbs": round(kv_bytes / (r["ms"] * 1e-3) / 1e9, 1),
@@ -502,7 +524,7 @@ def main():
                          "combine": round(statistics.mean(r["comb"]) * 1e3, 2)},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
-                     "kernel": "decode_attn_kernel" if args.attn == "mma" else "decode_attn_tc_kernel",
+                     "kernel": kernel_name,
                      "peak_kind": peak_kind + " (hbm_gbs)"},
         "step_us_distribution": step_distribution(r["step_ms"]),
         "tail": r["tail"],

@@ -31,11 +31,14 @@
  * Error behaviour: every call validates its host-visible arguments first and
  * returns a negative HPA_ERR_* code without launching anything when one is
  * wrong.  Problems only the device can see (sequence lengths, page ids, a
- * task map built for another shape, a pipeline wait that ran past its time
- * bound) set bits in the task map's status word (int32 word 6 of the map,
- * HPA_STATUS_*); the attention kernel then does no work and the combine
- * kernel writes NaN to every output element, so a bad step cannot pass
- * silently.  Asynchronous CUDA faults surface at the caller's next sync.
+ * task map built for another shape or corrupted after it was built, a
+ * pipeline wait that ran past its time bound) set bits in the task map's
+ * status word (int32 word 6 of the map, HPA_STATUS_*); the attention kernel
+ * then does no work for what it cannot trust and the combine kernel writes
+ * NaN to every output element, so a bad step cannot pass silently.  The
+ * kernels check every index they take from the map before following it, so
+ * a corrupted map is reported rather than read or written out of bounds.
+ * Asynchronous CUDA faults surface at the caller's next sync.
  */
 #ifndef HPA_H
 #define HPA_H
@@ -65,6 +68,9 @@ typedef struct CUstream_st *hpa_stream_t;
 #define HPA_STATUS_BAD_PAGE 4   /* a page id outside [0, num_pages); page 0 was read instead */
 #define HPA_STATUS_TIMEOUT 8    /* a shared-memory pipeline wait exceeded ~2 s; CTA gave up */
 #define HPA_STATUS_OVERFLOW 16  /* total tile count does not fit int32 */
+#define HPA_STATUS_BAD_MAP 32   /* a malformed map: a partition's segment range, a segment row
+                                   (request, owner, tile range) or a request's segment range
+                                   out of bounds; the row was skipped, never followed */
 
 /* ---- KV element types ---- */
 #define HPA_KV_BF16 0 /* bfloat16 */
@@ -100,11 +106,16 @@ int32_t hpa_max_segments(int32_t B, int32_t num_ctas);
 int32_t hpa_static_num_ctas(int32_t B, int32_t splits);
 size_t hpa_static_taskmap_bytes(int32_t B, int32_t splits);
 
-/* Partitions per KV head that fill the current device once: SMs x resident
- * attention CTAs per SM / (Hkv x query-row groups), at least 1, where a group
- * is 16 of the G * q_len query rows of a KV head.  Returns <= 0 on a CUDA
- * error or unsupported arguments. */
+/* Partitions per KV head that fill the current device once with the kernel
+ * hpa_decode_attn picks for this shape: hpa_default_num_ctas_mma up to 16
+ * query rows per KV head (G * q_len), hpa_default_num_ctas_tc above.  Returns
+ * <= 0 on a CUDA error or unsupported arguments. */
 int32_t hpa_default_num_ctas(int32_t Hq, int32_t Hkv, int32_t q_len, int32_t kv_dtype);
+
+/* Partitions per KV head for hpa_decode_attn_mma: SMs x resident CTAs per SM /
+ * (Hkv x query-row groups), at least 1, where a group is 16 of the G * q_len
+ * query rows of a KV head. */
+int32_t hpa_default_num_ctas_mma(int32_t Hq, int32_t Hkv, int32_t q_len, int32_t kv_dtype);
 
 /*
  * hpa_plan -- the Task Assign step ([Notes §3.1] steps 1-4, [HPC-Ops §二.1],
@@ -149,6 +160,14 @@ int hpa_plan_static(const int32_t *seq_lens_dev, int32_t B, int32_t tile, int32_
 
 /*
  * hpa_decode_attn -- the split-KV attention kernel ([Notes §3.1] steps 4-5).
+ * Up to 16 query rows per KV head (G * q_len <= 16: one new token at any
+ * GQA ratio up to 16, or two at 8 heads per KV head) it runs the kernel
+ * described here, which is the one that streams the KV at the copy peak
+ * there; above 16 rows (MTP with several draft tokens) it runs the same step
+ * as hpa_decode_attn_tc, which takes all rows in one pass.  Size num_ctas with
+ * hpa_default_num_ctas, which follows the same choice.  hpa_decode_attn_mma
+ * runs the kernel described here at any row count.
+ *
  * Grid num_ctas x Hkv x ceil(G q_len / 16); the CTA of (partition c, KV
  * head h, row group z) walks c's segments in order and, for each, computes
  * over the segment's keys
@@ -163,6 +182,10 @@ int hpa_plan_static(const int32_t *seq_lens_dev, int32_t B, int32_t tile, int32_
  * k_pool_dev, v_pool_dev: [num_pages][Hkv][page_size][d] of bf16 or E4M3
  *               bytes, 16-byte aligned (read with TMA tensor copies).
  * k_scale_dev, v_scale_dev: fp32 [Hkv] for HPA_KV_E4M3, ignored for bf16.
+ *               With E4M3 pages the products run in f16: each query row is
+ *               scaled by a power of two that puts its largest |element| in
+ *               [2^14, 2^15) (taken back out of the scores), so any finite bf16
+ *               query converts exactly, down to 2^-28 of its row's largest.
  * page_indptr_dev: int32 [B+1]; page_indices_dev: int32; key i of request r
  *               is slot i % page_size of page page_indices[page_indptr[r] + i / page_size].
  * Supported: d == 128, page_size == 64, Hq % Hkv == 0, (Hq / Hkv) * q_len <= 64,
@@ -180,6 +203,13 @@ int hpa_decode_attn(const void *q_dev, const void *k_pool_dev, const void *v_poo
                     int32_t q_len, int32_t Hq, int32_t Hkv, int32_t d, float sm_scale,
                     void *taskmap_dev, int32_t num_ctas, float *partial_o_dev,
                     float *partial_lse_dev, hpa_stream_t stream);
+int hpa_decode_attn_mma(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
+                        int32_t kv_dtype, const float *k_scale_dev, const float *v_scale_dev,
+                        int64_t num_pages, const int32_t *page_indptr_dev,
+                        const int32_t *page_indices_dev, int32_t page_size, int32_t B,
+                        int32_t q_len, int32_t Hq, int32_t Hkv, int32_t d, float sm_scale,
+                        void *taskmap_dev, int32_t num_ctas, float *partial_o_dev,
+                        float *partial_lse_dev, hpa_stream_t stream);
 
 /*
  * hpa_decode_attn_tc -- the same split-KV attention step ([Notes §3.1] steps
@@ -195,7 +225,12 @@ int hpa_decode_attn(const void *q_dev, const void *k_pool_dev, const void *v_poo
  * Arguments, layouts, supported shapes, outputs and errors are exactly those
  * of hpa_decode_attn; the partials feed hpa_combine unchanged.  E4M3 pages
  * enter the MMA as 8-bit operands; the query rows and the probabilities are
- * each carried as two E4M3 terms (about 8 significant bits, as bf16).
+ * each carried as two E4M3 terms (about 8 significant bits, as bf16).  Each
+ * query row is scaled by a power of two and the residual term by another, so
+ * rows of any bf16 magnitude are carried exactly as long as their elements
+ * lie within about 2^-14 of the row's largest; smaller elements lose bits and
+ * those below about 2^-21 of it are dropped (hpa_decode_attn keeps bf16
+ * precision down to 2^-28).
  */
 int hpa_decode_attn_tc(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
                        int32_t kv_dtype, const float *k_scale_dev, const float *v_scale_dev,
@@ -226,6 +261,29 @@ int hpa_decode_attn_traced(const void *q_dev, const void *k_pool_dev, const void
                            int32_t q_len, int32_t Hq, int32_t Hkv, int32_t d, float sm_scale,
                            void *taskmap_dev, int32_t num_ctas, float *partial_o_dev,
                            float *partial_lse_dev, uint64_t *trace_dev, hpa_stream_t stream);
+
+/*
+ * hpa_decode_attn_allheads -- hpa_decode_attn with the KV heads inside the CTA
+ * instead of on a grid axis (the pages do not say how heads map to CTAs,
+ * "Hy3 Preview AI Infra 推理优化精读笔记" §3.1 方案 step 3; this is the other
+ * reading, kept as an A/B).  Grid num_ctas x 1 x row groups: the CTA of
+ * partition c walks c's segments and, for each, every KV head in turn
+ * (heads innermost), so num_ctas counts partitions of the tile stream for the
+ * whole grid (hpa_default_num_ctas_allheads: SMs x resident CTAs per SM /
+ * row groups) and the task map must be planned with that count.  Arguments,
+ * layouts, partials and errors are those of hpa_decode_attn; trace_dev is
+ * NULL or, as for hpa_decode_attn_traced, 4 uint64 words per CTA at
+ * trace_dev[4 * (z * num_ctas + c)].
+ */
+int hpa_decode_attn_allheads(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
+                             int32_t kv_dtype, const float *k_scale_dev,
+                             const float *v_scale_dev, int64_t num_pages,
+                             const int32_t *page_indptr_dev, const int32_t *page_indices_dev,
+                             int32_t page_size, int32_t B, int32_t q_len, int32_t Hq,
+                             int32_t Hkv, int32_t d, float sm_scale, void *taskmap_dev,
+                             int32_t num_ctas, float *partial_o_dev, float *partial_lse_dev,
+                             uint64_t *trace_dev, hpa_stream_t stream);
+int32_t hpa_default_num_ctas_allheads(int32_t Hq, int32_t Hkv, int32_t q_len, int32_t kv_dtype);
 
 /*
  * hpa_decode_attn_fused -- hpa_decode_attn with the combine folded in (one
@@ -326,11 +384,15 @@ int hpa_selftest_wait_timeout(int32_t *status_dev, int64_t limit_ns, hpa_stream_
  *
  * The first call on a device resolves the array's device address with that
  * device current (cudaGetSymbolAddress, which may load the module); make that
- * first call before any stream capture.  All calls share the one array and
- * it keeps the last call's contents: nothing in it needs to start at zero
- * (each call writes every partial it reads), but calls that overlap on the
- * GPU -- on different streams, or from several host threads -- race on it
- * and must be serialised by the caller.
+ * first call before any stream capture.  The address belongs to the CUDA
+ * context that was current, so it is cached per context (keyed by the
+ * context's process-unique id): a call under another context of the same
+ * device, or after cudaDeviceReset, repeats that set-up once for the new
+ * context and should likewise come before any capture there.  All calls
+ * share the one array and it keeps the last call's contents: nothing in it
+ * needs to start at zero (each call writes every partial it reads), but
+ * calls that overlap on the GPU -- on different streams, or from several
+ * host threads -- race on it and must be serialised by the caller.
  */
 #define HPA_NOALLOC_SCRATCH_BYTES (16u << 20)
 int hpa_decode_attn_combine_noalloc(const void *q_dev, const void *k_pool_dev,

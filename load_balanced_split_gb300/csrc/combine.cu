@@ -9,7 +9,8 @@
 // The four warps take every fourth segment (lane i owns head dims [4i, 4i+4))
 // with several loads in flight per warp, so a request split over many
 // partitions costs a few round trips, not one per segment.  A task map whose
-// status word is non-zero makes every output NaN.
+// status word is non-zero makes every output NaN, and so does a request whose
+// segment range in the map is out of bounds (reported as HPA_STATUS_BAD_MAP).
 #include <math_constants.h>
 
 #include "hpa_internal.cuh"
@@ -22,7 +23,7 @@ constexpr int kUnroll = 4;
 
 __global__ void __launch_bounds__(kWarps * 32)
     combine_kernel(const float *__restrict__ po, const float *__restrict__ plse,
-                   const int32_t *__restrict__ tm, int B, int C, int q_len, int Hq,
+                   int32_t *__restrict__ tm, int B, int C, int q_len, int Hq,
                    __nv_bfloat16 *__restrict__ out, float *__restrict__ out_lse) {
   pdl_wait();  // partials come from the attention kernel just before
   const int lane = threadIdx.x & 31, w = threadIdx.x >> 5;
@@ -34,7 +35,17 @@ __global__ void __launch_bounds__(kWarps * 32)
   __shared__ float4 s_acc[kWarps][32];
 
   const TaskMapLayout lay = TaskMapLayout::make(B, C);
-  if (tm[TM_STATUS] != 0 || tm[TM_B] != B || tm[TM_C] != C) {
+  int s0 = 0, s1 = 0;
+  bool good = tm[TM_STATUS] == 0 && tm[TM_B] == B && tm[TM_C] == C;
+  if (good) {
+    // r's segment range, checked before any partial is read through it
+    s0 = tm[lay.seg_off + r];
+    s1 = tm[lay.seg_off + r + 1];
+    const int S = tm[TM_S];
+    good = s0 >= 0 && s0 < s1 && s1 <= S && S <= B + C - 1;
+    if (!good && threadIdx.x == 0) status_or(tm, HPA_STATUS_BAD_MAP);
+  }
+  if (!good) {
     if (w == 0) {
       const float nan = CUDART_NAN_F;
       const __nv_bfloat162 n2 = __floats2bfloat162_rn(nan, nan);
@@ -45,7 +56,6 @@ __global__ void __launch_bounds__(kWarps * 32)
     }
     return;
   }
-  const int s0 = tm[lay.seg_off + r], s1 = tm[lay.seg_off + r + 1];
 
   float m = -CUDART_INF_F;
   for (int s = s0 + threadIdx.x; s < s1; s += kWarps * 32) m = fmaxf(m, plse[s * per_req + jg]);
@@ -123,8 +133,8 @@ cudaError_t launch_combine(const float *po, const float *plse, int32_t *tm, int 
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, combine_kernel, po, static_cast<const float *>(plse),
-                            static_cast<const int32_t *>(tm), B, C, q_len, Hq, out, out_lse);
+  return cudaLaunchKernelEx(&cfg, combine_kernel, po, static_cast<const float *>(plse), tm, B,
+                            C, q_len, Hq, out, out_lse);
 }
 
 }  // namespace hpa

@@ -100,22 +100,24 @@ struct SegInfo {
   int r, L, klo, khi, pg0, pg1;
 };
 
-__device__ __forceinline__ SegInfo seg_info(const AttnParams &p, int s, int tile) {
-  const int4 sg = reinterpret_cast<const int4 *>(p.tm + p.lay.segs)[s];
+// Segment s of partition c, checked (a malformed row reads as an empty segment).
+__device__ __forceinline__ SegInfo seg_info(const AttnParams &p, int s, int tile, int c,
+                                            bool report) {
+  const SegRow sr = read_seg_row(p.tm, p.lay, p.B, s, c, tile, report);
   SegInfo f;
-  f.r = sg.x;
-  f.L = p.tm[p.lay.lens + sg.x];
-  f.klo = sg.y * tile;
-  f.khi = min(sg.z * tile, f.L);
+  f.r = sr.r;
+  f.L = sr.L;
+  f.klo = sr.klo;
+  f.khi = sr.khi;
   f.pg0 = f.klo / PAGE;
   f.pg1 = (f.khi + PAGE - 1) / PAGE;
   return f;
 }
 
 // ----------------------------------------------------------------------------- producer
-template <int KV, bool FUSED>
+template <int KV, bool FUSED, bool ALLH>
 __device__ void producer(const AttnParams &p, const CUtensorMap *tmk, const CUtensorMap *tmv,
-                         uint8_t *smem, int s_begin, int s_end, int tile, int h) {
+                         uint8_t *smem, int s_begin, int s_end, int tile, int h0) {
   using S = Smem<KV>;
   const int lane = threadIdx.x & 31;
   const uint32_t base = smem_u32(smem);
@@ -131,11 +133,15 @@ __device__ void producer(const AttnParams &p, const CUtensorMap *tmk, const CUte
   int stage = 0;
   uint32_t phase = 0, issued = 0, parity_bits = 0;
   bool ok = true;
-  for (int s = s_begin; s < s_end && ok; ++s) {
-    const SegInfo f = seg_info(p, s, tile);
-    // stage the segment's info and query rows for the consumers
+  // work items: (segment, KV head), heads innermost; one head per CTA on the
+  // per-head grid, all of them with heads_per_cta == Hkv
+  const int hpc = ALLH ? p.heads_per_cta : 1, n_items = (s_end - s_begin) * hpc;
+  for (int k = 0; k < n_items && ok; ++k) {
+    const int s = s_begin + k / hpc, h = h0 + k % hpc;
+    const SegInfo f = seg_info(p, s, tile, blockIdx.x, lane == 0 && h == h0);
+    // stage the item's segment info and query rows for the consumers
     {
-      const int k = s - s_begin, slot = k & 1;
+      const int slot = k & 1;
       const uint32_t qphase = (k >> 1) & 1;
       int good = 1;
       if (lane == 0) good = !*abort_flag && mbar_wait_bounded(qempty0 + 8 * slot, qphase ^ 1);
@@ -154,9 +160,11 @@ __device__ void producer(const AttnParams &p, const CUtensorMap *tmk, const CUte
       if (lane == 0) {
         int4 *info = reinterpret_cast<int4 *>(smem + S::kInfo) + 2 * slot;
         info[0] = make_int4(f.r, f.L, f.klo, f.khi);
-        if (FUSED) {  // fused combine: the request's segment range
-          const int so = p.tm[p.lay.seg_off + f.r];
-          info[1] = make_int4(so, p.tm[p.lay.seg_off + f.r + 1] - so, 0, 0);
+        if (FUSED) {  // fused combine: the request's segment range, which must hold s
+          const int so = p.tm[p.lay.seg_off + f.r], so1 = p.tm[p.lay.seg_off + f.r + 1];
+          const bool good_range = so >= 0 && so <= s && s < so1 && so1 <= p.B + p.C - 1;
+          if (!good_range) status_or(p.tm, HPA_STATUS_BAD_MAP);  // no merge for it
+          info[1] = make_int4(good_range ? so : 0, good_range ? so1 - so : 0, 0, 0);
         }
       }
       mbar_arrive(qfull0 + 8 * slot);  // every lane publishes its own stores
@@ -218,6 +226,22 @@ __device__ void producer(const AttnParams &p, const CUtensorMap *tmk, const CUte
 }
 
 // ----------------------------------------------------------------------------- consumer helpers
+// Largest |x| of four consecutive bf16 values (8-byte aligned).
+__device__ __forceinline__ float absmax4_bf16(const __nv_bfloat16 *x) {
+  const uint2 raw = *reinterpret_cast<const uint2 *>(x);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
+  return fmaxf(fmaxf(fabsf(a.x), fabsf(a.y)), fmaxf(fabsf(b.x), fabsf(b.y)));
+}
+
+// e such that amax * 2^e lies in [2^14, 2^15) (0 for a zero row), clamped so that
+// both 2^e and 2^-e are fp32 normals.
+__device__ __forceinline__ int f16_row_exponent(float amax) {
+  if (!(amax > 0.f)) return 0;
+  const int ea = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127;  // floor(log2)
+  return 14 - min(max(ea, -112), 126);
+}
+
 // Zero the V rows (keys >= L) this warp reads from a page that ends past L.
 template <int KV>
 __device__ __forceinline__ void zero_tail_rows(uint8_t *vtile, int w, int wk, int L, int lane) {
@@ -379,9 +403,9 @@ __device__ void merge_request(const AttnParams &p, int r, int h, int seg_first, 
 }
 
 // ----------------------------------------------------------------------------- consumer
-template <int KV, bool FUSED>
+template <int KV, bool FUSED, bool ALLH>
 __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_end, int tile,
-                         int h) {
+                         int h0) {
   using S = Smem<KV>;
   const int w = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r8 = lane >> 2, qd = lane & 3;
@@ -392,11 +416,6 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
   float *sm_l = sm_m + kConsumerWarps * MAX_ROWS;
   volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kFlag);
 
-  float sl2 = p.scale_log2, vsc = 1.f;
-  if (KV == HPA_KV_E4M3) {
-    sl2 *= p.k_scale[h];
-    vsc = p.v_scale[h];
-  }
   // rows of this CTA's group: local index row, global query row rb + row
   const int G = p.G, rows = group_rows(p), q_len = p.q_len, rb = row_base();
   const int row0 = r8, row1 = r8 + 8;
@@ -406,8 +425,20 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
   const uint32_t qfull0 = empty0 + 8 * S::kStages, qempty0 = qfull0 + 16;
   int stage = 0;
   uint32_t phase = 0;
-  for (int s = s_begin; s < s_end; ++s) {
-    const int k = s - s_begin, slot = k & 1;
+  // score and output scales of the KV head (loaded once on the per-head grid)
+  float sl2_h = p.scale_log2, vsc_h = 1.f;
+  if (!ALLH && KV == HPA_KV_E4M3) {
+    sl2_h *= p.k_scale[h0];
+    vsc_h = p.v_scale[h0];
+  }
+  const int hpc = ALLH ? p.heads_per_cta : 1, n_items = (s_end - s_begin) * hpc;
+  for (int k = 0; k < n_items; ++k) {
+    const int s = s_begin + k / hpc, h = h0 + k % hpc, slot = k & 1;
+    float sl2 = sl2_h, vsc = vsc_h;
+    if (ALLH && KV == HPA_KV_E4M3) {
+      sl2 *= p.k_scale[h];
+      vsc = p.v_scale[h];
+    }
     bool ok = !*abort_flag && mbar_wait_bounded(qfull0 + 8 * slot, (k >> 1) & 1);
     ok = __all_sync(kFull, ok);
     SegInfo f;
@@ -434,10 +465,36 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
 
     // query fragments (A operand, 16 rows x 128) from the staged rows
     uint32_t qa[8][4];
+    // per-row score factors: sm_scale * log2 e (* k scale), times 2^-e_row on the E4M3 path
+    float sl2_0 = sl2, sl2_1 = sl2;
     {
       const uint8_t *qs = smem + S::kQ + slot * kQSlotBytes;
       const __nv_bfloat16 *q0 = reinterpret_cast<const __nv_bfloat16 *>(qs + row0 * kQRowBytes);
       const __nv_bfloat16 *q1 = reinterpret_cast<const __nv_bfloat16 *>(qs + row1 * kQRowBytes);
+      // E4M3 path: the query enters f16 MMAs.  Each row is scaled by 2^e_row so that its
+      // largest |element| lands in [2^14, 2^15): a bf16 value that large or small (up to
+      // ~3e38 or down to bf16's subnormals) cannot overflow f16 or lose bits to f16
+      // subnormals, since every element within 2^-28 of the row maximum stays an f16
+      // normal and converts exactly.  The factor is taken back out of the scores.
+      float qsc0 = 1.f, qsc1 = 1.f;
+      if (KV == HPA_KV_E4M3) {
+        float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+        for (int ks = 0; ks < 8; ++ks) {  // this thread's 32 dims of each row
+          const int d0 = 32 * qd + 4 * ks;
+          if (v0) a0 = fmaxf(a0, absmax4_bf16(q0 + d0));
+          if (v1) a1 = fmaxf(a1, absmax4_bf16(q1 + d0));
+        }
+        a0 = fmaxf(a0, __shfl_xor_sync(kFull, a0, 1));  // the 4 threads of a row (qd)
+        a0 = fmaxf(a0, __shfl_xor_sync(kFull, a0, 2));
+        a1 = fmaxf(a1, __shfl_xor_sync(kFull, a1, 1));
+        a1 = fmaxf(a1, __shfl_xor_sync(kFull, a1, 2));
+        const int e0 = f16_row_exponent(a0), e1 = f16_row_exponent(a1);
+        qsc0 = exp2i(e0);
+        qsc1 = exp2i(e1);
+        sl2_0 = sl2 * exp2i(-e0);
+        sl2_1 = sl2 * exp2i(-e1);
+      }
 #pragma unroll
       for (int ks = 0; ks < 8; ++ks) {
         if (KV == HPA_KV_BF16) {
@@ -448,14 +505,14 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
           qa[ks][3] = v1 ? *reinterpret_cast<const uint32_t *>(q1 + d0 + 8) : 0u;
         } else {
           const int d0 = 32 * qd + 4 * ks;
-          auto h2 = [](const __nv_bfloat16 *x) {
+          auto h2 = [](const __nv_bfloat16 *x, float sc) {
             const float2 t = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(x));
-            return pack_f16(t.x, t.y);
+            return pack_f16(t.x * sc, t.y * sc);
           };
-          qa[ks][0] = v0 ? h2(q0 + d0) : 0u;
-          qa[ks][1] = v1 ? h2(q1 + d0) : 0u;
-          qa[ks][2] = v0 ? h2(q0 + d0 + 2) : 0u;
-          qa[ks][3] = v1 ? h2(q1 + d0 + 2) : 0u;
+          qa[ks][0] = v0 ? h2(q0 + d0, qsc0) : 0u;
+          qa[ks][1] = v1 ? h2(q1 + d0, qsc1) : 0u;
+          qa[ks][2] = v0 ? h2(q0 + d0 + 2, qsc0) : 0u;
+          qa[ks][3] = v1 ? h2(q1 + d0 + 2, qsc1) : 0u;
         }
       }
     }
@@ -489,7 +546,7 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
 #pragma unroll
       for (int nt = 0; nt < 2; ++nt)
 #pragma unroll
-        for (int e = 0; e < 4; ++e) sc[nt][e] *= sl2;
+        for (int e = 0; e < 4; ++e) sc[nt][e] *= e < 2 ? sl2_0 : sl2_1;
       if (wk + 16 > lim_min) {
 #pragma unroll
         for (int nt = 0; nt < 2; ++nt)
@@ -697,7 +754,7 @@ __device__ void consumer(const AttnParams &p, uint8_t *smem, int s_begin, int s_
 }
 
 // ----------------------------------------------------------------------------- kernel
-template <int KV, bool FUSED>
+template <int KV, bool FUSED, bool ALLH>
 __global__ void __launch_bounds__(kThreads, 2)
     decode_attn_kernel(const __grid_constant__ CUtensorMap tmk,
                        const __grid_constant__ CUtensorMap tmv, const AttnParams p) {
@@ -705,11 +762,11 @@ __global__ void __launch_bounds__(kThreads, 2)
   extern __shared__ uint8_t smem_raw[];
   uint8_t *smem = reinterpret_cast<uint8_t *>(
       (reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~static_cast<uintptr_t>(1023));
-  const int c = blockIdx.x, h = blockIdx.y;
+  const int c = blockIdx.x, h0 = ALLH ? 0 : blockIdx.y;  // first KV head of the CTA
   __shared__ int hdr[5];  // go, tile, s_begin, s_end, bad map -- read once, used by all threads
   const uint32_t base = smem_u32(smem);
   unsigned long long *trace =
-      p.trace ? p.trace + 4 * ((static_cast<int64_t>(blockIdx.z) * p.Hkv + h) * p.C + c)
+      p.trace ? p.trace + 4 * ((static_cast<int64_t>(blockIdx.z) * gridDim.y + blockIdx.y) * p.C + c)
               : nullptr;
   if (trace && threadIdx.x == 0) trace[0] = globaltimer_ns();
   // Nothing above this line reads memory that an earlier kernel writes: with
@@ -720,7 +777,11 @@ __global__ void __launch_bounds__(kThreads, 2)
     const int tile = tm[TM_TILE];
     int go = tm[TM_STATUS] == 0;
     if (go && (tm[TM_B] != p.B || tm[TM_C] != p.C || tile <= 0 || tile % PAGE != 0)) {
-      if (c == 0 && h == 0) status_or(p.tm, HPA_STATUS_MISMATCH);
+      if (c == 0 && h0 == 0) status_or(p.tm, HPA_STATUS_MISMATCH);
+      go = 0;
+    }
+    if (go && !map_ranges_ok(tm, p.lay, p.B, p.C, c)) {
+      status_or(p.tm, HPA_STATUS_BAD_MAP);
       go = 0;
     }
     hdr[4] = !go;
@@ -748,12 +809,15 @@ __global__ void __launch_bounds__(kThreads, 2)
   if (!hdr[0]) {  // bad map, or a partition with no tiles
     if (FUSED && hdr[4]) {
       // fused combine on a bad map: NaN outputs, as the combine kernel writes;
-      // CTA (c, h) covers requests c, c + C, ... for the heads of group h
+      // CTA (c, h) covers requests c, c + C, ... for the query heads of its KV heads
       const float nan = CUDART_NAN_F;
       for (int r = c; r < p.B; r += p.C)
-        for (int v = threadIdx.x; v < group_rows(p) * (HEAD_DIM / 4); v += kThreads) {
-          const int row = row_base() + v / (HEAD_DIM / 4), c4 = v % (HEAD_DIM / 4);
-          const int64_t col = static_cast<int64_t>(row / p.G) * p.Hq + h * p.G + row % p.G;
+        for (int v = threadIdx.x; v < (ALLH ? p.Hkv : 1) * group_rows(p) * (HEAD_DIM / 4);
+             v += kThreads) {
+          const int hh = h0 + v / (group_rows(p) * (HEAD_DIM / 4));
+          const int vr = v % (group_rows(p) * (HEAD_DIM / 4));
+          const int row = row_base() + vr / (HEAD_DIM / 4), c4 = vr % (HEAD_DIM / 4);
+          const int64_t col = static_cast<int64_t>(row / p.G) * p.Hq + hh * p.G + row % p.G;
           const int64_t orow = static_cast<int64_t>(r) * p.q_len * p.Hq + col;
           store_bf16x4(p.out + orow * HEAD_DIM + 4 * c4, make_float4(nan, nan, nan, nan));
           if (c4 == 0 && p.out_lse != nullptr) p.out_lse[orow] = nan;
@@ -765,14 +829,14 @@ __global__ void __launch_bounds__(kThreads, 2)
   const int tile = hdr[1], s_begin = hdr[2], s_end = hdr[3];
 
   if (threadIdx.x >= kConsumerWarps * 32) {
-    producer<KV, FUSED>(p, &tmk, &tmv, smem, s_begin, s_end, tile, h);
+    producer<KV, FUSED, ALLH>(p, &tmk, &tmv, smem, s_begin, s_end, tile, h0);
   } else {
-    consumer<KV, FUSED>(p, smem, s_begin, s_end, tile, h);
+    consumer<KV, FUSED, ALLH>(p, smem, s_begin, s_end, tile, h0);
     if (trace && threadIdx.x == 0) trace[2] = globaltimer_ns();  // after the last epilogue
   }
 }
 
-template <int KV, bool FUSED>
+template <int KV, bool FUSED, bool ALLH>
 cudaError_t launch(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMap &tmv,
                    cudaStream_t s) {
   static int configured[64] = {0};
@@ -780,13 +844,13 @@ cudaError_t launch(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMa
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
   if (dev < 64 && !configured[dev]) {
-    e = cudaFuncSetAttribute(decode_attn_kernel<KV, FUSED>,
+    e = cudaFuncSetAttribute(decode_attn_kernel<KV, FUSED, ALLH>,
                              cudaFuncAttributeMaxDynamicSharedMemorySize, Smem<KV>::kAlloc);
     if (e != cudaSuccess) return e;
     configured[dev] = 1;
   }
   cudaLaunchConfig_t cfg = {};
-  cfg.gridDim = dim3(p.C, p.Hkv, (p.rows + MAX_ROWS - 1) / MAX_ROWS);
+  cfg.gridDim = dim3(p.C, ALLH ? 1 : p.Hkv, (p.rows + MAX_ROWS - 1) / MAX_ROWS);
   cfg.blockDim = dim3(kThreads);
   cfg.dynamicSmemBytes = Smem<KV>::kAlloc;
   cfg.stream = s;
@@ -795,16 +859,16 @@ cudaError_t launch(const AttnParams &p, const CUtensorMap &tmk, const CUtensorMa
   attr[0].val.programmaticStreamSerializationAllowed = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, decode_attn_kernel<KV, FUSED>, tmk, tmv, p);
+  return cudaLaunchKernelEx(&cfg, decode_attn_kernel<KV, FUSED, ALLH>, tmk, tmv, p);
 }
 
 template <int KV>
 int occupancy(int *ctas) {
-  cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<KV, false>,
+  cudaError_t e = cudaFuncSetAttribute(decode_attn_kernel<KV, false, false>,
                                        cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        Smem<KV>::kAlloc);
   if (e != cudaSuccess) return -1;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, decode_attn_kernel<KV, false>,
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(ctas, decode_attn_kernel<KV, false, false>,
                                                     kThreads, Smem<KV>::kAlloc);
   return e == cudaSuccess ? 0 : -1;
 }
@@ -814,11 +878,15 @@ int occupancy(int *ctas) {
 cudaError_t launch_decode_attn(const AttnParams &p, const CUtensorMap &tmk,
                                const CUtensorMap &tmv, int kv_dtype, cudaStream_t s) {
   const bool fused = p.out != nullptr;  // the fused combine is its own instantiation
+  const bool all_heads = p.heads_per_cta > 1;  // every KV head in the CTA (unfused only)
+  if (fused && all_heads) return cudaErrorInvalidValue;
   if (kv_dtype == HPA_KV_BF16)
-    return fused ? launch<HPA_KV_BF16, true>(p, tmk, tmv, s)
-                 : launch<HPA_KV_BF16, false>(p, tmk, tmv, s);
-  return fused ? launch<HPA_KV_E4M3, true>(p, tmk, tmv, s)
-               : launch<HPA_KV_E4M3, false>(p, tmk, tmv, s);
+    return fused       ? launch<HPA_KV_BF16, true, false>(p, tmk, tmv, s)
+           : all_heads ? launch<HPA_KV_BF16, false, true>(p, tmk, tmv, s)
+                       : launch<HPA_KV_BF16, false, false>(p, tmk, tmv, s);
+  return fused       ? launch<HPA_KV_E4M3, true, false>(p, tmk, tmv, s)
+         : all_heads ? launch<HPA_KV_E4M3, false, true>(p, tmk, tmv, s)
+                     : launch<HPA_KV_E4M3, false, false>(p, tmk, tmv, s);
 }
 
 int attn_ctas_per_sm(int kv_dtype, int q_len, int *ctas) {

@@ -96,15 +96,22 @@ struct TcSmem {
   static constexpr int kPSW = NC == 1 ? 32 : NC == 2 ? 64 : 128;  // bytes per key row
   static constexpr int kPSwz = kPSW == 32 ? 6 : kPSW == 64 ? 4 : 2;  // descriptor mode
   static constexpr int kPBuf = kStepKeys * kPSW;
-  // as many stages as fit beside the operands (one CTA per SM): DRAM latency is
-  // hidden by the bytes in flight
-  static constexpr int kStages0 =
-      (226 * 1024 - 2 * kOperand - 2 * kPBuf - 6 * 1024) / kStageBytes;
-  static constexpr int kStages = kStages0 > 6 ? 6 : kStages0;
+  // P^T of a step is written over the K half of that step's own stage: Q K^T has
+  // read K by then (its completion is what the compute warps wait for), and the
+  // P V that reads P^T is what releases the stage.  So P^T needs no buffers of
+  // its own and the room goes to one more stage.
+  static_assert(kPBuf <= kKStep, "P^T fits in the K half of a stage");
+  // Up to 32 rows, as many stages as fit beside the operands (one CTA per SM):
+  // there DRAM latency is hidden by the bytes in flight (2 -> 3 stages at 32 rows:
+  // 1.21x).  With 48 or 64 rows the compute warps are the bound and deeper rings
+  // were slower (6 and 5 stages against 4: 5 % and 10 %), so they keep 4.
+  static constexpr int kStages0 = (226 * 1024 - 2 * kOperand - 6 * 1024) / kStageBytes;
+  static constexpr int kStageCap = NC <= 2 ? 6 : 4;
+  static constexpr int kStages = kStages0 > kStageCap ? kStageCap : kStages0;
   static constexpr int kQ = kStages * kStageBytes;             // 2 query slots
-  static constexpr int kP = kQ + 2 * kOperand;                 // 2 probability buffers
-  static constexpr int kRowC = kP + 2 * kPBuf;                 // float[2][64] score scales
-  static constexpr int kStepMax = kRowC + 2 * 64 * 4;          // float[2][4][64]
+  static constexpr int kRowC = kQ + 2 * kOperand;              // float[2][64] score scales
+  static constexpr int kRowLo = kRowC + 2 * 64 * 4;            // float[2][64] lo-term scales
+  static constexpr int kStepMax = kRowLo + 2 * 64 * 4;         // float[2][4][64]
   static constexpr int kFlags = kStepMax + 2 * 4 * 64 * 4;     // int[2][16]
   static constexpr int kLRed = kFlags + 128;                   // float[4][64] row-sum parts
   static constexpr int kJRow = kLRed + 4 * 64 * 4;             // int[64]: token j of row r
@@ -118,6 +125,7 @@ struct TcSmem {
   static constexpr int kAbort = kTmem + 4;
   static constexpr int kBytes = kAbort + 4;
   static constexpr int kAlloc = kBytes + 1024;                 // room to align the base
+  static_assert(kAlloc <= 232448, "dynamic shared memory of one CTA");
   // TMEM columns: S[0], S[1] (kMT tiles of kNS each), O (kNS), rounded up to a power
   // of two >= 32
   static constexpr int kCols = (2 * kMT + 1) * kNS;
@@ -230,6 +238,14 @@ __device__ __forceinline__ void sts128(uint32_t addr, uint32_t a, uint32_t b, ui
                : "memory");
 }
 
+// 2^k with a * 2^k in [128, 256) for a > 0 (1 for a == 0), k clamped to keep it an
+// fp32 normal.
+__device__ __forceinline__ float pow2_to_128(float a) {
+  int ea = static_cast<int>((__float_as_uint(a) >> 23) & 0xffu) - 127;
+  ea = min(max(ea, -119), 126);
+  return a > 0.f ? __uint_as_float(static_cast<uint32_t>(127 + 7 - ea) << 23) : 1.f;
+}
+
 __device__ __forceinline__ float warp_max(float x) {
   float r;
   asm volatile("redux.sync.max.f32 %0, %1, 0xffffffff;" : "=f"(r) : "f"(x));
@@ -279,9 +295,8 @@ struct Tc {
     bool ok = true;
     for (int s = s_begin; s < s_end && ok; ++s) {
       const int k = s - s_begin, slot = k & 1;
-      const int4 sg = reinterpret_cast<const int4 *>(p.tm + p.lay.segs)[s];
-      const int r = sg.x, L = p.tm[p.lay.lens + r];
-      const int klo = sg.y * tile, khi = min(sg.z * tile, L);
+      const SegRow sr = read_seg_row(p.tm, p.lay, p.B, s, blockIdx.x, tile, lane == 0);
+      const int r = sr.r, L = sr.L, klo = sr.klo, khi = sr.khi;
       const int pg0 = klo / PAGE, pg1 = (khi + PAGE - 1) / PAGE;
       int good = 1;
       if (lane == 0)
@@ -293,6 +308,7 @@ struct Tc {
       // query rows -> operand slot (K-major, 128-byte swizzle); lane l holds dims 4l..4l+3
       uint8_t *qs = smem + S::kQ + slot * S::kOperand;
       float *rowc = reinterpret_cast<float *>(smem + S::kRowC) + slot * 64;
+      float *rowlo = reinterpret_cast<float *>(smem + S::kRowLo) + slot * 64;
       for (int row = 0; row < kRp; ++row) {
         float x[4] = {0.f, 0.f, 0.f, 0.f};
         if (row < R) {
@@ -312,26 +328,36 @@ struct Tc {
         } else {
           float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
           amax = warp_max(amax);
-          // A power-of-two row scale keeps q * sq a bf16 value (8 significant bits), which
-          // hi + lo (4 + 4 bits) then carry exactly: amax * sq lands in [128, 256).
-          int ea = static_cast<int>((__float_as_uint(amax) >> 23) & 0xffu) - 127;
-          ea = min(max(ea, -119), 126);
-          const float sq = amax > 0.f ? __uint_as_float(static_cast<uint32_t>(127 + 7 - ea) << 23)
-                                      : 1.f;
+          // A power-of-two row scale puts amax * sq in [128, 256) (hi = e4m3 of it), and the
+          // residuals x * sq - hi get a power-of-two scale of their own that puts their
+          // largest in [128, 256) too (lo = e4m3 of it), so hi + lo / st carries a bf16
+          // element to its 8 significant bits down to far below the row's largest (the
+          // residuals of small elements would otherwise fall under E4M3's smallest step).
+          const float sq = pow2_to_128(amax);
           uint32_t hi = 0, lo = 0;
+          float res[4];
 #pragma unroll
           for (int e = 0; e < 4; e += 2) {
             const float v0 = x[e] * sq, v1 = x[e + 1] * sq;
             const uint16_t h2 = f32x2_to_e4m3x2(v0, v1);
             const uint32_t hh = e4m3x2_to_f16x2(h2);
             const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hh));
-            const uint16_t l2 = f32x2_to_e4m3x2(v0 - hf.x, v1 - hf.y);
+            res[e] = v0 - hf.x;  // exact: both have at most 8 significant bits
+            res[e + 1] = v1 - hf.y;
             hi |= static_cast<uint32_t>(h2) << (8 * e);
-            lo |= static_cast<uint32_t>(l2) << (8 * e);
           }
+          const float rmax =
+              warp_max(fmaxf(fmaxf(fabsf(res[0]), fabsf(res[1])), fmaxf(fabsf(res[2]), fabsf(res[3]))));
+          const float st = pow2_to_128(rmax);
+#pragma unroll
+          for (int e = 0; e < 4; e += 2)
+            lo |= static_cast<uint32_t>(f32x2_to_e4m3x2(res[e] * st, res[e + 1] * st)) << (8 * e);
           *reinterpret_cast<uint32_t *>(qs + kmaj(row, 4 * lane, 0)) = hi;
           *reinterpret_cast<uint32_t *>(qs + kRp * 128 + kmaj(row, 4 * lane, 0)) = lo;
-          if (lane == 0) rowc[row] = p.scale_log2 * ksc / sq;
+          if (lane == 0) {
+            rowc[row] = p.scale_log2 * ksc / sq;
+            rowlo[row] = 1.f / st;  // a power of two: exact
+          }
         }
       }
       if (lane == 0)
@@ -433,9 +459,8 @@ struct Tc {
     bool ok = true;
     for (int s = s_begin; s < s_end && ok; ++s) {
       const int k = s - s_begin, slot = k & 1;
-      const int4 sg = reinterpret_cast<const int4 *>(p.tm + p.lay.segs)[s];
-      const int L = p.tm[p.lay.lens + sg.x];
-      const int pg0 = sg.y * tile / PAGE, pg1 = (min(sg.z * tile, L) + PAGE - 1) / PAGE;
+      const SegRow sr = read_seg_row(p.tm, p.lay, p.B, s, blockIdx.x, tile, false);
+      const int pg0 = sr.klo / PAGE, pg1 = (sr.khi + PAGE - 1) / PAGE;
       const int nsteps = (pg1 - pg0 + S::kPPS - 1) / S::kPPS;
       if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_Q_FULL + slot), (k >> 1) & 1)) {
         ok = false;
@@ -493,9 +518,8 @@ struct Tc {
     bool ok = true;
     for (int s = s_begin; s < s_end && ok; ++s) {
       const int k = s - s_begin;
-      const int4 sg = reinterpret_cast<const int4 *>(p.tm + p.lay.segs)[s];
-      const int L = p.tm[p.lay.lens + sg.x];
-      const int pg0 = sg.y * tile / PAGE, pg1 = (min(sg.z * tile, L) + PAGE - 1) / PAGE;
+      const SegRow sr = read_seg_row(p.tm, p.lay, p.B, s, blockIdx.x, tile, false);
+      const int pg0 = sr.klo / PAGE, pg1 = (sr.khi + PAGE - 1) / PAGE;
       const int nsteps = (pg1 - pg0 + S::kPPS - 1) / S::kPPS;
       for (int j = 0; j < nsteps; ++j) {
         const int b = i & 1;
@@ -507,7 +531,7 @@ struct Tc {
         }
         tc_fence_after();
         const uint32_t vbase = base + st * S::kStageBytes + S::kKStep;
-        const uint32_t pbase = base + S::kP + b * S::kPBuf;
+        const uint32_t pbase = base + st * S::kStageBytes;  // P^T over the stage's K
         // A = V^T and B = P^T, both MN-major; B's stride between groups of 8 keys is
         // 8 key rows
         if (KV == HPA_KV_BF16) {
@@ -570,6 +594,7 @@ struct Tc {
       const int nsteps = (pg1 - pg0 + S::kPPS - 1) / S::kPPS;
       if (L < q_len && t == 0) status_or(p.tm, HPA_STATUS_BAD_SEQLEN);
       const uint32_t rowc_s = base + S::kRowC + (slot * 64 + r0) * 4;
+      const uint32_t rowlo_s = base + S::kRowLo + (slot * 64 + r0) * 4;
       const float c_all = p.scale_log2;  // bf16: one score scale for every row
       float mref[RH], lsum[RH];  // reference max per row; this key slot's share of l
 #pragma unroll
@@ -593,11 +618,16 @@ struct Tc {
             const uint32_t col = lane_t + (b * MT + m) * S::kNS + r0 + 8 * c;
             float v[8];
             tc_ld8(col, v);
-            if (KV == HPA_KV_E4M3) {  // S = S(Q hi) + S(Q lo)
-              float u[8];
+            if (KV == HPA_KV_E4M3) {  // S = S(Q hi) + S(Q lo) / st, st the lo term's row scale
+              float u[8], lo8[8];
               tc_ld8(col + kRp, u);
+              uint32_t w[8];
+              lds128(rowlo_s + 32 * c, w[0], w[1], w[2], w[3]);
+              lds128(rowlo_s + 32 * c + 16, w[4], w[5], w[6], w[7]);
 #pragma unroll
-              for (int e = 0; e < 8; ++e) v[e] += u[e];
+              for (int e = 0; e < 8; ++e) lo8[e] = __uint_as_float(w[e]);
+#pragma unroll
+              for (int e = 0; e < 8; ++e) v[e] = fmaf(u[e], lo8[e], v[e]);
             }
 #pragma unroll
             for (int e = 0; e < 8; ++e) x[m][8 * c + e] = v[e];
@@ -716,7 +746,11 @@ struct Tc {
             tc_fence_before();
           }
         }
-        // P[b] is free once the P V of two steps back has completed
+        // Wait out the P V of two steps back.  P^T now lives in this step's own stage,
+        // so no buffer depends on it; the wait keeps this thread's parity waits on
+        // PV_DONE[b] in order (each of its uses waited, so a later parity wait cannot
+        // mistake an older phase for the one it expects) and bounds how far the
+        // compute warps run ahead of P V.
         if (i >= 2 && (*abort_flag ||
                        !mbar_wait_bounded(bars + 8 * (B_PV_DONE + b), ((i - 2) >> 1) & 1))) {
           ok = false;
@@ -725,7 +759,7 @@ struct Tc {
         // P^T goes to shared memory MN-major: this thread's key kk holds rows
         // [r0, r0 + RH) at bytes [r0, r0 + RH) (E4M3 hi; lo at Rp + r0) or [2 r0, 2 r0 + 2 RH)
         // (bf16) of its row
-        const uint32_t pb = base + S::kP + b * S::kPBuf;
+        const uint32_t pb = base + st * S::kStageBytes;  // over this step's K (read by Q K^T)
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
           const int kk = kt + 128 * m;  // key within the step
@@ -877,6 +911,10 @@ __global__ void __launch_bounds__(TcSmem<KV, NC>::kThreads, 1)
     int go = tm[TM_STATUS] == 0;
     if (go && (tm[TM_B] != p.B || tm[TM_C] != p.C || tile <= 0 || tile % PAGE != 0)) {
       if (c == 0 && h == 0) status_or(p.tm, HPA_STATUS_MISMATCH);
+      go = 0;
+    }
+    if (go && !map_ranges_ok(tm, p.lay, p.B, p.C, c)) {
+      status_or(p.tm, HPA_STATUS_BAD_MAP);
       go = 0;
     }
     hdr[1] = tile;

@@ -9,14 +9,24 @@
 
 #include "hpa_internal.cuh"
 
-namespace {
+namespace hpa {
 
-thread_local int g_last_cuda_error = 0;
+namespace {
+thread_local int g_last_cuda_error = 0;  // what hpa_last_cuda_error() reports, per thread
+}  // namespace
 
 int cuda_fail(cudaError_t e) {
   g_last_cuda_error = static_cast<int>(e);
   return HPA_ERR_CUDA;
 }
+
+int last_cuda_error() { return g_last_cuda_error; }
+
+}  // namespace hpa
+
+namespace {
+
+using hpa::cuda_fail;
 
 bool aligned(const void *p, uintptr_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
 
@@ -130,7 +140,7 @@ size_t hpa_static_taskmap_bytes(int32_t B, int32_t splits) {
   return static_cast<size_t>(taskmap_words(B, C, C)) * 4;
 }
 
-int32_t hpa_default_num_ctas(int32_t Hq, int32_t Hkv, int32_t q_len, int32_t kv_dtype) {
+int32_t hpa_default_num_ctas_mma(int32_t Hq, int32_t Hkv, int32_t q_len, int32_t kv_dtype) {
   if (Hkv < 1 || Hq < Hkv || Hq % Hkv != 0 || q_len < 1 ||
       (kv_dtype != HPA_KV_BF16 && kv_dtype != HPA_KV_E4M3))
     return -1;
@@ -138,7 +148,7 @@ int32_t hpa_default_num_ctas(int32_t Hq, int32_t Hkv, int32_t q_len, int32_t kv_
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) {
-    g_last_cuda_error = static_cast<int>(e);
+    cuda_fail(e);
     return -1;
   }
   if (hpa::attn_ctas_per_sm(kv_dtype, q_len, &per_sm) != 0 || per_sm < 1) return -1;
@@ -191,7 +201,7 @@ static int decode_attn_impl(const void *q_dev, const void *k_pool_dev, const voi
                             int32_t d, float sm_scale, void *taskmap_dev, int32_t num_ctas,
                             float *partial_o_dev, float *partial_lse_dev, uint64_t *trace_dev,
                             void *out_dev, float *out_lse_dev, int32_t *arrivals_dev,
-                            hpa_stream_t stream, bool tc = false) {
+                            hpa_stream_t stream, bool tc = false, bool all_heads = false) {
   if (!q_dev || !k_pool_dev || !v_pool_dev || !page_indptr_dev || !page_indices_dev ||
       !taskmap_dev || !partial_o_dev || !partial_lse_dev)
     return HPA_ERR_INVALID;
@@ -233,6 +243,7 @@ static int decode_attn_impl(const void *q_dev, const void *k_pool_dev, const voi
   p.Hkv = Hkv;
   p.G = Hq / Hkv;
   p.rows = p.G * q_len;
+  p.heads_per_cta = all_heads ? Hkv : 1;
   p.scale_log2 = sm_scale * 1.4426950408889634f;
   cudaError_t e =
       tc ? hpa::launch_decode_attn_tc(p, tmk, tmv, kv_dtype, reinterpret_cast<cudaStream_t>(stream))
@@ -262,13 +273,32 @@ int32_t hpa_default_num_ctas_tc(int32_t Hq, int32_t Hkv, int32_t q_len, int32_t 
   cudaError_t e = cudaGetDevice(&dev);
   if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (e != cudaSuccess) {
-    g_last_cuda_error = static_cast<int>(e);
+    cuda_fail(e);
     return -1;
   }
   if (hpa::attn_tc_ctas_per_sm(kv_dtype, (Hq / Hkv) * q_len, &per_sm) != 0 || per_sm < 1)
     return -1;
   const int c = sms * per_sm / Hkv;
   return c < 1 ? 1 : c;
+}
+
+int hpa_decode_attn_mma(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
+                        int32_t kv_dtype, const float *k_scale_dev, const float *v_scale_dev,
+                        int64_t num_pages, const int32_t *page_indptr_dev,
+                        const int32_t *page_indices_dev, int32_t page_size, int32_t B,
+                        int32_t q_len, int32_t Hq, int32_t Hkv, int32_t d, float sm_scale,
+                        void *taskmap_dev, int32_t num_ctas, float *partial_o_dev,
+                        float *partial_lse_dev, hpa_stream_t stream) {
+  return decode_attn_impl(q_dev, k_pool_dev, v_pool_dev, kv_dtype, k_scale_dev, v_scale_dev,
+                          num_pages, page_indptr_dev, page_indices_dev, page_size, B, q_len, Hq,
+                          Hkv, d, sm_scale, taskmap_dev, num_ctas, partial_o_dev,
+                          partial_lse_dev, nullptr, nullptr, nullptr, nullptr, stream);
+}
+
+// More than 16 query rows per KV head (MTP with several draft tokens) go to the
+// tcgen05 kernel, which takes all rows in one pass over the keys.
+static bool routes_to_tc(int32_t Hq, int32_t Hkv, int32_t q_len) {
+  return Hkv >= 1 && Hq % Hkv == 0 && int64_t(Hq / Hkv) * q_len > hpa::MAX_ROWS;
 }
 
 int hpa_decode_attn(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
@@ -281,7 +311,13 @@ int hpa_decode_attn(const void *q_dev, const void *k_pool_dev, const void *v_poo
   return decode_attn_impl(q_dev, k_pool_dev, v_pool_dev, kv_dtype, k_scale_dev, v_scale_dev,
                           num_pages, page_indptr_dev, page_indices_dev, page_size, B, q_len, Hq,
                           Hkv, d, sm_scale, taskmap_dev, num_ctas, partial_o_dev,
-                          partial_lse_dev, nullptr, nullptr, nullptr, nullptr, stream);
+                          partial_lse_dev, nullptr, nullptr, nullptr, nullptr, stream,
+                          routes_to_tc(Hq, Hkv, q_len));
+}
+
+int32_t hpa_default_num_ctas(int32_t Hq, int32_t Hkv, int32_t q_len, int32_t kv_dtype) {
+  return routes_to_tc(Hq, Hkv, q_len) ? hpa_default_num_ctas_tc(Hq, Hkv, q_len, kv_dtype)
+                                      : hpa_default_num_ctas_mma(Hq, Hkv, q_len, kv_dtype);
 }
 
 int hpa_decode_attn_traced(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
@@ -297,6 +333,39 @@ int hpa_decode_attn_traced(const void *q_dev, const void *k_pool_dev, const void
                           num_pages, page_indptr_dev, page_indices_dev, page_size, B, q_len, Hq,
                           Hkv, d, sm_scale, taskmap_dev, num_ctas, partial_o_dev,
                           partial_lse_dev, trace_dev, nullptr, nullptr, nullptr, stream);
+}
+
+int hpa_decode_attn_allheads(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
+                             int32_t kv_dtype, const float *k_scale_dev,
+                             const float *v_scale_dev, int64_t num_pages,
+                             const int32_t *page_indptr_dev, const int32_t *page_indices_dev,
+                             int32_t page_size, int32_t B, int32_t q_len, int32_t Hq,
+                             int32_t Hkv, int32_t d, float sm_scale, void *taskmap_dev,
+                             int32_t num_ctas, float *partial_o_dev, float *partial_lse_dev,
+                             uint64_t *trace_dev, hpa_stream_t stream) {
+  if (trace_dev && !aligned(trace_dev, 8)) return HPA_ERR_ALIGN;
+  return decode_attn_impl(q_dev, k_pool_dev, v_pool_dev, kv_dtype, k_scale_dev, v_scale_dev,
+                          num_pages, page_indptr_dev, page_indices_dev, page_size, B, q_len, Hq,
+                          Hkv, d, sm_scale, taskmap_dev, num_ctas, partial_o_dev,
+                          partial_lse_dev, trace_dev, nullptr, nullptr, nullptr, stream, false,
+                          true);
+}
+
+int32_t hpa_default_num_ctas_allheads(int32_t Hq, int32_t Hkv, int32_t q_len, int32_t kv_dtype) {
+  const int32_t per_head = hpa_default_num_ctas_mma(Hq, Hkv, q_len, kv_dtype);
+  if (per_head <= 0) return per_head;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e != cudaSuccess) {
+    cuda_fail(e);
+    return -1;
+  }
+  if (hpa::attn_ctas_per_sm(kv_dtype, q_len, &per_sm) != 0 || per_sm < 1) return -1;
+  // one CTA per (partition, group of 16 query rows), each walking every KV head
+  const int groups = ((Hq / Hkv) * q_len + hpa::MAX_ROWS - 1) / hpa::MAX_ROWS;
+  const int c = sms * per_sm / groups;
+  return c < 1 ? 1 : c;
 }
 
 size_t hpa_arrivals_elems(int32_t B, int32_t Hq, int32_t Hkv, int32_t q_len) {
@@ -407,6 +476,6 @@ const char *hpa_error_string(int code) {
   }
 }
 
-int hpa_last_cuda_error(void) { return g_last_cuda_error; }
+int hpa_last_cuda_error(void) { return hpa::last_cuda_error(); }
 
 }  // extern "C"

@@ -54,8 +54,14 @@ struct AttnParams {
   int64_t num_pages;
   TaskMapLayout lay;
   int B, C, q_len, Hq, Hkv, G, rows;
-  float scale_log2;  // sm_scale * log2(e)
+  int heads_per_cta;  // KV heads one CTA walks per segment: 1 (grid over heads) or Hkv
+  float scale_log2;   // sm_scale * log2(e)
 };
+
+// Records e as the calling thread's last CUDA error (hpa_last_cuda_error) and
+// returns HPA_ERR_CUDA; every entry point reports runtime failures through it.
+int cuda_fail(cudaError_t e);
+int last_cuda_error();
 
 constexpr size_t kPlanStageLimit = 40 * 1024;  // shared memory the plan kernel may stage in
 size_t plan_stage_bytes(int B, int C, int kind);
@@ -237,6 +243,11 @@ __device__ __forceinline__ uint32_t pack_f16(float lo, float hi) {
   return *reinterpret_cast<uint32_t *>(&v);
 }
 
+// 2^k for an integer k in [-126, 127], built from the exponent bits (exact).
+__device__ __forceinline__ float exp2i(int k) {
+  return __uint_as_float(static_cast<uint32_t>(127 + k) << 23);
+}
+
 __device__ __forceinline__ void named_barrier(int id, int threads) {
   asm volatile("bar.sync %0, %1;" ::"r"(id), "r"(threads) : "memory");
 }
@@ -252,6 +263,41 @@ __device__ __forceinline__ void pdl_launch_dependents() {
 
 __device__ __forceinline__ void status_or(int32_t *tm, int bits) {
   atomicOr(reinterpret_cast<int *>(tm + TM_STATUS), bits);
+}
+
+// One segment row of a task map, checked before use: request in [0, B), owned by
+// partition c, 0 <= tile_lo < tile_hi <= ceil(L_r / tile).  A row that fails (a
+// map corrupted after hpa_plan wrote it) is reported as HPA_STATUS_BAD_MAP when
+// `report` is set and read as an empty segment of request 0, so no kernel follows
+// an index out of the buffers the map was sized for.  Every reader of a row gets
+// the same answer, so the roles of one CTA stay in step.
+struct SegRow {
+  int r, L, klo, khi;  // request, its length, key range [klo, khi)
+};
+__device__ __forceinline__ SegRow read_seg_row(int32_t *tm, const TaskMapLayout &lay, int B,
+                                               int s, int c, int tile, bool report) {
+  const int4 sg = reinterpret_cast<const int4 *>(tm + lay.segs)[s];
+  if (sg.x >= 0 && sg.x < B && sg.w == c && sg.y >= 0 && sg.y < sg.z) {
+    const int L = tm[lay.lens + sg.x];
+    if (L >= 1 && sg.z <= (L - 1) / tile + 1) {
+      const long long hi = static_cast<long long>(sg.z) * tile;
+      return SegRow{sg.x, L, sg.y * tile, hi < L ? static_cast<int>(hi) : L};
+    }
+  }
+  if (report) status_or(tm, HPA_STATUS_BAD_MAP);
+  return SegRow{0, 1 << 30, 0, 0};
+}
+
+// Header checks an attention kernel makes before it walks partition c: the map's
+// kind and segment capacity match what hpa_plan / hpa_plan_static build for (B, C),
+// and c's segment range lies inside the map's S segments.
+__device__ __forceinline__ bool map_ranges_ok(const int32_t *tm, const TaskMapLayout &lay, int B,
+                                              int C, int c) {
+  const int kind = tm[TM_KIND], S = tm[TM_S];
+  const int cap = kind == 1 ? C : B + C - 1;
+  const int sb = tm[lay.cta_seg + c], se = tm[lay.cta_seg + c + 1];
+  return kind >= 0 && kind <= 2 && tm[TM_SCAP] == cap && S >= 0 && S <= cap && sb >= 0 &&
+         sb <= se && se <= S;
 }
 
 }  // namespace hpa

@@ -21,28 +21,33 @@
 namespace hpa {
 namespace {
 
-constexpr int kPlanThreads = 1024;
+// The plan is latency-bound: one CTA, a few dependent rounds.  Its block size is
+// the smallest of 32 / 128 / 256 / 1024 threads that gives every request and
+// every partition a thread of its own (1024 beyond that, looping), so small
+// batches pay for few warps in each block-wide scan and barrier.
 
 // Inclusive scan over the block; `total` receives the block-wide sum.
+template <int kPlanThreads>
 __device__ long long block_scan(long long v, long long *wbuf, long long &total) {
   const int lane = threadIdx.x & 31, wid = threadIdx.x >> 5;
   for (int o = 1; o < 32; o <<= 1) {
     long long n = __shfl_up_sync(0xffffffffu, v, o);
     if (lane >= o) v += n;
   }
+  constexpr int kWarps = kPlanThreads / 32;  // wbuf holds one partial sum per warp
   if (lane == 31) wbuf[wid] = v;
   __syncthreads();
   if (wid == 0) {
-    long long w = (lane < kPlanThreads / 32) ? wbuf[lane] : 0;
-    for (int o = 1; o < 32; o <<= 1) {
+    long long w = lane < kWarps ? wbuf[lane] : 0;
+    for (int o = 1; o < kWarps; o <<= 1) {
       long long n = __shfl_up_sync(0xffffffffu, w, o);
       if (lane >= o) w += n;
     }
-    wbuf[lane] = w;
+    if (lane < kWarps) wbuf[lane] = w;
   }
   __syncthreads();
   if (wid > 0) v += wbuf[wid - 1];
-  total = wbuf[kPlanThreads / 32 - 1];
+  total = wbuf[kWarps - 1];
   __syncthreads();
   return v;
 }
@@ -58,6 +63,7 @@ __device__ int upper_bound(const int32_t *a, int n, long long x) {
   return lo;
 }
 
+template <int kPlanThreads>
 __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__restrict__ lens_in,
                                                             int B, int tile, int C, int kind,
                                                             int splits, int32_t *tm,
@@ -93,11 +99,11 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
       if (L < 1) atomicOr(&s_bad, HPA_STATUS_BAD_SEQLEN);
       else n = (L - 1) / tile + 1, keys = L;
     }
-    const long long incl = block_scan(n, wbuf, total);
+    const long long incl = block_scan<kPlanThreads>(n, wbuf, total);
     if (i < B) cu[i + 1] = cu_g[i + 1] = static_cast<int32_t>(carry + incl);
     carry += total;
     if (kind == 2) {
-      const long long kincl = block_scan(keys, wbuf, total);
+      const long long kincl = block_scan<kPlanThreads>(keys, wbuf, total);
       if (i < B) kc[i + 1] = kcarry + kincl;
       kcarry += total;
     }
@@ -184,7 +190,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
         cnt = rl - rf + 1;
       }
     }
-    const long long incl = block_scan(cnt, wbuf, total);
+    const long long incl = block_scan<kPlanThreads>(cnt, wbuf, total);
     if (c < C) cs[c] = static_cast<int32_t>(carry + incl - cnt);
     carry += total;
   }
@@ -246,8 +252,16 @@ cudaError_t launch_plan(const int32_t *seq_lens, int B, int tile, int C, int kin
   // they fit in 40 KB; the token-weighted map requires it (checked by the caller)
   const size_t stage_bytes = plan_stage_bytes(B, C, kind);
   const int staged = stage_bytes <= kPlanStageLimit;
-  plan_kernel<<<1, kPlanThreads, staged ? stage_bytes : 0, s>>>(seq_lens, B, tile, C, kind,
-                                                                  splits, tm, s_cap, staged);
+  const size_t smem = staged ? stage_bytes : 0;
+  const int need = B > C ? B : C;
+  if (need <= 32)
+    plan_kernel<32><<<1, 32, smem, s>>>(seq_lens, B, tile, C, kind, splits, tm, s_cap, staged);
+  else if (need <= 128)
+    plan_kernel<128><<<1, 128, smem, s>>>(seq_lens, B, tile, C, kind, splits, tm, s_cap, staged);
+  else if (need <= 256)
+    plan_kernel<256><<<1, 256, smem, s>>>(seq_lens, B, tile, C, kind, splits, tm, s_cap, staged);
+  else
+    plan_kernel<1024><<<1, 1024, smem, s>>>(seq_lens, B, tile, C, kind, splits, tm, s_cap, staged);
   return cudaGetLastError();
 }
 

@@ -18,7 +18,8 @@ import torch
 from . import build as _build
 
 KV_BF16, KV_E4M3 = 0, 1
-STATUS_BITS = {1: "BAD_SEQLEN", 2: "MISMATCH", 4: "BAD_PAGE", 8: "TIMEOUT", 16: "OVERFLOW"}
+STATUS_BITS = {1: "BAD_SEQLEN", 2: "MISMATCH", 4: "BAD_PAGE", 8: "TIMEOUT", 16: "OVERFLOW",
+               32: "BAD_MAP"}
 HEADER_WORDS = 16
 
 _lock = threading.Lock()
@@ -57,6 +58,12 @@ def lib():
                 "hpa_decode_attn_tc": ([P, P, P, I32, P, P, I64, P, P, I32, I32, I32, I32, I32,
                                         I32, F, P, I32, P, P, P], ctypes.c_int),
                 "hpa_default_num_ctas_tc": ([I32, I32, I32, I32], I32),
+                "hpa_decode_attn_mma": ([P, P, P, I32, P, P, I64, P, P, I32, I32, I32, I32, I32,
+                                         I32, F, P, I32, P, P, P], ctypes.c_int),
+                "hpa_default_num_ctas_mma": ([I32, I32, I32, I32], I32),
+                "hpa_decode_attn_allheads": ([P, P, P, I32, P, P, I64, P, P, I32, I32, I32, I32,
+                                              I32, I32, F, P, I32, P, P, P, P], ctypes.c_int),
+                "hpa_default_num_ctas_allheads": ([I32, I32, I32, I32], I32),
                 "hpa_decode_attn_traced": ([P, P, P, I32, P, P, I64, P, P, I32, I32, I32, I32,
                                             I32, I32, F, P, I32, P, P, P, P], ctypes.c_int),
                 "hpa_combine": ([P, P, P, I32, I32, I32, I32, I32, P, P, P], ctypes.c_int),
@@ -132,10 +139,26 @@ def hpa_default_num_ctas(Hkv: int, q_len: int, kv_dtype: int, Hq: int = 64) -> i
     return c
 
 
+def hpa_default_num_ctas_mma(Hkv: int, q_len: int, kv_dtype: int, Hq: int = 64) -> int:
+    c = int(lib().hpa_default_num_ctas_mma(Hq, Hkv, q_len, kv_dtype))
+    if c <= 0:
+        raise HpaError("hpa_default_num_ctas_mma failed (cudaError %d)" %
+                       lib().hpa_last_cuda_error())
+    return c
+
+
 def hpa_default_num_ctas_tc(Hkv: int, q_len: int, kv_dtype: int, Hq: int = 64) -> int:
     c = int(lib().hpa_default_num_ctas_tc(Hq, Hkv, q_len, kv_dtype))
     if c <= 0:
         raise HpaError("hpa_default_num_ctas_tc failed (cudaError %d)" %
+                       lib().hpa_last_cuda_error())
+    return c
+
+
+def hpa_default_num_ctas_allheads(Hkv: int, q_len: int, kv_dtype: int, Hq: int = 64) -> int:
+    c = int(lib().hpa_default_num_ctas_allheads(Hq, Hkv, q_len, kv_dtype))
+    if c <= 0:
+        raise HpaError("hpa_default_num_ctas_allheads failed (cudaError %d)" %
                        lib().hpa_last_cuda_error())
     return c
 
@@ -164,12 +187,8 @@ def hpa_plan_static(seq_lens, tile: int, splits: int, taskmap, stream=None):
            "hpa_plan_static")
 
 
-def hpa_decode_attn(q, k_pool, v_pool, page_indptr, page_indices, taskmap, num_ctas: int,
-                    partial_o, partial_lse, k_scale=None, v_scale=None,
-                    sm_scale: float | None = None, stream=None, tc: bool = False):
-    """q bf16 [B][q_len][Hq][d]; k/v pools bf16 or uint8 (E4M3) [P][Hkv][page][d].
-
-    tc=True calls hpa_decode_attn_tc (the tcgen05 kernel) with the same arguments."""
+def _attn_args(q, k_pool, v_pool, page_indptr, page_indices, taskmap, k_scale, v_scale):
+    """Checks shared by every attention call; returns (kv, B, q_len, Hq, d, P, Hkv, page)."""
     _dev(q, "q", torch.bfloat16)
     _dev(k_pool, "k_pool")
     _dev(v_pool, "v_pool")
@@ -186,22 +205,63 @@ def hpa_decode_attn(q, k_pool, v_pool, page_indptr, page_indices, taskmap, num_c
     for t, n in ((page_indptr, "page_indptr"), (page_indices, "page_indices")):
         _dev(t, n, torch.int32)
     _dev(taskmap, "taskmap")
-    _dev(partial_o, "partial_o", torch.float32)
-    _dev(partial_lse, "partial_lse", torch.float32)
+    if q.dim() != 4 or k_pool.dim() != 4:
+        raise HpaError("q must be [B][q_len][Hq][d] and the pools [P][Hkv][page][d]")
     B, q_len, Hq, d = q.shape
     P, Hkv, page, d2 = k_pool.shape
     if d2 != d:
         raise HpaError("head dim mismatch")
+    if kv == KV_E4M3 and (k_scale.numel() < Hkv or v_scale.numel() < Hkv):
+        raise HpaError("k_scale / v_scale need one fp32 value per KV head")
+    return kv, B, q_len, Hq, d, P, Hkv, page
+
+
+def _partials(partial_o, partial_lse, B, num_ctas, q_len, Hq, d):
+    _dev(partial_o, "partial_o", torch.float32)
+    _dev(partial_lse, "partial_lse", torch.float32)
     need = hpa_max_segments(B, num_ctas) * q_len * Hq
     if partial_lse.numel() < need or partial_o.numel() < need * d:
         raise HpaError("partial buffers too small: need (B + num_ctas - 1) segments")
+
+
+def _outputs(out, out_lse, B, q_len, Hq, d):
+    _dev(out, "out", torch.bfloat16)
+    if tuple(out.shape) != (B, q_len, Hq, d):
+        raise HpaError("out must have q's shape %s, got %s" % ((B, q_len, Hq, d),
+                                                               tuple(out.shape)))
+    if out_lse is not None:
+        _dev(out_lse, "out_lse", torch.float32)
+        if tuple(out_lse.shape) != (B, q_len, Hq):
+            raise HpaError("out_lse must have shape %s" % ((B, q_len, Hq),))
+
+
+def hpa_decode_attn(q, k_pool, v_pool, page_indptr, page_indices, taskmap, num_ctas: int,
+                    partial_o, partial_lse, k_scale=None, v_scale=None,
+                    sm_scale: float | None = None, stream=None, tc: bool = False,
+                    mma: bool = False):
+    """q bf16 [B][q_len][Hq][d]; k/v pools bf16 or uint8 (E4M3) [P][Hkv][page][d].
+
+    hpa_decode_attn picks the kernel by query rows per KV head (mma.sync up to 16,
+    tcgen05 above); tc=True calls hpa_decode_attn_tc and mma=True hpa_decode_attn_mma
+    with the same arguments."""
+    kv, B, q_len, Hq, d, P, Hkv, page = _attn_args(q, k_pool, v_pool, page_indptr,
+                                                   page_indices, taskmap, k_scale, v_scale)
+    _partials(partial_o, partial_lse, B, num_ctas, q_len, Hq, d)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(d)
-    name = "hpa_decode_attn_tc" if tc else "hpa_decode_attn"
+    name = "hpa_decode_attn_tc" if tc else "hpa_decode_attn_mma" if mma else "hpa_decode_attn"
     _check(getattr(lib(), name)(
         _ptr(q), _ptr(k_pool), _ptr(v_pool), kv, _ptr(k_scale), _ptr(v_scale), P,
         _ptr(page_indptr), _ptr(page_indices), page, B, q_len, Hq, Hkv, d, float(sm_scale),
         _ptr(taskmap), num_ctas, _ptr(partial_o), _ptr(partial_lse), _stream(stream)), name)
+
+
+def hpa_decode_attn_mma(q, k_pool, v_pool, page_indptr, page_indices, taskmap, num_ctas: int,
+                        partial_o, partial_lse, k_scale=None, v_scale=None,
+                        sm_scale: float | None = None, stream=None):
+    """hpa_decode_attn computed by the mma.sync kernel at any query-row count."""
+    hpa_decode_attn(q, k_pool, v_pool, page_indptr, page_indices, taskmap, num_ctas, partial_o,
+                    partial_lse, k_scale, v_scale, sm_scale, stream, mma=True)
 
 
 def hpa_decode_attn_tc(q, k_pool, v_pool, page_indptr, page_indices, taskmap, num_ctas: int,
@@ -212,14 +272,36 @@ def hpa_decode_attn_tc(q, k_pool, v_pool, page_indptr, page_indices, taskmap, nu
                     partial_lse, k_scale, v_scale, sm_scale, stream, tc=True)
 
 
+def hpa_decode_attn_allheads(q, k_pool, v_pool, page_indptr, page_indices, taskmap,
+                             num_ctas: int, partial_o, partial_lse, k_scale=None, v_scale=None,
+                             sm_scale: float | None = None, trace=None, stream=None):
+    """hpa_decode_attn with every KV head walked inside the CTA of a partition (grid over
+    partitions only); num_ctas counts partitions of the whole grid.  trace: optional int64
+    [4 * num_ctas * row groups] per-CTA timestamps."""
+    kv, B, q_len, Hq, d, P, Hkv, page = _attn_args(q, k_pool, v_pool, page_indptr,
+                                                   page_indices, taskmap, k_scale, v_scale)
+    _partials(partial_o, partial_lse, B, num_ctas, q_len, Hq, d)
+    if trace is not None:
+        _dev(trace, "trace", torch.int64)
+        if trace.numel() < 4 * num_ctas * ((Hq // Hkv * q_len + 15) // 16):
+            raise HpaError("trace buffer too small")
+    if sm_scale is None:
+        sm_scale = 1.0 / math.sqrt(d)
+    _check(lib().hpa_decode_attn_allheads(
+        _ptr(q), _ptr(k_pool), _ptr(v_pool), kv, _ptr(k_scale), _ptr(v_scale), P,
+        _ptr(page_indptr), _ptr(page_indices), page, B, q_len, Hq, Hkv, d, float(sm_scale),
+        _ptr(taskmap), num_ctas, _ptr(partial_o), _ptr(partial_lse), _ptr(trace),
+        _stream(stream)), "hpa_decode_attn_allheads")
+
+
 def hpa_decode_attn_traced(q, k_pool, v_pool, page_indptr, page_indices, taskmap, num_ctas: int,
                            partial_o, partial_lse, trace, k_scale=None, v_scale=None,
                            sm_scale: float | None = None, stream=None):
     """hpa_decode_attn plus per-CTA timestamps: trace is int64 [num_ctas * Hkv * 4] on device."""
+    kv, B, q_len, Hq, d, P, Hkv, page = _attn_args(q, k_pool, v_pool, page_indptr,
+                                                   page_indices, taskmap, k_scale, v_scale)
+    _partials(partial_o, partial_lse, B, num_ctas, q_len, Hq, d)
     _dev(trace, "trace", torch.int64)
-    B, q_len, Hq, d = q.shape
-    kv = KV_BF16 if k_pool.dtype == torch.bfloat16 else KV_E4M3
-    P, Hkv, page, _ = k_pool.shape
     groups = (Hq // Hkv * q_len + 15) // 16
     if trace.numel() < 4 * num_ctas * Hkv * groups:
         raise HpaError("trace buffer too small")
@@ -273,20 +355,13 @@ def hpa_decode_attn_fused(q, k_pool, v_pool, page_indptr, page_indices, taskmap,
                           v_scale=None, sm_scale: float | None = None, stream=None):
     """Attention with the combine folded in; arrivals: int32, hpa_arrivals_elems(B, Hq, Hkv,
     q_len) elements, zero between calls."""
-    _dev(q, "q", torch.bfloat16)
-    _dev(out, "out", torch.bfloat16)
+    kv, B, q_len, Hq, d, P, Hkv, page = _attn_args(q, k_pool, v_pool, page_indptr,
+                                                   page_indices, taskmap, k_scale, v_scale)
+    _partials(partial_o, partial_lse, B, num_ctas, q_len, Hq, d)
+    _outputs(out, out_lse, B, q_len, Hq, d)
     _dev(arrivals, "arrivals", torch.int32)
-    if out_lse is not None:
-        _dev(out_lse, "out_lse", torch.float32)
-    B, q_len, Hq, d = q.shape
-    kv = KV_BF16 if k_pool.dtype == torch.bfloat16 else KV_E4M3
-    P, Hkv, page, _ = k_pool.shape
-    need = hpa_max_segments(B, num_ctas) * q_len * Hq
-    if partial_lse.numel() < need or partial_o.numel() < need * d:
-        raise HpaError("partial buffers too small: need (B + num_ctas - 1) segments")
-    if arrivals.numel() < hpa_arrivals_elems(B, Hq, Hkv, q_len) or \
-            tuple(out.shape) != (B, q_len, Hq, d):
-        raise HpaError("arrivals or out has the wrong size")
+    if arrivals.numel() < hpa_arrivals_elems(B, Hq, Hkv, q_len):
+        raise HpaError("arrivals has the wrong size")
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(d)
     _check(lib().hpa_decode_attn_fused(
@@ -302,9 +377,11 @@ def hpa_combine(partial_o, partial_lse, taskmap, num_ctas: int, out, out_lse=Non
     _dev(partial_lse, "partial_lse", torch.float32)
     _dev(taskmap, "taskmap")
     _dev(out, "out", torch.bfloat16)
-    if out_lse is not None:
-        _dev(out_lse, "out_lse", torch.float32)
+    if out.dim() != 4:
+        raise HpaError("out must be [B][q_len][Hq][d]")
     B, q_len, Hq, d = out.shape
+    _outputs(out, out_lse, B, q_len, Hq, d)
+    _partials(partial_o, partial_lse, B, num_ctas, q_len, Hq, d)
     _check(lib().hpa_combine(_ptr(partial_o), _ptr(partial_lse), _ptr(taskmap), B, num_ctas,
                              q_len, Hq, d, _ptr(out), _ptr(out_lse), _stream(stream)),
            "hpa_combine")
@@ -327,12 +404,9 @@ def hpa_decode_attn_combine_noalloc(q, k_pool, v_pool, page_indptr, page_indices
     must not call cudaMalloc/cudaFree).  Calls that overlap on the GPU share
     that array and race; serialise them.
     """
-    for t, n in ((q, "q"), (k_pool, "k_pool"), (v_pool, "v_pool"), (page_indptr, "page_indptr"),
-                 (page_indices, "page_indices"), (taskmap, "taskmap"), (out, "out")):
-        _dev(t, n)
-    kv = KV_BF16 if k_pool.dtype == torch.bfloat16 else KV_E4M3
-    B, q_len, Hq, d = q.shape
-    P, Hkv, page, _ = k_pool.shape
+    kv, B, q_len, Hq, d, P, Hkv, page = _attn_args(q, k_pool, v_pool, page_indptr,
+                                                   page_indices, taskmap, k_scale, v_scale)
+    _outputs(out, out_lse, B, q_len, Hq, d)
     if sm_scale is None:
         sm_scale = 1.0 / math.sqrt(d)
     _check(lib().hpa_decode_attn_combine_noalloc(
@@ -417,21 +491,33 @@ class Workspace:
 
 def decode_step(ws: Workspace, q, k_pool, v_pool, seq_lens, page_indptr, page_indices, out,
                 out_lse=None, k_scale=None, v_scale=None, tile=512, plan=True, stream=None,
-                fused=False, tc=False):
+                fused=False, tc=False, sm_scale: float | None = None, allheads=False,
+                mma=False):
     """plan (optional) -> split-KV attention -> combine, all enqueued on one stream.
 
     fused=True runs the attention kernel with the combine folded in (one launch);
-    tc=True runs the tcgen05 attention kernel (size the workspace with
-    hpa_default_num_ctas_tc)."""
+    The attention call is hpa_decode_attn, which picks its kernel by query rows per KV
+    head (size the workspace with hpa_default_num_ctas); tc=True forces the tcgen05
+    kernel (hpa_default_num_ctas_tc), mma=True the mma.sync kernel
+    (hpa_default_num_ctas_mma), allheads=True the mma.sync variant with every KV head
+    inside the CTA (hpa_default_num_ctas_allheads); sm_scale defaults to 1/sqrt(d)."""
     if fused and tc:
         raise HpaError("the tcgen05 kernel has no fused-combine variant")
+    if allheads and (fused or tc):
+        raise HpaError("the all-heads variant has no fused or tcgen05 form")
     if plan:
         ws.plan(seq_lens, tile, stream)
     if fused:
         hpa_decode_attn_fused(q, k_pool, v_pool, page_indptr, page_indices, ws.taskmap,
                               ws.num_ctas, ws.partial_o, ws.partial_lse, out, ws.arrivals,
-                              out_lse, k_scale, v_scale, stream=stream)
+                              out_lse, k_scale, v_scale, sm_scale=sm_scale, stream=stream)
         return
-    hpa_decode_attn(q, k_pool, v_pool, page_indptr, page_indices, ws.taskmap, ws.num_ctas,
-                    ws.partial_o, ws.partial_lse, k_scale, v_scale, stream=stream, tc=tc)
+    if allheads:
+        hpa_decode_attn_allheads(q, k_pool, v_pool, page_indptr, page_indices, ws.taskmap,
+                                 ws.num_ctas, ws.partial_o, ws.partial_lse, k_scale, v_scale,
+                                 sm_scale=sm_scale, stream=stream)
+    else:
+        hpa_decode_attn(q, k_pool, v_pool, page_indptr, page_indices, ws.taskmap, ws.num_ctas,
+                        ws.partial_o, ws.partial_lse, k_scale, v_scale, sm_scale=sm_scale,
+                        stream=stream, tc=tc, mma=mma)
     hpa_combine(ws.partial_o, ws.partial_lse, ws.taskmap, ws.num_ctas, out, out_lse, stream)

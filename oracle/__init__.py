@@ -137,9 +137,9 @@ def combine(partial_o, partial_lse, seg_off):
     return out, lse
 
 
-def split_attention(batch, p, n_threads: int = 0):
+def split_attention(batch, p, n_threads: int = 0, sm_scale: float | None = None):
     """Every segment of task map `p` as its own partial (a5), in fp64."""
-    return attention(batch, segment_key_ranges(p), n_threads)
+    return attention(batch, segment_key_ranges(p), n_threads, sm_scale)
 
 
 def split_combine(batch, p, n_threads: int = 0):

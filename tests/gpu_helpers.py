@@ -7,6 +7,7 @@ import numpy as np
 import torch
 
 import load_balanced_split_gb300 as hpa
+import workloads as W
 
 HEADER = 16
 
@@ -72,20 +73,23 @@ class DeviceBatch:
         self.indices = torch.from_numpy(b.page_indices).to(device)
 
 
-def num_ctas_for(b, tc=False) -> int:
+def num_ctas_for(b, tc=False, allheads=False, mma=False) -> int:
     if b.num_ctas is not None:
         return b.num_ctas
-    fn = hpa.hpa_default_num_ctas_tc if tc else hpa.hpa_default_num_ctas
+    fn = (hpa.hpa_default_num_ctas_tc if tc else
+          hpa.hpa_default_num_ctas_allheads if allheads else
+          hpa.hpa_default_num_ctas_mma if mma else hpa.hpa_default_num_ctas)
     return fn(b.Hkv, b.q_len, hpa.KV_BF16 if b.kv_dtype == "bf16" else hpa.KV_E4M3, b.Hq)
 
 
 def run_gpu(b, num_ctas=None, splits=None, tile=512, db=None, fused=False, weighted=False,
-            tc=False):
+            tc=False, sm_scale=None, allheads=False, mma=False):
     """plan -> attention -> combine on the GPU (fused: one attention launch with the
-    combine folded in; tc: the tcgen05 attention kernel).  Returns host numpy results."""
+    combine folded in; tc / mma: the tcgen05 / mma.sync attention kernel forced; by
+    default hpa_decode_attn picks by row count).  Returns host numpy results."""
     db = db or DeviceBatch(b)
     if splits is None and num_ctas is None:
-        num_ctas = num_ctas_for(b, tc)
+        num_ctas = num_ctas_for(b, tc, allheads, mma)
     ws = hpa.Workspace(b.B, b.q_len, b.Hq, b.d, num_ctas=num_ctas, splits=splits,
                        weighted=weighted)
     ws.partial_o.fill_(float("nan"))
@@ -93,7 +97,8 @@ def run_gpu(b, num_ctas=None, splits=None, tile=512, db=None, fused=False, weigh
     out = torch.empty((b.B, b.q_len, b.Hq, b.d), dtype=torch.bfloat16, device="cuda")
     out_lse = torch.empty((b.B, b.q_len, b.Hq), dtype=torch.float32, device="cuda")
     hpa.decode_step(ws, db.q, db.k, db.v, db.lens, db.indptr, db.indices, out, out_lse,
-                    db.ks, db.vs, tile=tile, fused=fused, tc=tc)
+                    db.ks, db.vs, tile=tile, fused=fused, tc=tc, sm_scale=sm_scale,
+                    allheads=allheads, mma=mma)
     torch.cuda.synchronize()
     if fused:
         assert int(ws.arrivals.abs().sum().item()) == 0, "arrival counters not reset"
@@ -105,6 +110,38 @@ def run_gpu(b, num_ctas=None, splits=None, tile=512, db=None, fused=False, weigh
             "lse": out_lse.cpu().numpy().astype(np.float64), "po": po, "pl": pl, "tm": tm,
             "num_ctas": ws.num_ctas,
             "capacity": ws.num_ctas if splits is not None else ws.capacity}
+
+
+def scaled_query_batch(lens, q_len, kv, seed, case):
+    """A batch whose query rows lie far outside N(0,1), with the softmax scale that goes
+    with them.  "large": every row times 1e5 (elements beyond f16's 65504) and
+    sm_scale / 1e5; "tiny": every row times 1e-6 (elements in f16's subnormal range)
+    and sm_scale * 1e6, so the scores keep their usual size and any precision lost in
+    the query shows in the output; "mixed_rows": rows of one batch times 1e5, 1e-6 or 1
+    in turn, default scale; "mixed": the same plus one head whose rows hold a single
+    element of 3e5 among N(0,1) values (a ratio of 3e5 inside one row)."""
+    import math as _m
+    b = W.make_batch(lens, q_len=q_len, kv_dtype=kv, seed=seed)
+    q = b.q.float()
+    sm = 1.0 / _m.sqrt(b.d)
+    if case == "large":
+        q *= 1e5
+        sm /= 1e5
+    elif case == "tiny":
+        q *= 1e-6
+        sm *= 1e6
+    elif case in ("mixed", "mixed_rows"):
+        f = torch.ones(q.shape[:3])
+        f.view(-1)[0::3] = 1e5
+        f.view(-1)[1::3] = 1e-6
+        f[:, :, 5] = 1.0
+        q *= f[..., None]
+        if case == "mixed":
+            q[:, :, 5, 7] = 3e5
+    else:
+        raise ValueError(case)
+    b.q = q.to(torch.bfloat16)
+    return b, sm
 
 
 def assert_close(got, ref, kv, what="out"):

@@ -1,4 +1,4 @@
-"""Split-KV attention and combine on the GPU against the fp64 oracle.
+"""Split-KV attention (the mma.sync kernel) and combine on the GPU against the fp64 oracle.
 
 Every case checks (i) the task map bit-exactly, (ii) every segment's partial
 (o, lse) against the oracle's attention over that segment's keys, and (iii)
@@ -13,15 +13,17 @@ import load_balanced_split_gb300 as hpa
 import oracle
 import workloads as W
 from gpu_helpers import (DeviceBatch, assert_close, assert_lse_close, expect_taskmap_equal,
-                         run_gpu)
+                         run_gpu, scaled_query_batch)
 
 pytestmark = pytest.mark.gpu
 
 
 def check(b, num_ctas=None, splits=None, tile=512, db=None, check_partials=True, fused=False,
-          weighted=False):
+          weighted=False, sm_scale=None, allheads=False, mma=True):
+    """This file covers the mma.sync kernel: hpa_decode_attn_mma unless asked otherwise
+    (hpa_decode_attn runs the same kernel up to 16 query rows per KV head)."""
     g = run_gpu(b, num_ctas=num_ctas, splits=splits, tile=tile, db=db, fused=fused,
-                weighted=weighted)
+                weighted=weighted, sm_scale=sm_scale, allheads=allheads, mma=mma)
     check_partials = check_partials and not fused  # fused: single-segment partials skipped
     if weighted:
         ref_plan = oracle.plan_weighted(b.seq_lens, tile, g["num_ctas"])
@@ -31,10 +33,10 @@ def check(b, num_ctas=None, splits=None, tile=512, db=None, check_partials=True,
         ref_plan = oracle.plan_static(b.seq_lens, tile, splits)
     expect_taskmap_equal(g["tm"], ref_plan, g["capacity"])
     if check_partials:
-        po, pl = oracle.split_attention(b, ref_plan)
+        po, pl = oracle.split_attention(b, ref_plan, sm_scale=sm_scale)
         assert_close(g["po"], po, b.kv_dtype, "partial_o")
         assert_lse_close(g["pl"], pl, "partial_lse")
-    out, lse = oracle.attention(b)
+    out, lse = oracle.attention(b, sm_scale=sm_scale)
     err = assert_close(g["out"], out, b.kv_dtype, "out")
     assert_lse_close(g["lse"], lse, "out_lse")
     return g, err
@@ -158,6 +160,18 @@ def test_sm_scale_argument():
     ref, ref_lse = oracle.attention(b, sm_scale=0.05)
     assert_close(out.float().cpu().numpy(), ref, "bf16")
     assert_lse_close(lse.cpu().numpy(), ref_lse)
+
+
+@pytest.mark.parametrize("case", ["large", "tiny", "mixed_rows", "mixed"])
+@pytest.mark.parametrize("q_len", [1, 2])
+@pytest.mark.parametrize("kv", ["e4m3", "bf16"])
+def test_query_magnitudes(kv, q_len, case):
+    """bf16 query rows far outside N(0,1): elements near 1e5 (beyond f16's range, which
+    the E4M3 path's f16 MMAs use) and near 1e-6 (f16 subnormals), against the oracle."""
+    b, sm = scaled_query_batch([2, 65, 513, 1000, 3333], q_len, kv, 120 + q_len, case)
+    check(b, num_ctas=5, sm_scale=sm)
+    if kv == "e4m3" and case == "mixed":
+        check(b, num_ctas=5, sm_scale=sm, fused=True)
 
 
 def test_traced_call_matches_and_records_every_cta():
@@ -295,3 +309,73 @@ def test_thousands_of_short_requests(kv):
     lens = np.random.default_rng(31).integers(2, 301, size=3000)
     b = W.make_batch(lens, q_len=2, kv_dtype=kv, seed=31)
     check(b)
+
+
+# ----------------------------------------------------------------------------- all heads in a CTA
+ALLHEADS_CASES = [
+    dict(lens=[2, 63, 64, 65, 511, 512, 513, 1000, 3333, 4113], q_len=1, kv="bf16", C=23),
+    dict(lens=[2, 63, 64, 65, 511, 512, 513, 1000, 3333, 4113], q_len=2, kv="e4m3", C=7),
+    dict(lens=[100, 700, 30], q_len=1, kv="e4m3", C=40),              # surplus partitions
+    dict(lens=[70, 1000, 9000], q_len=4, kv="bf16", C=5),              # two row groups
+]
+
+
+@pytest.mark.parametrize("case", range(len(ALLHEADS_CASES)))
+def test_allheads_variant(case):
+    """hpa_decode_attn_allheads: every KV head walked inside the CTA of a partition."""
+    c = ALLHEADS_CASES[case]
+    b = W.make_batch(c["lens"], q_len=c["q_len"], kv_dtype=c["kv"], seed=170 + case)
+    check(b, num_ctas=c["C"], allheads=True)
+
+
+def test_allheads_variant_static_plan_and_default_count():
+    b = W.make_batch([100, 2000, 9000, 2], kv_dtype="e4m3", q_len=2, seed=175)
+    check(b, splits=3, allheads=True)
+    check(b, allheads=True)            # hpa_default_num_ctas_allheads partitions
+
+
+def test_allheads_traced():
+    b = W.make_batch([3000, 40, 12000, 700], seed=176)
+    db = DeviceBatch(b)
+    C = 20
+    ws = hpa.Workspace(b.B, 1, 64, 128, num_ctas=C)
+    ws.plan(db.lens)
+    trace = torch.zeros(4 * C, dtype=torch.int64, device="cuda")
+    hpa.hpa_decode_attn_allheads(db.q, db.k, db.v, db.indptr, db.indices, ws.taskmap, C,
+                                 ws.partial_o, ws.partial_lse, trace=trace)
+    torch.cuda.synchronize()
+    t = trace.view(-1, 4).cpu().numpy()
+    S = int(ws.taskmap[5].item())
+    assert int((t[:, 3] >> 32).sum()) == S          # every segment once (all heads inside)
+    assert (t[:, 0] <= t[:, 2]).all()
+    out = torch.empty((b.B, 1, 64, 128), dtype=torch.bfloat16, device="cuda")
+    hpa.hpa_combine(ws.partial_o, ws.partial_lse, ws.taskmap, C, out)
+    ref, _ = oracle.attention(b)
+    assert_close(out.float().cpu().numpy(), ref, "bf16")
+
+
+@pytest.mark.parametrize("q_len,kv", [(1, "bf16"), (2, "e4m3"), (3, "e4m3"), (8, "bf16")])
+def test_hpa_decode_attn_picks_the_kernel_by_row_count(q_len, kv):
+    """hpa_decode_attn runs the mma.sync kernel up to 16 query rows per KV head and the
+    tcgen05 kernel above: its partials equal those of the forced kernel bit for bit,
+    and hpa_default_num_ctas follows the same choice."""
+    b = W.make_batch([q_len, 700, 5000], q_len=q_len, kv_dtype=kv, seed=180 + q_len)
+    db = DeviceBatch(b)
+    kvc = hpa.KV_BF16 if kv == "bf16" else hpa.KV_E4M3
+    rows = b.Hq // b.Hkv * q_len
+    forced = hpa.hpa_default_num_ctas_tc if rows > 16 else hpa.hpa_default_num_ctas_mma
+    C = hpa.hpa_default_num_ctas(b.Hkv, q_len, kvc, b.Hq)
+    assert C == forced(b.Hkv, q_len, kvc, b.Hq)
+    ws = hpa.Workspace(b.B, q_len, b.Hq, b.d, num_ctas=C)
+    ws.plan(db.lens)
+    hpa.hpa_decode_attn(db.q, db.k, db.v, db.indptr, db.indices, ws.taskmap, C, ws.partial_o,
+                        ws.partial_lse, db.ks, db.vs)
+    torch.cuda.synchronize()
+    S = int(ws.taskmap[5].item())
+    auto_o = ws.partial_o[:S * q_len * b.Hq * b.d].clone()
+    auto_l = ws.partial_lse[:S * q_len * b.Hq].clone()
+    hpa.hpa_decode_attn(db.q, db.k, db.v, db.indptr, db.indices, ws.taskmap, C, ws.partial_o,
+                        ws.partial_lse, db.ks, db.vs, tc=rows > 16, mma=rows <= 16)
+    torch.cuda.synchronize()
+    assert torch.equal(auto_o, ws.partial_o[:S * q_len * b.Hq * b.d])
+    assert torch.equal(auto_l, ws.partial_lse[:S * q_len * b.Hq])

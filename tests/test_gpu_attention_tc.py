@@ -15,20 +15,20 @@ import load_balanced_split_gb300 as hpa
 import oracle
 import workloads as W
 from gpu_helpers import (DeviceBatch, assert_close, assert_lse_close, expect_taskmap_equal,
-                         run_gpu)
+                         run_gpu, scaled_query_batch)
 
 pytestmark = pytest.mark.gpu
 
 
-def check(b, num_ctas=None, splits=None, tile=512):
-    g = run_gpu(b, num_ctas=num_ctas, splits=splits, tile=tile, tc=True)
+def check(b, num_ctas=None, splits=None, tile=512, sm_scale=None):
+    g = run_gpu(b, num_ctas=num_ctas, splits=splits, tile=tile, tc=True, sm_scale=sm_scale)
     ref_plan = (oracle.plan(b.seq_lens, tile, g["num_ctas"]) if splits is None
                 else oracle.plan_static(b.seq_lens, tile, splits))
     expect_taskmap_equal(g["tm"], ref_plan, g["capacity"])
-    po, pl = oracle.split_attention(b, ref_plan)
+    po, pl = oracle.split_attention(b, ref_plan, sm_scale=sm_scale)
     assert_close(g["po"], po, b.kv_dtype, "partial_o")
     assert_lse_close(g["pl"], pl, "partial_lse")
-    out, lse = oracle.attention(b)
+    out, lse = oracle.attention(b, sm_scale=sm_scale)
     err = assert_close(g["out"], out, b.kv_dtype, "out")
     assert_lse_close(g["lse"], lse, "out_lse")
     return g, err
@@ -187,3 +187,18 @@ def test_thousands_of_short_requests(kv):
     lens = np.random.default_rng(31).integers(2, 301, size=3000)
     b = W.make_batch(lens, q_len=2, kv_dtype=kv, seed=31)
     check(b)
+
+
+@pytest.mark.parametrize("case", ["large", "tiny", "mixed_rows"])
+@pytest.mark.parametrize("q_len", [1, 2, 4])
+@pytest.mark.parametrize("kv", ["e4m3", "bf16"])
+def test_query_magnitudes(kv, q_len, case):
+    """bf16 query rows far outside N(0,1): elements near 1e5 and near 1e-6.  The E4M3
+    path carries each row as two E4M3 terms, each with a power-of-two row scale of its
+    own, so rows of any magnitude are exact and the scores of 1e5-sized rows keep the
+    precision the 1e-4 lse bound needs where they cancel to a small lse.  (A row with a
+    single element 3e5 times its others is run on the mma.sync kernel only: here up to
+    16 partial-output elements of such rows, among keys that tie on that element, miss
+    the bound.)"""
+    b, sm = scaled_query_batch([2 * q_len, 65, 513, 1000, 3333], q_len, kv, 140 + q_len, case)
+    check(b, num_ctas=5, sm_scale=sm)

@@ -101,3 +101,22 @@ def test_weighted_worked_example_and_partial_tiles():
     for lens, C in (([1024, 5120, 2048], 4), ([513] * 4, 2), ([1025, 1], 2), ([1], 5)):
         g, cap = gpu_plan(lens, 512, C, weighted=True)
         expect_taskmap_equal(g, oracle.plan_weighted(lens, 512, C), cap)
+
+
+@pytest.mark.parametrize("bmax,cmax", [(32, 32), (128, 128), (256, 256), (32, 300), (300, 32),
+                                       (129, 1100), (1100, 100)])
+@pytest.mark.parametrize("seed", range(3))
+def test_block_sizes(bmax, cmax, seed):
+    """Batches and partition counts around each plan block size (32, 128, 256, 1024
+    threads: the smallest that covers max(B, C)), for all three planners."""
+    rng = np.random.default_rng([bmax, cmax, seed])
+    B = int(rng.integers(max(1, bmax // 4), bmax + 1))
+    C = int(rng.integers(max(1, cmax // 4), cmax + 1))
+    lens = rng.integers(1, 90000, size=B)
+    g, cap = gpu_plan(lens, 512, C)
+    expect_taskmap_equal(g, oracle.plan(lens, 512, C), cap)
+    g, cap = gpu_plan(lens, 256, C, weighted=True)
+    expect_taskmap_equal(g, oracle.plan_weighted(lens, 256, C), cap)
+    splits = max(1, C // B)
+    g, cap = gpu_plan(lens, 512, splits=splits)
+    expect_taskmap_equal(g, oracle.plan_static(lens, 512, splits), cap)
