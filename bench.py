@@ -164,7 +164,10 @@ def run_ours(args, rank, world, local_rank):
     default_c = (hpa.hpa_default_num_ctas_tc if tc else
                  hpa.hpa_default_num_ctas_allheads if allh else
                  hpa.hpa_default_num_ctas_mma if mma else hpa.hpa_default_num_ctas)
-    C = args.num_ctas or b.num_ctas or default_c(b.Hkv, b.q_len, kv, b.Hq)
+    if args.num_ctas == 0:        # the device default, even where the workload fixes a count
+        C = default_c(b.Hkv, b.q_len, kv, b.Hq)
+    else:
+        C = args.num_ctas or b.num_ctas or default_c(b.Hkv, b.q_len, kv, b.Hq)
     groups = (b.Hq // b.Hkv * b.q_len + 15) // 16  # query-row groups per (partition, head)
     q = b.q.to(dev)
     k, v = b.k_pool.to(dev), b.v_pool.to(dev)
@@ -454,7 +457,8 @@ def main():
     ap.add_argument("--plan", default="tiles", choices=["tiles", "weighted"],
                     help="tile budgets (the pages' method) or the token-weighted variant")
     ap.add_argument("--num-ctas", type=int, default=None,
-                    help="partitions per KV head (default: the device default)")
+                    help="partitions per KV head (default: the workload's own count, else the "
+                         "device default; 0: the device default)")
     ap.add_argument("--attn", default="auto", choices=["auto", "mma", "tc", "allheads"],
                     help="attention kernel: hpa_decode_attn's own choice by query rows per KV "
                          "head (auto), mma.sync (hpa_decode_attn_mma), tcgen05 "

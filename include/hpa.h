@@ -218,10 +218,10 @@ int hpa_decode_attn_mma(const void *q_dev, const void *k_pool_dev, const void *v
  * num_ctas x Hkv: one CTA covers all G * q_len query rows of its KV head
  * (up to 64) in a single pass over the keys, where hpa_decode_attn makes one
  * pass per group of 16 rows.  It pays for MTP with more than 16 rows per KV
- * head (on the E4M3 MTP workload at 64/8 heads: 1.4x at q_len 3-4, 1.85x
- * at q_len 6, 1.37x at q_len 8).  With up to 16 rows, or with many short
- * segments per partition (hundreds of short requests), hpa_decode_attn is as
- * fast or faster.
+ * head, and hpa_decode_attn runs it there (on the E4M3 MTP workload at 64/8
+ * heads: 1.7x the mma.sync kernel at q_len 3-4, 1.8x at q_len 6, 1.4x at
+ * q_len 8).  With up to 16 rows, or with many short segments per partition
+ * (hundreds of short requests), the mma.sync kernel is as fast or faster.
  * Arguments, layouts, supported shapes, outputs and errors are exactly those
  * of hpa_decode_attn; the partials feed hpa_combine unchanged.  E4M3 pages
  * enter the MMA as 8-bit operands; the query rows and the probabilities are

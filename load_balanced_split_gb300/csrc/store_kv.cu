@@ -3,8 +3,9 @@
 // Quant + Store KV": the element-wise chain after the QKV projection, fused so
 // the new keys and values go from registers straight into the low-bit cache).
 //
-// One warp per (request r, new token j), four KV heads at a time (8 lanes per
-// head, 16 dims per lane).  For the key: rotate-half RoPE with the caller's
+// Warps walk (token, chunk of 8 KV heads) items, double-buffering each item's
+// raw K and V rows in shared memory with asynchronous copies; four KV heads at
+// a time (8 lanes per head, 16 dims per lane).  For the key: rotate-half RoPE with the caller's
 // cos/sin table, RMSNorm over the 128 dims, optional orthonormal Walsh-Hadamard
 // transform, then E4M3 codes of x / scale (round to nearest even, saturating)
 // or bf16.  The value is only converted.  Token j of request r is written at
@@ -25,7 +26,6 @@ constexpr uint32_t kFull = 0xffffffffu;
 constexpr int kLanesPerHead = 8;
 constexpr int kHeadsPerPass = 32 / kLanesPerHead;
 
-constexpr int kPasses = 2;  // passes of 4 heads whose rows are loaded together
 
 __device__ __forceinline__ void unpack16(const uint4 (&raw)[2], float (&x)[16]) {
   const uint4 a = raw[0], b = raw[1];
@@ -38,25 +38,24 @@ __device__ __forceinline__ void unpack16(const uint4 (&raw)[2], float (&x)[16]) 
   }
 }
 
-// x[0..7] -> dims 8k.., x[8..15] -> dims 64 + 8k.. of pool row `row`.
+// scale * x[0..7] -> dims 8k.., scale * x[8..15] -> dims 64 + 8k.. of pool row `row`
+// (bf16, or E4M3 codes: round to nearest even, saturating).
 __device__ __forceinline__ void store16(void *pool, int kv_dtype, int64_t row, int k,
-                                        const float (&x)[16], float inv_scale) {
+                                        const float (&x)[16], float scale) {
   if (kv_dtype == HPA_KV_BF16) {
     __nv_bfloat16 *base = static_cast<__nv_bfloat16 *>(pool) + row * HEAD_DIM;
-    uint4 a, b;
-    a.x = pack_bf16(x[0], x[1]), a.y = pack_bf16(x[2], x[3]);
-    a.z = pack_bf16(x[4], x[5]), a.w = pack_bf16(x[6], x[7]);
-    b.x = pack_bf16(x[8], x[9]), b.y = pack_bf16(x[10], x[11]);
-    b.z = pack_bf16(x[12], x[13]), b.w = pack_bf16(x[14], x[15]);
-    reinterpret_cast<uint4 *>(base + 8 * k)[0] = a;
-    reinterpret_cast<uint4 *>(base + 64 + 8 * k)[0] = b;
+    uint32_t w[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) w[i] = pack_bf16(x[2 * i] * scale, x[2 * i + 1] * scale);
+    reinterpret_cast<uint4 *>(base + 8 * k)[0] = make_uint4(w[0], w[1], w[2], w[3]);
+    reinterpret_cast<uint4 *>(base + 64 + 8 * k)[0] = make_uint4(w[4], w[5], w[6], w[7]);
   } else {
     uint8_t *base = static_cast<uint8_t *>(pool) + row * HEAD_DIM;
     uint32_t q[4];
 #pragma unroll
     for (int i = 0; i < 4; ++i) {
-      const uint32_t lo = f32x2_to_e4m3x2(x[4 * i] * inv_scale, x[4 * i + 1] * inv_scale);
-      const uint32_t hi = f32x2_to_e4m3x2(x[4 * i + 2] * inv_scale, x[4 * i + 3] * inv_scale);
+      const uint32_t lo = f32x2_to_e4m3x2(x[4 * i] * scale, x[4 * i + 1] * scale);
+      const uint32_t hi = f32x2_to_e4m3x2(x[4 * i + 2] * scale, x[4 * i + 3] * scale);
       q[i] = lo | (hi << 16);
     }
     reinterpret_cast<uint2 *>(base + 8 * k)[0] = make_uint2(q[0], q[1]);
@@ -65,9 +64,13 @@ __device__ __forceinline__ void store16(void *pool, int kv_dtype, int64_t row, i
 }
 
 // RoPE + RMSNorm + (Hadamard) of one key row, 16 dims in this lane (see above).
-__device__ __forceinline__ void key_transform(float (&y)[16], const float (&c)[8],
-                                              const float (&sn)[8], const float (&w)[16],
-                                              float eps, int use_hadamard) {
+// The row's scalar factors -- 1 / rms, and 1 / sqrt(128) with the transform -- are
+// linear and common to the row, so they are not applied here: y leaves as
+// H (w * rope(x)) (or w * rope(x)), and the returned factor is applied once, with the
+// cache scale, where the row is stored.
+__device__ __forceinline__ float key_transform(float (&y)[16], const float (&c)[8],
+                                               const float (&sn)[8], const float (&w)[16],
+                                               float eps, int use_hadamard) {
 #pragma unroll
   for (int i = 0; i < 8; ++i) {  // rotate-half RoPE: (y_i, y_{i+64}) turned by angle i
     const float lo = y[i], hi = y[8 + i];
@@ -80,10 +83,10 @@ __device__ __forceinline__ void key_transform(float (&y)[16], const float (&c)[8
   ss += __shfl_xor_sync(kFull, ss, 1);
   ss += __shfl_xor_sync(kFull, ss, 2);
   ss += __shfl_xor_sync(kFull, ss, 4);
-  const float inv = rsqrtf(ss / HEAD_DIM + eps);
+  float f = rsqrtf(ss / HEAD_DIM + eps);
 #pragma unroll
-  for (int i = 0; i < 16; ++i) y[i] *= inv * w[i];
-  if (!use_hadamard) return;
+  for (int i = 0; i < 16; ++i) y[i] *= w[i];
+  if (!use_hadamard) return f;
   // orthonormal Walsh-Hadamard transform, Sylvester order: a butterfly
   // (a, b) -> (a + b, a - b) over every dim bit; in-register bits 0-2 and 6
 #pragma unroll
@@ -99,20 +102,61 @@ __device__ __forceinline__ void key_transform(float (&y)[16], const float (&c)[8
   const int lane = threadIdx.x & 31;
 #pragma unroll
   for (int m = 1; m < kLanesPerHead; m <<= 1) {  // dim bits 3-5: partner lane ^ m
-    const bool up = lane & m;
+    // the lane holding a keeps a + b, the one holding b gets a - b: partner + sign * own
+    const float sgn = (lane & m) ? -1.f : 1.f;
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const float p = __shfl_xor_sync(kFull, y[i], m);
-      y[i] = up ? p - y[i] : y[i] + p;
-    }
+    for (int i = 0; i < 16; ++i) y[i] = fmaf(sgn, y[i], __shfl_xor_sync(kFull, y[i], m));
   }
-  const float n = 0.08838834764831845f;  // 1 / sqrt(128)
-#pragma unroll
-  for (int i = 0; i < 16; ++i) y[i] *= n;
+  return f * 0.08838834764831845f;  // 1 / sqrt(128)
 }
 
-// One warp per new token (r, j): the position, page and RoPE row are looked up
-// once and shared by the token's KV heads, four heads per pass.
+// 16-byte asynchronous global -> shared copies (cp.async), grouped per token.
+__device__ __forceinline__ void cp_async16(uint32_t dst, const void *src) {
+  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(dst), "l"(src) : "memory");
+}
+__device__ __forceinline__ void cp_async_commit() {
+  asm volatile("cp.async.commit_group;" ::: "memory");
+}
+__device__ __forceinline__ void cp_async_wait_1() {
+  asm volatile("cp.async.wait_group 1;" ::: "memory");
+}
+
+// An item is one new token (r, j) and a chunk of up to 8 of its KV heads; each
+// warp keeps two items' raw K and V rows in its own shared-memory slots (4 KB
+// each), so the next item's rows stream in while this one's page lookup and
+// arithmetic run.
+constexpr int kChunkHeads = 8;
+constexpr int kSlotBytes = kChunkHeads * HEAD_DIM * 2 * 2;  // K then V, bf16
+constexpr int kWarpSmem = 2 * kSlotBytes;
+
+struct Item {
+  int64_t rj;  // token index r * q_len + j
+  int hc;      // first head of the chunk
+  int nh;      // heads in the chunk
+};
+
+__device__ __forceinline__ Item item_at(int64_t it, int n_chunks, int Hkv) {
+  Item x;
+  x.rj = it / n_chunks;
+  x.hc = static_cast<int>(it % n_chunks) * kChunkHeads;
+  x.nh = min(kChunkHeads, Hkv - x.hc);
+  return x;
+}
+
+// Issue the copies of an item's K and V rows (nh * 256 bytes each) into a slot.
+__device__ __forceinline__ void fetch_item(const Item &x, const __nv_bfloat16 *k_new,
+                                           const __nv_bfloat16 *v_new, int Hkv, uint32_t slot,
+                                           int lane) {
+  const int64_t src = (x.rj * Hkv + x.hc) * HEAD_DIM;
+  const int chunks = x.nh * (HEAD_DIM * 2 / 16);  // 16-byte chunks per tensor
+  for (int c = lane; c < chunks; c += 32) {
+    cp_async16(slot + 16 * c, k_new + src + 8 * c);
+    cp_async16(slot + kSlotBytes / 2 + 16 * c, v_new + src + 8 * c);
+  }
+}
+
+// Warps walk the items grid-stride; each holds its next item's rows in flight
+// (one cp.async group) while it works on the current one.
 __global__ void __launch_bounds__(kWarps * 32, 2)
     store_kv_kernel(const __nv_bfloat16 *__restrict__ k_new,
                     const __nv_bfloat16 *__restrict__ v_new, const int32_t *__restrict__ seq_lens,
@@ -123,51 +167,19 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
                     const float *__restrict__ k_scale, const float *__restrict__ v_scale,
                     void *k_pool, void *v_pool, int B, int q_len, int Hkv,
                     int32_t *__restrict__ status) {
-  const int lane = threadIdx.x & 31;
+  extern __shared__ __align__(16) uint8_t kv_smem[];
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const int k = lane % kLanesPerHead, hp = lane / kLanesPerHead;
-  const int64_t rj = static_cast<int64_t>(blockIdx.x) * kWarps + (threadIdx.x >> 5);
-  if (rj >= static_cast<int64_t>(B) * q_len) return;
-  const int r = static_cast<int>(rj / q_len), j = static_cast<int>(rj % q_len);
-  const int64_t src0 = rj * Hkv * HEAD_DIM;
-  // raw bf16 rows of this lane's heads, kPasses x 4 heads per block, loaded before
-  // they are needed so a token's K and V (4 KB for 8 heads) is in flight at once
-  uint4 kraw[kPasses][2], vraw[kPasses][2];
-  auto load_block = [&](int hb) {
-#pragma unroll
-    for (int ps = 0; ps < kPasses; ++ps) {
-      const int h = hb + ps * kHeadsPerPass + hp;
-      if (h < Hkv) {
-        const __nv_bfloat16 *kr = k_new + src0 + static_cast<int64_t>(h) * HEAD_DIM;
-        const __nv_bfloat16 *vr = v_new + src0 + static_cast<int64_t>(h) * HEAD_DIM;
-        kraw[ps][0] = reinterpret_cast<const uint4 *>(kr + 8 * k)[0];
-        kraw[ps][1] = reinterpret_cast<const uint4 *>(kr + 64 + 8 * k)[0];
-        vraw[ps][0] = reinterpret_cast<const uint4 *>(vr + 8 * k)[0];
-        vraw[ps][1] = reinterpret_cast<const uint4 *>(vr + 64 + 8 * k)[0];
-      }
-    }
-  };
-  load_block(0);  // independent of the page lookup below
+  const uint32_t slots = smem_u32(kv_smem + warp * kWarpSmem);
+  const int n_chunks = (Hkv + kChunkHeads - 1) / kChunkHeads;
+  const int64_t n_items = static_cast<int64_t>(B) * q_len * n_chunks;
+  const int64_t stride = static_cast<int64_t>(gridDim.x) * kWarps;
+  int64_t it = static_cast<int64_t>(blockIdx.x) * kWarps + warp;
+  if (it >= n_items) return;
 
-  const int pos = seq_lens[r] - q_len + j;
-  if (pos < 0 || pos >= max_pos) {
-    if (lane == 0 && status) atomicOr(reinterpret_cast<int *>(status), HPA_STATUS_BAD_SEQLEN);
-    return;
-  }
-  const int pi = page_indptr[r] + pos / PAGE;
-  const int page = pi < page_indptr[r + 1] ? page_indices[pi] : -1;
-  if (page < 0 || page >= num_pages) {
-    if (lane == 0 && status) atomicOr(reinterpret_cast<int *>(status), HPA_STATUS_BAD_PAGE);
-    return;
-  }
-  float c[8], sn[8], w[16];
+  // RMSNorm weights of this lane's 16 dims (the same for every item)
+  float w[16];
   {
-    const float4 *cs = reinterpret_cast<const float4 *>(cos_sin + static_cast<int64_t>(pos) * HEAD_DIM);
-    const float4 c0 = cs[2 * k], c1 = cs[2 * k + 1];             // cos of dims 8k..8k+7
-    const float4 s0 = cs[16 + 2 * k], s1 = cs[16 + 2 * k + 1];   // sin of the same
-    const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-    const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-    for (int i = 0; i < 8; ++i) c[i] = cc[i], sn[i] = ss[i];
     const float4 *wv = reinterpret_cast<const float4 *>(norm_w);
     const float4 w0 = wv[2 * k], w1 = wv[2 * k + 1], w2 = wv[16 + 2 * k], w3 = wv[16 + 2 * k + 1];
     const float ww[16] = {w0.x, w0.y, w0.z, w0.w, w1.x, w1.y, w1.z, w1.w,
@@ -176,36 +188,108 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     for (int i = 0; i < 16; ++i) w[i] = ww[i];
   }
   const bool e4m3 = kv_dtype == HPA_KV_E4M3;
-  for (int hb = 0; hb < Hkv; hb += kPasses * kHeadsPerPass) {
-    if (hb > 0) load_block(hb);
+  Item cur = item_at(it, n_chunks, Hkv);
+  fetch_item(cur, k_new, v_new, Hkv, slots, lane);
+  cp_async_commit();
+  for (int buf = 0; it < n_items; it += stride, buf ^= 1) {
+    // next item's rows into the other slot (an empty group when there is none)
+    const int64_t nx = it + stride;
+    Item nxt = cur;
+    if (nx < n_items) {
+      nxt = item_at(nx, n_chunks, Hkv);
+      fetch_item(nxt, k_new, v_new, Hkv, slots + (buf ^ 1) * kSlotBytes, lane);
+    }
+    cp_async_commit();
+
+    // position, page and RoPE row of the current token (shared by its heads)
+    const int r = static_cast<int>(cur.rj / q_len), j = static_cast<int>(cur.rj % q_len);
+    const int pos = seq_lens[r] - q_len + j;
+    bool good = pos >= 0 && pos < max_pos;
+    int page = -1;
+    if (good) {
+      const int pi = page_indptr[r] + pos / PAGE;
+      page = pi < page_indptr[r + 1] ? page_indices[pi] : -1;
+    }
+    if (lane == 0 && status && cur.hc == 0) {
+      if (!good) atomicOr(reinterpret_cast<int *>(status), HPA_STATUS_BAD_SEQLEN);
+      else if (page < 0 || page >= num_pages) atomicOr(reinterpret_cast<int *>(status), HPA_STATUS_BAD_PAGE);
+    }
+    good = good && page >= 0 && page < num_pages;
+    float c[8], sn[8];
+    if (good) {
+      const float4 *cs = reinterpret_cast<const float4 *>(cos_sin + static_cast<int64_t>(pos) * HEAD_DIM);
+      const float4 c0 = cs[2 * k], c1 = cs[2 * k + 1];            // cos of dims 8k..8k+7
+      const float4 s0 = cs[16 + 2 * k], s1 = cs[16 + 2 * k + 1];  // sin of the same
+      const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
+      const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
 #pragma unroll
-  for (int ps = 0; ps < kPasses; ++ps) {
-    const int h = hb + ps * kHeadsPerPass + hp;
-    const bool active = h < Hkv;  // lanes of a missing head still take the shuffles
-    float y[16], x[16];
-    if (active) {
-      unpack16(kraw[ps], y);
-      unpack16(vraw[ps], x);
+      for (int i = 0; i < 8; ++i) c[i] = cc[i], sn[i] = ss[i];
     } else {
 #pragma unroll
-      for (int i = 0; i < 16; ++i) y[i] = x[i] = 0.f;
+      for (int i = 0; i < 8; ++i) c[i] = sn[i] = 0.f;
     }
-    key_transform(y, c, sn, w, eps, use_hadamard);
-    if (active) {
-      const int64_t row = (static_cast<int64_t>(page) * Hkv + h) * PAGE + pos % PAGE;
-      store16(k_pool, kv_dtype, row, k, y, e4m3 ? 1.f / k_scale[h] : 1.f);
-      store16(v_pool, kv_dtype, row, k, x, e4m3 ? 1.f / v_scale[h] : 1.f);  // value: converted only
+    cp_async_wait_1();  // this item's group has landed (the next one may still fly)
+    __syncwarp();
+    const uint32_t slot = slots + buf * kSlotBytes;
+    if (good) {
+#pragma unroll
+      for (int ps = 0; ps < kChunkHeads / kHeadsPerPass; ++ps) {
+        const int hh = ps * kHeadsPerPass + hp;  // head within the chunk
+        const bool active = hh < cur.nh;  // lanes of a missing head still take the shuffles
+        float y[16], x[16];
+        if (active) {
+          uint4 kr[2], vr[2];
+          const uint32_t ka = slot + hh * (HEAD_DIM * 2) + 16 * k;
+          lds128(ka, kr[0].x, kr[0].y, kr[0].z, kr[0].w);
+          lds128(ka + 128, kr[1].x, kr[1].y, kr[1].z, kr[1].w);
+          lds128(ka + kSlotBytes / 2, vr[0].x, vr[0].y, vr[0].z, vr[0].w);
+          lds128(ka + kSlotBytes / 2 + 128, vr[1].x, vr[1].y, vr[1].z, vr[1].w);
+          unpack16(kr, y);
+          unpack16(vr, x);
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) y[i] = x[i] = 0.f;
+        }
+        const float fk = key_transform(y, c, sn, w, eps, use_hadamard);
+        if (active) {
+          const int h = cur.hc + hh;
+          const int64_t row = (static_cast<int64_t>(page) * Hkv + h) * PAGE + pos % PAGE;
+          store16(k_pool, kv_dtype, row, k, y, e4m3 ? fk / k_scale[h] : fk);
+          store16(v_pool, kv_dtype, row, k, x, e4m3 ? 1.f / v_scale[h] : 1.f);  // value: converted only
+        }
+      }
     }
+    __syncwarp();  // every lane is done with this slot before it is refilled
+    cur = nxt;
   }
-  }
+  cp_async_wait_1();  // nothing of this warp's is left landing in shared memory
 }
 
 }  // namespace
 
 cudaError_t launch_store_kv(const StoreKvParams &p, cudaStream_t s) {
-  const int64_t items = static_cast<int64_t>(p.B) * p.q_len;  // one warp per new token
-  const unsigned blocks = static_cast<unsigned>((items + kWarps - 1) / kWarps);
-  store_kv_kernel<<<blocks, kWarps * 32, 0, s>>>(
+  static int configured[64] = {0};
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  constexpr int kSmem = kWarps * kWarpSmem;  // 64 KB: two 4 KB slots per warp
+  if (dev < 64 && !configured[dev]) {
+    e = cudaFuncSetAttribute(store_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+    if (e != cudaSuccess) return e;
+    configured[dev] = 1;
+  }
+  int sms = 0, per_sm = 0;
+  e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (e == cudaSuccess)
+    e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, store_kv_kernel, kWarps * 32, kSmem);
+  if (e != cudaSuccess) return e;
+  // one resident wave of warps that walk the items grid-stride
+  const int64_t n_items = static_cast<int64_t>(p.B) * p.q_len *
+                          ((p.Hkv + kChunkHeads - 1) / kChunkHeads);
+  const int64_t want = (n_items + kWarps - 1) / kWarps;
+  const int64_t wave = static_cast<int64_t>(sms) * (per_sm > 0 ? per_sm : 1);
+  const unsigned blocks = static_cast<unsigned>(want < wave ? want : wave);
+  store_kv_kernel<<<blocks, kWarps * 32, kSmem, s>>>(
       p.k_new, p.v_new, p.seq_lens, p.page_indptr, p.page_indices, p.num_pages, p.cos_sin,
       p.max_pos, p.norm_w, p.eps, p.use_hadamard, p.kv_dtype, p.k_scale, p.v_scale, p.k_pool,
       p.v_pool, p.B, p.q_len, p.Hkv, p.status);

@@ -43,9 +43,9 @@ def _e4m3_ok(got, x):
     return np.where(sat, got == np.sign(x) * 448.0, ok)
 
 
-def _run(lens, q_len, kv, hadamard, seed):
-    b = W.make_batch(lens, q_len=q_len, kv_dtype=kv, seed=seed)
-    fi = W.make_feeder_inputs(seed, b.B, q_len, max_pos=int(max(lens)) + 1)
+def _run(lens, q_len, kv, hadamard, seed, Hkv=8):
+    b = W.make_batch(lens, q_len=q_len, kv_dtype=kv, seed=seed, Hq=8 * Hkv, Hkv=Hkv)
+    fi = W.make_feeder_inputs(seed, b.B, q_len, max_pos=int(max(lens)) + 1, Hkv=Hkv)
     db = DeviceBatch(b)
     k0, v0 = db.k.clone(), db.v.clone()
     cs = torch.from_numpy(fi.cos_sin).cuda()
@@ -68,12 +68,7 @@ def _values(pool, kv):
     return pool.view(torch.float8_e4m3fn).float().cpu().numpy().astype(np.float64)
 
 
-@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
-@pytest.mark.parametrize("hadamard", [True, False])
-@pytest.mark.parametrize("q_len", [1, 2, 4])
-def test_store_kv_matches_oracle(kv, hadamard, q_len):
-    lens = [q_len, 64, 65, 513, 3000, 131072]
-    b, db, k0, v0, ref = _run(lens, q_len, kv, hadamard, seed=q_len + 10 * hadamard)
+def _check_written(db, k0, v0, ref, kv):
     K, V = _values(db.k, kv), _values(db.v, kv)
     ok = _bf16_ok if kv == "bf16" else _e4m3_ok
     written = np.zeros(K.shape[:3], bool)
@@ -88,6 +83,29 @@ def test_store_kv_matches_oracle(kv, hadamard, q_len):
     same_k = (K == k0v) | (np.isnan(K) & np.isnan(k0v))
     same_v = (V == v0v) | (np.isnan(V) & np.isnan(v0v))
     assert same_k[~written].all() and same_v[~written].all()
+
+
+@pytest.mark.parametrize("kv", ["bf16", "e4m3"])
+@pytest.mark.parametrize("hadamard", [True, False])
+@pytest.mark.parametrize("q_len", [1, 2, 4])
+def test_store_kv_matches_oracle(kv, hadamard, q_len):
+    lens = [q_len, 64, 65, 513, 3000, 131072]
+    b, db, k0, v0, ref = _run(lens, q_len, kv, hadamard, seed=q_len + 10 * hadamard)
+    _check_written(db, k0, v0, ref, kv)
+
+
+@pytest.mark.parametrize("Hkv,q_len", [(2, 3), (12, 2), (20, 1)])
+def test_store_kv_head_counts(Hkv, q_len):
+    """KV head counts that are not a multiple of the kernel's chunk of 8 heads."""
+    b, db, k0, v0, ref = _run([q_len, 700, 5000], q_len, "e4m3", True, seed=30 + Hkv, Hkv=Hkv)
+    _check_written(db, k0, v0, ref, "e4m3")
+
+
+def test_store_kv_many_tokens():
+    """4096 new tokens of one request: more (token, head chunk) items than resident
+    warps, so each warp walks several of them."""
+    b, db, k0, v0, ref = _run([6000], 4096, "bf16", True, seed=44)
+    _check_written(db, k0, v0, ref, "bf16")
 
 
 def test_store_then_attend():
