@@ -268,6 +268,21 @@ def run_ours(args, rank, world, local_rank):
 
     tail = traced_tail(ws)
 
+    def event_floor_us(reps=200):
+        """The same event bracket around a one-element fill (a launch that does almost
+        nothing): what any small kernel in the breakdown pays for its launch and events."""
+        dummy = torch.zeros(1, dtype=torch.int32, device=dev)
+        evs = [[torch.cuda.Event(enable_timing=True) for _ in range(2)] for _ in range(reps)]
+        with torch.cuda.stream(stream):
+            for e0, e1 in evs:
+                e0.record(stream)
+                dummy.fill_(0)
+                e1.record(stream)
+        torch.cuda.synchronize(dev)
+        return round(statistics.mean(e0.elapsed_time(e1) for e0, e1 in evs) * 1e3, 2)
+
+    floor_us = event_floor_us()
+
     # the same step with the combine folded into the attention launch (one kernel fewer)
     def fused_step(ev=None):
         hpa.decode_step(ws, q, k, v, lens, indptr, indices, out, out_lse, ks, vs, tile=b.tile,
@@ -344,7 +359,7 @@ def run_ours(args, rank, world, local_rank):
 
     feeder = None if args.no_feeder else feeder_measure(hpa, dev, stream, args, timed)
     return dict(b=b, C=C, ms=ms, attn=attn, plan=plan_ms, comb=comb_ms, step_ms=step_ms,
-                clocks=clocks, tail=tail,
+                clocks=clocks, tail=tail, floor_us=floor_us,
                 feeder=feeder,
                 fused_ms=fused_ms, comparator=comparator, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
 
@@ -525,7 +540,8 @@ def main():
         "pct_of_hbm_peak": round(100.0 * kv_bytes / (r["ms"] * 1e-3) / 1e9 / peak, 1),
         "breakdown_us": {"plan": round(statistics.mean(r["plan"]) * 1e3, 2),
                          "attention": round(attn_ms * 1e3, 2),
-                         "combine": round(statistics.mean(r["comb"]) * 1e3, 2)},
+                         "combine": round(statistics.mean(r["comb"]) * 1e3, 2),
+                         "event_floor": r["floor_us"]},
         "roofline": {"bound": "hbm", "achieved": round(achieved, 1), "peak": peak,
                      "unit": "GB/s", "frac": round(achieved / peak, 4), "traffic": traffic,
                      "kernel": kernel_name,

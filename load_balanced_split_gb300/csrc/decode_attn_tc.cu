@@ -110,8 +110,7 @@ struct TcSmem {
   static constexpr int kStages = kStages0 > kStageCap ? kStageCap : kStages0;
   static constexpr int kQ = kStages * kStageBytes;             // 2 query slots
   static constexpr int kRowC = kQ + 2 * kOperand;              // float[2][64] score scales
-  static constexpr int kRowLo = kRowC + 2 * 64 * 4;            // float[2][64] lo-term scales
-  static constexpr int kStepMax = kRowLo + 2 * 64 * 4;         // float[2][4][64]
+  static constexpr int kStepMax = kRowC + 2 * 64 * 4;          // float[2][4][64]
   static constexpr int kFlags = kStepMax + 2 * 4 * 64 * 4;     // int[2][16]
   static constexpr int kLRed = kFlags + 128;                   // float[4][64] row-sum parts
   static constexpr int kJRow = kLRed + 4 * 64 * 4;             // int[64]: token j of row r
@@ -308,7 +307,6 @@ struct Tc {
       // query rows -> operand slot (K-major, 128-byte swizzle); lane l holds dims 4l..4l+3
       uint8_t *qs = smem + S::kQ + slot * S::kOperand;
       float *rowc = reinterpret_cast<float *>(smem + S::kRowC) + slot * 64;
-      float *rowlo = reinterpret_cast<float *>(smem + S::kRowLo) + slot * 64;
       for (int row = 0; row < kRp; ++row) {
         float x[4] = {0.f, 0.f, 0.f, 0.f};
         if (row < R) {
@@ -328,11 +326,11 @@ struct Tc {
         } else {
           float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
           amax = warp_max(amax);
-          // A power-of-two row scale puts amax * sq in [128, 256) (hi = e4m3 of it), and the
-          // residuals x * sq - hi get a power-of-two scale of their own that puts their
-          // largest in [128, 256) too (lo = e4m3 of it), so hi + lo / st carries a bf16
-          // element to its 8 significant bits down to far below the row's largest (the
-          // residuals of small elements would otherwise fall under E4M3's smallest step).
+          // A power-of-two row scale puts amax * sq in [128, 256) (hi = e4m3 of it).  Every
+          // residual x * sq - hi is then at most half an E4M3 step of [128, 256), i.e. 8, so
+          // lo = e4m3(16 (x * sq - hi)) never saturates, and hi + lo / 16 carries a bf16
+          // element to its 8 significant bits down to 2^-12 of the row's largest (without
+          // the 16, residuals of small elements fall under E4M3's smallest step).
           const float sq = pow2_to_128(amax);
           uint32_t hi = 0, lo = 0;
           float res[4];
@@ -346,18 +344,12 @@ struct Tc {
             res[e + 1] = v1 - hf.y;
             hi |= static_cast<uint32_t>(h2) << (8 * e);
           }
-          const float rmax =
-              warp_max(fmaxf(fmaxf(fabsf(res[0]), fabsf(res[1])), fmaxf(fabsf(res[2]), fabsf(res[3]))));
-          const float st = pow2_to_128(rmax);
 #pragma unroll
           for (int e = 0; e < 4; e += 2)
-            lo |= static_cast<uint32_t>(f32x2_to_e4m3x2(res[e] * st, res[e + 1] * st)) << (8 * e);
+            lo |= static_cast<uint32_t>(f32x2_to_e4m3x2(16.f * res[e], 16.f * res[e + 1])) << (8 * e);
           *reinterpret_cast<uint32_t *>(qs + kmaj(row, 4 * lane, 0)) = hi;
           *reinterpret_cast<uint32_t *>(qs + kRp * 128 + kmaj(row, 4 * lane, 0)) = lo;
-          if (lane == 0) {
-            rowc[row] = p.scale_log2 * ksc / sq;
-            rowlo[row] = 1.f / st;  // a power of two: exact
-          }
+          if (lane == 0) rowc[row] = p.scale_log2 * ksc / sq;
         }
       }
       if (lane == 0)
@@ -594,14 +586,17 @@ struct Tc {
       const int nsteps = (pg1 - pg0 + S::kPPS - 1) / S::kPPS;
       if (L < q_len && t == 0) status_or(p.tm, HPA_STATUS_BAD_SEQLEN);
       const uint32_t rowc_s = base + S::kRowC + (slot * 64 + r0) * 4;
-      const uint32_t rowlo_s = base + S::kRowLo + (slot * 64 + r0) * 4;
       const float c_all = p.scale_log2;  // bf16: one score scale for every row
-      float mref[RH], lsum[RH];  // reference max per row; this key slot's share of l
+      // Per row: bo = (reference max) - kPOff, -inf until the row has a reference, and
+      // this key slot's share of l.  A probability is 2^(x - bo), x = c * S the score in
+      // base 2, so one FMA per element gives the exp2 argument a = c * S - bo.
+      float bo[RH], lsum[RH];
 #pragma unroll
       for (int e = 0; e < RH; ++e) {
-        mref[e] = -CUDART_INF_F;
+        bo[e] = -CUDART_INF_F;
         lsum[e] = 0.f;
       }
+      const bool full = r0 + RH <= R;  // every row of this warp is a query row (warp-uniform)
 
       for (int jp = 0; jp < nsteps; ++jp) {
         const int b = i & 1, st = i % S::kStages;
@@ -610,70 +605,75 @@ struct Tc {
           break;
         }
         tc_fence_after();
-        float x[MT][RH];
-#pragma unroll
-        for (int m = 0; m < MT; ++m)
-#pragma unroll
-          for (int c = 0; c < RH / 8; ++c) {
-            const uint32_t col = lane_t + (b * MT + m) * S::kNS + r0 + 8 * c;
-            float v[8];
-            tc_ld8(col, v);
-            if (KV == HPA_KV_E4M3) {  // S = S(Q hi) + S(Q lo) / st, st the lo term's row scale
-              float u[8], lo8[8];
-              tc_ld8(col + kRp, u);
-              uint32_t w[8];
-              lds128(rowlo_s + 32 * c, w[0], w[1], w[2], w[3]);
-              lds128(rowlo_s + 32 * c + 16, w[4], w[5], w[6], w[7]);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) lo8[e] = __uint_as_float(w[e]);
-#pragma unroll
-              for (int e = 0; e < 8; ++e) v[e] = fmaf(u[e], lo8[e], v[e]);
-            }
-#pragma unroll
-            for (int e = 0; e < 8; ++e) x[m][8 * c + e] = v[e];
-          }
-        tc_wait_ld();
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars + 8 * (B_S_FREE + b));
-
         const int key0 = (pg0 + S::kPPS * jp) * PAGE + kt;  // key of slot m: key0 + 128 m
         int d0[MT];
-        bool present[MT];
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
-          present[m] = key0 + 128 * m < pg1 * PAGE;  // the step's last pages may be missing
+          const bool present = key0 + 128 * m < pg1 * PAGE;  // the step's last pages may be missing
           // row r (token j = r / G) sees keys < L - q_len + 1 + j
-          d0[m] = present[m] ? key0 + 128 * m - (L - q_len + 1) : INT_MAX;
+          d0[m] = present ? key0 + 128 * m - (L - q_len + 1) : INT_MAX;
         }
-#pragma unroll
-        for (int e4 = 0; e4 < RH; e4 += 4) {
-          float c4[4] = {c_all, c_all, c_all, c_all};
-          if (KV == HPA_KV_E4M3) {  // per-row scale (the query rows' own power of two)
-            uint32_t w0, w1, w2, w3;
-            lds128(rowc_s + 4 * e4, w0, w1, w2, w3);
-            c4[0] = __uint_as_float(w0), c4[1] = __uint_as_float(w1);
-            c4[2] = __uint_as_float(w2), c4[3] = __uint_as_float(w3);
-          }
+        // a[m][e] = c_e * S - bias_e for this key slot and the warp's rows: -inf for keys a
+        // row may not see and for padding rows.  bias is bo, or 0 while computing the
+        // plain scores x (the rare path where a reference moves).
+        float a[MT][RH];
+        auto scores = [&](bool with_bias) {
 #pragma unroll
           for (int m = 0; m < MT; ++m)
 #pragma unroll
-            for (int e = 0; e < 4; ++e)
-              x[m][e4 + e] = r0 + e4 + e < R ? x[m][e4 + e] * c4[e] : -CUDART_INF_F;
-        }
+            for (int c = 0; c < RH / 8; ++c) {
+              const uint32_t col = lane_t + (b * MT + m) * S::kNS + r0 + 8 * c;
+              float v[8];
+              tc_ld8(col, v);
+              if (KV == HPA_KV_E4M3) {  // S = S(Q hi) + S(Q lo) / 16 (the lo term's fixed scale)
+                float u[8];
+                tc_ld8(col + kRp, u);
 #pragma unroll
-        for (int m = 0; m < MT; ++m)
-          if (__any_sync(kFull, d0[m] >= 0)) {  // near the request's end, or a missing page
+                for (int e = 0; e < 8; ++e) v[e] = fmaf(u[e], 0.0625f, v[e]);
+              }
 #pragma unroll
-            for (int e = 0; e < RH; ++e)
-              if (d0[m] >= jrow[r0 + e]) x[m][e] = -CUDART_INF_F;
+              for (int e = 0; e < 8; ++e) a[m][8 * c + e] = v[e];
+            }
+          tc_wait_ld();
+#pragma unroll
+          for (int e4 = 0; e4 < RH; e4 += 4) {
+            float c4[4] = {c_all, c_all, c_all, c_all};
+            if (KV == HPA_KV_E4M3) {  // per-row scale (the query rows' own power of two)
+              uint32_t w0, w1, w2, w3;
+              lds128(rowc_s + 4 * e4, w0, w1, w2, w3);
+              c4[0] = __uint_as_float(w0), c4[1] = __uint_as_float(w1);
+              c4[2] = __uint_as_float(w2), c4[3] = __uint_as_float(w3);
+            }
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+              for (int e = 0; e < 4; ++e)
+                a[m][e4 + e] = with_bias ? fmaf(a[m][e4 + e], c4[e], -bo[e4 + e])
+                                         : a[m][e4 + e] * c4[e];
           }
+          if (!full) {
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+              for (int e = 0; e < RH; ++e)
+                if (r0 + e >= R) a[m][e] = -CUDART_INF_F;
+          }
+#pragma unroll
+          for (int m = 0; m < MT; ++m)
+            if (__any_sync(kFull, d0[m] >= 0)) {  // near the request's end, or a missing page
+#pragma unroll
+              for (int e = 0; e < RH; ++e)
+                if (d0[m] >= jrow[r0 + e]) a[m][e] = -CUDART_INF_F;
+            }
+        };
+        scores(true);
+        // A reference moves only when some score exceeds it by more than the slack, i.e.
+        // when a > kSlack + kPOff (always, for a row with no reference yet: a = +inf).
         bool flag = false;
 #pragma unroll
         for (int m = 0; m < MT; ++m)
 #pragma unroll
-          for (int e = 0; e < RH; ++e) flag |= x[m][e] > mref[e] + kSlack;
-        // A reference max moves only when some score exceeds it by more than the slack.
+          for (int e = 0; e < RH; ++e) flag |= a[m][e] > kSlack + kPOff;
         // The 4 warps that share this warp's rows agree through an mbarrier of their own
         // (bounded waits, never named barriers: a warp that gives up must not leave the
         // others waiting without a limit).
@@ -692,12 +692,14 @@ struct Tc {
 #pragma unroll
         for (int x4 = 0; x4 < 4; ++x4) moved |= flags[b * 16 + 4 * hf + x4];
         if (moved) {
+          // S[b] is still this warp's (released below): read the plain scores x again
+          scores(false);
           float *sm = stepmax + (n_moved & 1) * 4 * 64;
 #pragma unroll
           for (int e = 0; e < RH; ++e) {
-            float v = x[0][e];
+            float v = a[0][e];
 #pragma unroll
-            for (int m = 1; m < MT; ++m) v = fmaxf(v, x[m][e]);
+            for (int m = 1; m < MT; ++m) v = fmaxf(v, a[m][e]);
             const float mx = warp_max(v);
             if (lane == 0) sm[qd * 64 + r0 + e] = mx;
           }
@@ -713,12 +715,17 @@ struct Tc {
 #pragma unroll
           for (int e = 0; e < RH; ++e) {
             const int r = r0 + e;
+            // new reference: the exact max of the row so far (never below the old one)
             const float mn = fmaxf(fmaxf(fmaxf(sm[r], sm[64 + r]), fmaxf(sm[128 + r], sm[192 + r])),
-                                   mref[e]);
-            alpha[e] = mn == mref[e] ? 1.f : exp2f(mref[e] - mn);  // 0 from -inf
+                                   bo[e] + kPOff);
+            const float bn = mn - kPOff;
+            alpha[e] = bn == bo[e] ? 1.f : exp2f(bo[e] - bn);  // 0 from -inf
             rescale |= alpha[e] != 1.f;
-            mref[e] = mn;
+            bo[e] = bn;
             lsum[e] *= alpha[e];
+            const float bsafe = bn == -CUDART_INF_F ? 0.f : bn;  // a row with no visible key yet
+#pragma unroll
+            for (int m = 0; m < MT; ++m) a[m][e] -= bsafe;
           }
           if (jp > 0 && __any_sync(kFull, rescale)) {
             // O holds the earlier steps of this segment: wait for the last P V, then
@@ -743,9 +750,12 @@ struct Tc {
                 tc_st8(col, o);
               }
             tc_wait_st();
-            tc_fence_before();
           }
         }
+        // S[b] may be overwritten by the Q K^T two steps on
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + 8 * (B_S_FREE + b));
         // Wait out the P V of two steps back.  P^T now lives in this step's own stage,
         // so no buffer depends on it; the wait keeps this thread's parity waits on
         // PV_DONE[b] in order (each of its uses waited, so a later parity wait cannot
@@ -768,9 +778,7 @@ struct Tc {
             uint32_t pw[RH / 2];  // rows (r0 + e, r0 + e + 1) in word e / 2
 #pragma unroll
             for (int e = 0; e < RH; e += 2) {
-              const float b0 = mref[e] == -CUDART_INF_F ? 0.f : mref[e];
-              const float b1 = mref[e + 1] == -CUDART_INF_F ? 0.f : mref[e + 1];
-              const float p0 = exp2f(x[m][e] - b0), p1 = exp2f(x[m][e + 1] - b1);
+              const float p0 = exp2f(a[m][e]), p1 = exp2f(a[m][e + 1]);
               lsum[e] += p0;
               lsum[e + 1] += p1;
               pw[e / 2] = pack_bf16(p0, p1);
@@ -787,10 +795,8 @@ struct Tc {
 #pragma unroll
               for (int e = 0; e < 4; e += 2) {
                 const int a0 = e4 + e;
-                const float b0 = mref[a0] == -CUDART_INF_F ? 0.f : mref[a0];
-                const float b1 = mref[a0 + 1] == -CUDART_INF_F ? 0.f : mref[a0 + 1];
-                const float p0 = exp2f(x[m][a0] - b0 + kPOff);
-                const float p1 = exp2f(x[m][a0 + 1] - b1 + kPOff);
+                const float p0 = exp2f(a[m][a0]);
+                const float p1 = exp2f(a[m][a0 + 1]);
                 lsum[a0] += p0;
                 lsum[a0 + 1] += p1;
                 // hi = e4m3(p), lo = e4m3(p - hi), the residual taken in f16 (exact there)
@@ -815,7 +821,7 @@ struct Tc {
             }
           }
           // V rows of keys past the request (or of a missing page) must be finite: zero them
-          if (hf == 0 && (!present[m] || key0 + 128 * m >= L)) {
+          if (hf == 0 && (key0 + 128 * m >= pg1 * PAGE || key0 + 128 * m >= L)) {
             uint8_t *vr = smem + st * S::kStageBytes + S::kKStep + (kk >> 3) * 1024 + (kk & 7) * 128;
             const int4 z = make_int4(0, 0, 0, 0);
 #pragma unroll
@@ -870,8 +876,7 @@ struct Tc {
                 p.partial_o[row * HEAD_DIM + kt] = l > 0.f ? o[e] / l * vsc : 0.f;
                 if (kt == 8 * c + e) {  // one thread per row writes its lse
                   p.partial_lse[row] =
-                      l > 0.f ? (mref[8 * c + e] - kPOff + log2f(l)) * 0.69314718055994531f
-                              : -CUDART_INF_F;
+                      l > 0.f ? (bo[8 * c + e] + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
                 }
               }
             }

@@ -179,6 +179,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
 
   // a4: segments per partition, their running sum, then the segment rows
   carry = 0;
+  int first_rf = 0, first_rl = -1;  // requests of partition tid, kept for the row pass
   for (int base = 0; base < C; base += kPlanThreads) {
     const int c = base + tid;
     long long cnt = 0;
@@ -188,6 +189,7 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
         const int rf = upper_bound(cu, B + 1, b) - 1;
         const int rl = upper_bound(cu, B + 1, e - 1) - 1;
         cnt = rl - rf + 1;
+        if (base == 0) first_rf = rf, first_rl = rl;
       }
     }
     const long long incl = block_scan<kPlanThreads>(cnt, wbuf, total);
@@ -204,8 +206,8 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
   for (int c = tid; c < C; c += kPlanThreads) {
     const int b = cb[c], e = cb[c + 1];
     if (e <= b) continue;
-    const int rf = upper_bound(cu, B + 1, b) - 1;
-    const int rl = upper_bound(cu, B + 1, e - 1) - 1;
+    const int rf = c == tid ? first_rf : upper_bound(cu, B + 1, b) - 1;
+    const int rl = c == tid ? first_rl : upper_bound(cu, B + 1, e - 1) - 1;
     int out = cs[c];
     for (int r = rf; r <= rl; ++r, ++out) {
       const int lo = (b > cu[r] ? b : cu[r]) - cu[r];

@@ -126,7 +126,9 @@ __device__ __forceinline__ void cp_async_wait_1() {
 // each), so the next item's rows stream in while this one's page lookup and
 // arithmetic run.
 constexpr int kChunkHeads = 8;
-constexpr int kSlotBytes = kChunkHeads * HEAD_DIM * 2 * 2;  // K then V, bf16
+constexpr int kRowsBytes = kChunkHeads * HEAD_DIM * 2 * 2;  // K then V, bf16
+constexpr int kCosOff = kRowsBytes;                         // then the token's cos/sin row
+constexpr int kSlotBytes = kRowsBytes + HEAD_DIM * 4;
 constexpr int kWarpSmem = 2 * kSlotBytes;
 
 struct Item {
@@ -151,8 +153,39 @@ __device__ __forceinline__ void fetch_item(const Item &x, const __nv_bfloat16 *k
   const int chunks = x.nh * (HEAD_DIM * 2 / 16);  // 16-byte chunks per tensor
   for (int c = lane; c < chunks; c += 32) {
     cp_async16(slot + 16 * c, k_new + src + 8 * c);
-    cp_async16(slot + kSlotBytes / 2 + 16 * c, v_new + src + 8 * c);
+    cp_async16(slot + kRowsBytes / 2 + 16 * c, v_new + src + 8 * c);
   }
+}
+
+// Where an item's token goes: its position, its page (or -1) and whether both are
+// valid; looked up one item ahead, when the item's rows are fetched.
+struct Place {
+  int pos, page;
+  bool good;
+};
+
+__device__ __forceinline__ Place look_up(const Item &x, const int32_t *seq_lens,
+                                         const int32_t *page_indptr,
+                                         const int32_t *page_indices, int64_t num_pages,
+                                         int max_pos, int q_len) {
+  Place pl;
+  const int r = static_cast<int>(x.rj / q_len), j = static_cast<int>(x.rj % q_len);
+  pl.pos = seq_lens[r] - q_len + j;
+  pl.page = -1;
+  if (pl.pos >= 0 && pl.pos < max_pos) {
+    const int pi = page_indptr[r] + pl.pos / PAGE;
+    pl.page = pi < page_indptr[r + 1] ? page_indices[pi] : -1;
+  }
+  pl.good = pl.pos >= 0 && pl.pos < max_pos && pl.page >= 0 && pl.page < num_pages;
+  return pl;
+}
+
+// The token's cos/sin row (HEAD_DIM floats) into the slot, one 16-byte chunk per lane.
+__device__ __forceinline__ void fetch_cos_sin(const Place &pl, const float *cos_sin,
+                                              uint32_t slot, int lane) {
+  if (pl.good)
+    cp_async16(slot + kCosOff + 16 * lane,
+               cos_sin + static_cast<int64_t>(pl.pos) * HEAD_DIM + 4 * lane);
 }
 
 // Warps walk the items grid-stride; each holds its next item's rows in flight
@@ -189,49 +222,46 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   }
   const bool e4m3 = kv_dtype == HPA_KV_E4M3;
   Item cur = item_at(it, n_chunks, Hkv);
+  Place here = look_up(cur, seq_lens, page_indptr, page_indices, num_pages, max_pos, q_len);
   fetch_item(cur, k_new, v_new, Hkv, slots, lane);
+  fetch_cos_sin(here, cos_sin, slots, lane);
   cp_async_commit();
   for (int buf = 0; it < n_items; it += stride, buf ^= 1) {
-    // next item's rows into the other slot (an empty group when there is none)
+    // next item: its rows, its place and its cos/sin row, into the other slot (an
+    // empty group when there is none)
     const int64_t nx = it + stride;
     Item nxt = cur;
+    Place there = here;
     if (nx < n_items) {
       nxt = item_at(nx, n_chunks, Hkv);
-      fetch_item(nxt, k_new, v_new, Hkv, slots + (buf ^ 1) * kSlotBytes, lane);
+      const uint32_t other = slots + (buf ^ 1) * kSlotBytes;
+      fetch_item(nxt, k_new, v_new, Hkv, other, lane);
+      there = look_up(nxt, seq_lens, page_indptr, page_indices, num_pages, max_pos, q_len);
+      fetch_cos_sin(there, cos_sin, other, lane);
     }
     cp_async_commit();
 
-    // position, page and RoPE row of the current token (shared by its heads)
-    const int r = static_cast<int>(cur.rj / q_len), j = static_cast<int>(cur.rj % q_len);
-    const int pos = seq_lens[r] - q_len + j;
-    bool good = pos >= 0 && pos < max_pos;
-    int page = -1;
-    if (good) {
-      const int pi = page_indptr[r] + pos / PAGE;
-      page = pi < page_indptr[r + 1] ? page_indices[pi] : -1;
-    }
-    if (lane == 0 && status && cur.hc == 0) {
-      if (!good) atomicOr(reinterpret_cast<int *>(status), HPA_STATUS_BAD_SEQLEN);
-      else if (page < 0 || page >= num_pages) atomicOr(reinterpret_cast<int *>(status), HPA_STATUS_BAD_PAGE);
-    }
-    good = good && page >= 0 && page < num_pages;
-    float c[8], sn[8];
-    if (good) {
-      const float4 *cs = reinterpret_cast<const float4 *>(cos_sin + static_cast<int64_t>(pos) * HEAD_DIM);
-      const float4 c0 = cs[2 * k], c1 = cs[2 * k + 1];            // cos of dims 8k..8k+7
-      const float4 s0 = cs[16 + 2 * k], s1 = cs[16 + 2 * k + 1];  // sin of the same
-      const float cc[8] = {c0.x, c0.y, c0.z, c0.w, c1.x, c1.y, c1.z, c1.w};
-      const float ss[8] = {s0.x, s0.y, s0.z, s0.w, s1.x, s1.y, s1.z, s1.w};
-#pragma unroll
-      for (int i = 0; i < 8; ++i) c[i] = cc[i], sn[i] = ss[i];
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) c[i] = sn[i] = 0.f;
-    }
+    // the current token: report a bad position or page once per token
+    const int pos = here.pos, page = here.page;
+    const bool good = here.good;
+    if (lane == 0 && status && cur.hc == 0 && !good)
+      atomicOr(reinterpret_cast<int *>(status), pos < 0 || pos >= max_pos ? HPA_STATUS_BAD_SEQLEN
+                                                                         : HPA_STATUS_BAD_PAGE);
     cp_async_wait_1();  // this item's group has landed (the next one may still fly)
     __syncwarp();
     const uint32_t slot = slots + buf * kSlotBytes;
     if (good) {
+      // cos of dims 8k..8k+7 (floats 8k..), sin of the same (floats 64 + 8k..)
+      float c[8], sn[8];
+      {
+        uint32_t w[16];
+        lds128(slot + kCosOff + 32 * k, w[0], w[1], w[2], w[3]);
+        lds128(slot + kCosOff + 32 * k + 16, w[4], w[5], w[6], w[7]);
+        lds128(slot + kCosOff + 256 + 32 * k, w[8], w[9], w[10], w[11]);
+        lds128(slot + kCosOff + 256 + 32 * k + 16, w[12], w[13], w[14], w[15]);
+#pragma unroll
+        for (int i = 0; i < 8; ++i) c[i] = __uint_as_float(w[i]), sn[i] = __uint_as_float(w[8 + i]);
+      }
 #pragma unroll
       for (int ps = 0; ps < kChunkHeads / kHeadsPerPass; ++ps) {
         const int hh = ps * kHeadsPerPass + hp;  // head within the chunk
@@ -242,8 +272,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
           const uint32_t ka = slot + hh * (HEAD_DIM * 2) + 16 * k;
           lds128(ka, kr[0].x, kr[0].y, kr[0].z, kr[0].w);
           lds128(ka + 128, kr[1].x, kr[1].y, kr[1].z, kr[1].w);
-          lds128(ka + kSlotBytes / 2, vr[0].x, vr[0].y, vr[0].z, vr[0].w);
-          lds128(ka + kSlotBytes / 2 + 128, vr[1].x, vr[1].y, vr[1].z, vr[1].w);
+          lds128(ka + kRowsBytes / 2, vr[0].x, vr[0].y, vr[0].z, vr[0].w);
+          lds128(ka + kRowsBytes / 2 + 128, vr[1].x, vr[1].y, vr[1].z, vr[1].w);
           unpack16(kr, y);
           unpack16(vr, x);
         } else {
@@ -261,6 +291,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     }
     __syncwarp();  // every lane is done with this slot before it is refilled
     cur = nxt;
+    here = there;
   }
   cp_async_wait_1();  // nothing of this warp's is left landing in shared memory
 }
