@@ -226,11 +226,11 @@ int hpa_decode_attn_mma(const void *q_dev, const void *k_pool_dev, const void *v
  * of hpa_decode_attn; the partials feed hpa_combine unchanged.  E4M3 pages
  * enter the MMA as 8-bit operands; the query rows and the probabilities are
  * each carried as two E4M3 terms (about 8 significant bits, as bf16).  Each
- * query row is scaled by a power of two and the residual term by another, so
- * rows of any bf16 magnitude are carried exactly as long as their elements
- * lie within about 2^-14 of the row's largest; smaller elements lose bits and
- * those below about 2^-21 of it are dropped (hpa_decode_attn keeps bf16
- * precision down to 2^-28).
+ * query row is scaled by a power of two (its largest element into [128, 256))
+ * and its residual term by a fixed 16, so rows of any bf16 magnitude are
+ * carried exactly as long as their elements lie within about 2^-12 of the
+ * row's largest; smaller elements lose bits and those below about 2^-21 of it
+ * are dropped (hpa_decode_attn_mma keeps bf16 precision down to 2^-28).
  */
 int hpa_decode_attn_tc(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
                        int32_t kv_dtype, const float *k_scale_dev, const float *v_scale_dev,
