@@ -114,7 +114,12 @@ struct TcSmem {
   static constexpr int kFlags = kStepMax + 2 * 4 * 64 * 4;     // int[2][16]
   static constexpr int kLRed = kFlags + 128;                   // float[4][64] row-sum parts
   static constexpr int kJRow = kLRed + 4 * 64 * 4;             // int[64]: token j of row r
-  static constexpr int kInfo = kJRow + 64 * 4;                 // int4[2]
+  // At 64 rows the 19 warps leave each thread 96 registers and the compute role
+  // spilled, so there the per-row biases live in shared memory (one slot of 16
+  // floats per compute warp, read with broadcast loads); elsewhere in registers.
+  static constexpr bool kBiasInSmem = NC == 4;
+  static constexpr int kBias = kJRow + 64 * 4;                 // float[16 warps][16]
+  static constexpr int kInfo = kBias + 16 * 16 * 4;            // int4[2]
   static constexpr int kBars = kInfo + 32;
   // q_full[2] q_empty[2] s_full[2] s_free[2] p_full[2] pv_done[2] o_free drain flag[2]
   // smax lred kv_full[kStages] kv_empty[kStages]
@@ -590,12 +595,33 @@ struct Tc {
       // Per row: bo = (reference max) - kPOff, -inf until the row has a reference, and
       // this key slot's share of l.  A probability is 2^(x - bo), x = c * S the score in
       // base 2, so one FMA per element gives the exp2 argument a = c * S - bo.
-      float bo[RH], lsum[RH];
+      float bo_r[S::kBiasInSmem ? 1 : RH], lsum[RH];
+      float *const bo_s = reinterpret_cast<float *>(smem + S::kBias) + w * 16;  // this warp's slot
+      // bo of rows e4 .. e4 + 3 of this warp
+      auto bias4 = [&](int e4, float (&v)[4]) {
+        if constexpr (S::kBiasInSmem) {
+          uint32_t w0, w1, w2, w3;
+          lds128(smem_u32(bo_s + e4), w0, w1, w2, w3);
+          v[0] = __uint_as_float(w0), v[1] = __uint_as_float(w1);
+          v[2] = __uint_as_float(w2), v[3] = __uint_as_float(w3);
+        } else {
+#pragma unroll
+          for (int e = 0; e < 4; ++e) v[e] = bo_r[e4 + e];
+        }
+      };
+      auto bias_set = [&](int e, float v) {  // every lane holds the same v
+        if constexpr (S::kBiasInSmem) {
+          if (lane == 0) bo_s[e] = v;
+        } else {
+          bo_r[e] = v;
+        }
+      };
 #pragma unroll
       for (int e = 0; e < RH; ++e) {
-        bo[e] = -CUDART_INF_F;
+        bias_set(e, -CUDART_INF_F);
         lsum[e] = 0.f;
       }
+      if constexpr (S::kBiasInSmem) __syncwarp();
       const bool full = r0 + RH <= R;  // every row of this warp is a query row (warp-uniform)
 
       for (int jp = 0; jp < nsteps; ++jp) {
@@ -644,11 +670,13 @@ struct Tc {
               c4[0] = __uint_as_float(w0), c4[1] = __uint_as_float(w1);
               c4[2] = __uint_as_float(w2), c4[3] = __uint_as_float(w3);
             }
+            float b4[4];
+            if (with_bias) bias4(e4, b4);
 #pragma unroll
             for (int m = 0; m < MT; ++m)
 #pragma unroll
               for (int e = 0; e < 4; ++e)
-                a[m][e4 + e] = with_bias ? fmaf(a[m][e4 + e], c4[e], -bo[e4 + e])
+                a[m][e4 + e] = with_bias ? fmaf(a[m][e4 + e], c4[e], -b4[e])
                                          : a[m][e4 + e] * c4[e];
           }
           if (!full) {
@@ -713,20 +741,29 @@ struct Tc {
           float alpha[RH];
           bool rescale = false;
 #pragma unroll
-          for (int e = 0; e < RH; ++e) {
-            const int r = r0 + e;
-            // new reference: the exact max of the row so far (never below the old one)
-            const float mn = fmaxf(fmaxf(fmaxf(sm[r], sm[64 + r]), fmaxf(sm[128 + r], sm[192 + r])),
-                                   bo[e] + kPOff);
-            const float bn = mn - kPOff;
-            alpha[e] = bn == bo[e] ? 1.f : exp2f(bo[e] - bn);  // 0 from -inf
-            rescale |= alpha[e] != 1.f;
-            bo[e] = bn;
-            lsum[e] *= alpha[e];
-            const float bsafe = bn == -CUDART_INF_F ? 0.f : bn;  // a row with no visible key yet
+          for (int e4 = 0; e4 < RH; e4 += 4) {
+            float b4[4], bn4[4];
+            bias4(e4, b4);
 #pragma unroll
-            for (int m = 0; m < MT; ++m) a[m][e] -= bsafe;
+            for (int e1 = 0; e1 < 4; ++e1) {
+              const int e = e4 + e1, r = r0 + e;
+              // new reference: the exact max of the row so far (never below the old one)
+              const float mn = fmaxf(fmaxf(fmaxf(sm[r], sm[64 + r]), fmaxf(sm[128 + r], sm[192 + r])),
+                                     b4[e1] + kPOff);
+              const float bn = mn - kPOff;
+              bn4[e1] = bn;
+              alpha[e] = bn == b4[e1] ? 1.f : exp2f(b4[e1] - bn);  // 0 from -inf
+              rescale |= alpha[e] != 1.f;
+              lsum[e] *= alpha[e];
+              const float bsafe = bn == -CUDART_INF_F ? 0.f : bn;  // a row with no visible key yet
+#pragma unroll
+              for (int m = 0; m < MT; ++m) a[m][e] -= bsafe;
+            }
+            if constexpr (S::kBiasInSmem) __syncwarp();  // every lane has read the old values
+#pragma unroll
+            for (int e1 = 0; e1 < 4; ++e1) bias_set(e4 + e1, bn4[e1]);
           }
+          if constexpr (S::kBiasInSmem) __syncwarp();
           if (jp > 0 && __any_sync(kFull, rescale)) {
             // O holds the earlier steps of this segment: wait for the last P V, then
             // rescale this warp's rows of it in TMEM (lane = output dim kt)
@@ -875,8 +912,11 @@ struct Tc {
                 const int64_t row = (static_cast<int64_t>(s) * q_len + j) * p.Hq + h * G + g;
                 p.partial_o[row * HEAD_DIM + kt] = l > 0.f ? o[e] / l * vsc : 0.f;
                 if (kt == 8 * c + e) {  // one thread per row writes its lse
+                  float b4[4];
+                  bias4((8 * c + e) & ~3, b4);
                   p.partial_lse[row] =
-                      l > 0.f ? (bo[8 * c + e] + log2f(l)) * 0.69314718055994531f : -CUDART_INF_F;
+                      l > 0.f ? (b4[(8 * c + e) & 3] + log2f(l)) * 0.69314718055994531f
+                              : -CUDART_INF_F;
                 }
               }
             }
