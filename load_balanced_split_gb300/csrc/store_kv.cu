@@ -133,17 +133,46 @@ constexpr int kWarpSmem = 2 * kSlotBytes;
 
 struct Item {
   int64_t rj;  // token index r * q_len + j
+  int r, j;    // request and new token within it
   int hc;      // first head of the chunk
   int nh;      // heads in the chunk
 };
 
-__device__ __forceinline__ Item item_at(int64_t it, int n_chunks, int Hkv) {
-  Item x;
-  x.rj = it / n_chunks;
-  x.hc = static_cast<int>(it % n_chunks) * kChunkHeads;
-  x.nh = min(kChunkHeads, Hkv - x.hc);
-  return x;
-}
+// A warp's items are it0, it0 + stride, ...: their coordinates advance by fixed
+// quotients, so the integer divisions are done once per warp, not per item.
+struct ItemWalk {
+  int64_t d_rj;  // stride / n_chunks
+  int d_ch;      // stride % n_chunks (chunks, 0 .. n_chunks - 1)
+  int64_t d_r;   // d_rj / q_len
+  int d_j;       // d_rj % q_len
+  int n_chunks, q_len, Hkv;
+
+  __device__ Item first(int64_t it) const {
+    Item x;
+    x.rj = it / n_chunks;
+    const int ch = static_cast<int>(it - x.rj * n_chunks);
+    x.r = static_cast<int>(x.rj / q_len);
+    x.j = static_cast<int>(x.rj - static_cast<int64_t>(x.r) * q_len);
+    x.hc = ch * kChunkHeads;
+    x.nh = min(kChunkHeads, Hkv - x.hc);
+    return x;
+  }
+  __device__ Item next(const Item &x) const {
+    Item y;
+    int ch = x.hc / kChunkHeads + d_ch;
+    int64_t drj = d_rj;
+    if (ch >= n_chunks) ch -= n_chunks, ++drj;  // one carry at most: d_ch < n_chunks
+    y.rj = x.rj + drj;
+    int j = x.j + d_j + static_cast<int>(drj - d_rj);
+    int64_t r = x.r + d_r;
+    if (j >= q_len) j -= q_len, ++r;  // d_j + 1 <= q_len, so one carry at most
+    y.r = static_cast<int>(r);
+    y.j = j;
+    y.hc = ch * kChunkHeads;
+    y.nh = min(kChunkHeads, Hkv - y.hc);
+    return y;
+  }
+};
 
 // Issue the copies of an item's K and V rows (nh * 256 bytes each) into a slot.
 __device__ __forceinline__ void fetch_item(const Item &x, const __nv_bfloat16 *k_new,
@@ -169,7 +198,7 @@ __device__ __forceinline__ Place look_up(const Item &x, const int32_t *seq_lens,
                                          const int32_t *page_indices, int64_t num_pages,
                                          int max_pos, int q_len) {
   Place pl;
-  const int r = static_cast<int>(x.rj / q_len), j = static_cast<int>(x.rj % q_len);
+  const int r = x.r, j = x.j;
   pl.pos = seq_lens[r] - q_len + j;
   pl.page = -1;
   if (pl.pos >= 0 && pl.pos < max_pos) {
@@ -221,7 +250,15 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     for (int i = 0; i < 16; ++i) w[i] = ww[i];
   }
   const bool e4m3 = kv_dtype == HPA_KV_E4M3;
-  Item cur = item_at(it, n_chunks, Hkv);
+  ItemWalk walk;
+  walk.n_chunks = n_chunks;
+  walk.q_len = q_len;
+  walk.Hkv = Hkv;
+  walk.d_rj = stride / n_chunks;
+  walk.d_ch = static_cast<int>(stride - walk.d_rj * n_chunks);
+  walk.d_r = walk.d_rj / q_len;
+  walk.d_j = static_cast<int>(walk.d_rj - walk.d_r * q_len);
+  Item cur = walk.first(it);
   Place here = look_up(cur, seq_lens, page_indptr, page_indices, num_pages, max_pos, q_len);
   fetch_item(cur, k_new, v_new, Hkv, slots, lane);
   fetch_cos_sin(here, cos_sin, slots, lane);
@@ -233,7 +270,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     Item nxt = cur;
     Place there = here;
     if (nx < n_items) {
-      nxt = item_at(nx, n_chunks, Hkv);
+      nxt = walk.next(cur);
       const uint32_t other = slots + (buf ^ 1) * kSlotBytes;
       fetch_item(nxt, k_new, v_new, Hkv, other, lane);
       there = look_up(nxt, seq_lens, page_indptr, page_indices, num_pages, max_pos, q_len);

@@ -142,3 +142,12 @@ def test_store_kv_flags_bad_pages_and_positions():
                      db.k, db.v, status=status)
     torch.cuda.synchronize()
     assert int(status.item()) & 4
+
+
+def test_store_kv_walk_carries():
+    """600 requests x 3 new tokens x 2 chunks of KV heads (12 heads) = 3600 items, more
+    than the resident warps: a warp's next item carries across chunks, tokens and
+    requests."""
+    lens = list(np.random.default_rng(45).integers(3, 900, size=600))
+    b, db, k0, v0, ref = _run(lens, 3, "e4m3", True, seed=45, Hkv=12)
+    _check_written(db, k0, v0, ref, "e4m3")
