@@ -697,11 +697,12 @@ struct Tc {
         scores(true);
         // A reference moves only when some score exceeds it by more than the slack, i.e.
         // when a > kSlack + kPOff (always, for a row with no reference yet: a = +inf).
-        bool flag = false;
+        float amax = a[0][0];
 #pragma unroll
         for (int m = 0; m < MT; ++m)
 #pragma unroll
-          for (int e = 0; e < RH; ++e) flag |= a[m][e] > kSlack + kPOff;
+          for (int e = 0; e < RH; ++e) amax = fmaxf(amax, a[m][e]);
+        const bool flag = amax > kSlack + kPOff;
         // The 4 warps that share this warp's rows agree through an mbarrier of their own
         // (bounded waits, never named barriers: a warp that gives up must not leave the
         // others waiting without a limit).
