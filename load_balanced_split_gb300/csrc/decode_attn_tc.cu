@@ -82,8 +82,11 @@ struct TcSmem {
   // is what a step of narrow MMAs costs).
   static constexpr int kNS = KV == HPA_KV_E4M3 ? 2 * kRp : kRp;
   // Pages per step: every step pays a fixed chain of waits (S ready, the reference-max
-  // vote, P V done), so the 8-bit path takes four pages when S fits twice in TMEM.
-  static constexpr int kPPS = KV == HPA_KV_E4M3 && NC <= 2 ? 4 : 2;
+  // vote, P V done), so the 8-bit path takes four pages when S fits twice in TMEM:
+  // up to 48 rows (48 rows: 2 x 2 tiles x 96 columns of S + 96 of O = 480 of 512;
+  // 1790 -> 1449 us at q_len 6 against two-page steps).  bf16 stages of four pages
+  // would not fit twice in shared memory.
+  static constexpr int kPPS = KV == HPA_KV_E4M3 && NC <= 3 ? 4 : 2;
   static constexpr int kMT = kPPS / 2;                         // 128-key tiles per step
   static constexpr int kStepKeys = PAGE * kPPS;
   static constexpr int kKStep = kPPS * TcCfg<KV>::kPageBytes;  // K of one step
@@ -114,10 +117,11 @@ struct TcSmem {
   static constexpr int kFlags = kStepMax + 2 * 4 * 64 * 4;     // int[2][16]
   static constexpr int kLRed = kFlags + 128;                   // float[4][64] row-sum parts
   static constexpr int kJRow = kLRed + 4 * 64 * 4;             // int[64]: token j of row r
-  // At 64 rows the 19 warps leave each thread 96 registers and the compute role
-  // spilled, so there the per-row biases live in shared memory (one slot of 16
-  // floats per compute warp, read with broadcast loads); elsewhere in registers.
-  static constexpr bool kBiasInSmem = NC == 4;
+  // From 48 rows on the compute role is short of registers (at 64 rows the 19 warps
+  // leave each thread 96; at 48 the two-tile steps need more), so there the per-row
+  // biases live in shared memory (one slot of 16 floats per compute warp, read with
+  // broadcast loads); below, in registers.
+  static constexpr bool kBiasInSmem = NC >= 3;
   static constexpr int kBias = kJRow + 64 * 4;                 // float[16 warps][16]
   static constexpr int kInfo = kBias + 16 * 16 * 4;            // int4[2]
   static constexpr int kBars = kInfo + 32;
