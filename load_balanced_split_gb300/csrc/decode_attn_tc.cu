@@ -598,11 +598,12 @@ struct Tc {
       const float c_all = p.scale_log2;  // bf16: one score scale for every row
       // Per row: bo = (reference max) - kPOff, -inf until the row has a reference, and
       // this key slot's share of l.  A probability is 2^(x - bo), x = c * S the score in
-      // base 2, so one FMA per element gives the exp2 argument a = c * S - bo.
+      // base 2, so one FMA per element gives the exp2 argument a = c * S - bo.  The
+      // biases are kept negated (nb = -bo), the FMA's addend.
       float bo_r[S::kBiasInSmem ? 1 : RH], lsum[RH];
       float *const bo_s = reinterpret_cast<float *>(smem + S::kBias) + w * 16;  // this warp's slot
-      // bo of rows e4 .. e4 + 3 of this warp
-      auto bias4 = [&](int e4, float (&v)[4]) {
+      // nb of rows e4 .. e4 + 3 of this warp
+      auto nbias4 = [&](int e4, float (&v)[4]) {
         if constexpr (S::kBiasInSmem) {
           uint32_t w0, w1, w2, w3;
           lds128(smem_u32(bo_s + e4), w0, w1, w2, w3);
@@ -613,11 +614,16 @@ struct Tc {
           for (int e = 0; e < 4; ++e) v[e] = bo_r[e4 + e];
         }
       };
-      auto bias_set = [&](int e, float v) {  // every lane holds the same v
+      auto bias4 = [&](int e4, float (&v)[4]) {  // bo
+        nbias4(e4, v);
+#pragma unroll
+        for (int e = 0; e < 4; ++e) v[e] = -v[e];
+      };
+      auto bias_set = [&](int e, float v) {  // bo; every lane holds the same v
         if constexpr (S::kBiasInSmem) {
-          if (lane == 0) bo_s[e] = v;
+          if (lane == 0) bo_s[e] = -v;
         } else {
-          bo_r[e] = v;
+          bo_r[e] = -v;
         }
       };
 #pragma unroll
@@ -658,8 +664,10 @@ struct Tc {
               if (KV == HPA_KV_E4M3) {  // S = S(Q hi) + S(Q lo) / 16 (the lo term's fixed scale)
                 float u[8];
                 tc_ld8(col + kRp, u);
+                const f32x2 k16 = pk(0.0625f, 0.0625f);
 #pragma unroll
-                for (int e = 0; e < 8; ++e) v[e] = fmaf(u[e], 0.0625f, v[e]);
+                for (int e = 0; e < 8; e += 2)
+                  upk(fma2(pk(u[e], u[e + 1]), k16, pk(v[e], v[e + 1])), v[e], v[e + 1]);
               }
 #pragma unroll
               for (int e = 0; e < 8; ++e) a[m][8 * c + e] = v[e];
@@ -674,14 +682,16 @@ struct Tc {
               c4[0] = __uint_as_float(w0), c4[1] = __uint_as_float(w1);
               c4[2] = __uint_as_float(w2), c4[3] = __uint_as_float(w3);
             }
-            float b4[4];
-            if (with_bias) bias4(e4, b4);
+            float nb4[4];
+            if (with_bias) nbias4(e4, nb4);
 #pragma unroll
             for (int m = 0; m < MT; ++m)
 #pragma unroll
-              for (int e = 0; e < 4; ++e)
-                a[m][e4 + e] = with_bias ? fmaf(a[m][e4 + e], c4[e], -b4[e])
-                                         : a[m][e4 + e] * c4[e];
+              for (int e = 0; e < 4; e += 2) {
+                const f32x2 s2 = pk(a[m][e4 + e], a[m][e4 + e + 1]), c2 = pk(c4[e], c4[e + 1]);
+                upk(with_bias ? fma2(s2, c2, pk(nb4[e], nb4[e + 1])) : mul2(s2, c2),
+                    a[m][e4 + e], a[m][e4 + e + 1]);
+              }
           }
           if (!full) {
 #pragma unroll
@@ -821,8 +831,7 @@ struct Tc {
 #pragma unroll
             for (int e = 0; e < RH; e += 2) {
               const float p0 = exp2f(a[m][e]), p1 = exp2f(a[m][e + 1]);
-              lsum[e] += p0;
-              lsum[e + 1] += p1;
+              upk(add2(pk(lsum[e], lsum[e + 1]), pk(p0, p1)), lsum[e], lsum[e + 1]);
               pw[e / 2] = pack_bf16(p0, p1);
             }
 #pragma unroll
@@ -839,8 +848,7 @@ struct Tc {
                 const int a0 = e4 + e;
                 const float p0 = exp2f(a[m][a0]);
                 const float p1 = exp2f(a[m][a0 + 1]);
-                lsum[a0] += p0;
-                lsum[a0 + 1] += p1;
+                upk(add2(pk(lsum[a0], lsum[a0 + 1]), pk(p0, p1)), lsum[a0], lsum[a0 + 1]);
                 // hi = e4m3(p), lo = e4m3(p - hi), the residual taken in f16 (exact there)
                 const uint32_t pf = pack_f16(p0, p1);
                 const uint16_t h2 = f16x2_to_e4m3x2(pf);
