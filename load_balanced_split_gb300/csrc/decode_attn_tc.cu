@@ -30,9 +30,9 @@
 // by more than 4 (base 2), so P <= 256.  bf16 pages use kind::f16 with bf16 Q
 // and P.
 //
-// Roles: CW = 8, 12 or 16 compute warps (softmax, epilogue; the warps with
-// w % 4 equal share TMEM lane quarter w % 4 -- the same keys, and the same
-// output dims -- and split the query rows, at most 16 rows each), then one TMA
+// Roles: CW = 8 or 12 compute warps (softmax, epilogue; the warps with w % 4
+// equal share TMEM lane quarter w % 4 -- the same keys, and the same output
+// dims -- and split the query rows, 8, 16 or 32 rows each), then one TMA
 // producer warp, one warp whose thread issues Q K^T and one issuing P V.  A
 // tcgen05.mma costs its issuing thread about 100 cycles whatever N is, so the
 // two products are issued from
@@ -72,9 +72,11 @@ struct TcCfg<HPA_KV_E4M3> {
 template <int KV, int NC>
 struct TcSmem {
   static constexpr int kRp = 16 * NC;
-  // Compute warps: 4 per group of rows, one group per TMEM lane quarter each; a
-  // warp takes at most 16 rows (8 warps up to 32 rows, 12 for 48, 16 for 64).
-  static constexpr int kCW = NC <= 2 ? 8 : 4 * NC;
+  // Compute warps: 4 per group of rows, one group per TMEM lane quarter each (8
+  // warps up to 32 rows, 12 for 48 and 8 of 32 rows each for 64).  At 64 rows, 16
+  // warps of 16 rows would leave 96 registers a thread (19 warps, 5 on some SM
+  // sub-partitions); 8 warps of 32 rows get 168 (11 warps) and were 1.2 % faster.
+  static constexpr int kCW = NC <= 2 || NC == 4 ? 8 : 4 * NC;
   static constexpr int kRH = kRp / (kCW / 4);                  // rows per compute warp
   static constexpr int kThreads = (kCW + 3) * 32;              // + producer, QK, PV issuers
   // Columns of S and of O: the hi and lo terms of the 8-bit path sit side by side
@@ -117,12 +119,13 @@ struct TcSmem {
   static constexpr int kFlags = kStepMax + 2 * 4 * 64 * 4;     // int[2][16]
   static constexpr int kLRed = kFlags + 128;                   // float[4][64] row-sum parts
   static constexpr int kJRow = kLRed + 4 * 64 * 4;             // int[64]: token j of row r
-  // From 48 rows on the compute role is short of registers (at 64 rows the 19 warps
-  // leave each thread 96; at 48 the two-tile steps need more), so there the per-row
-  // biases live in shared memory (one slot of 16 floats per compute warp, read with
-  // broadcast loads); below, in registers.
+  // From 48 rows on the compute role is short of registers (at 48 rows the two-tile
+  // steps, at 64 the 32 rows a warp), so there the per-row biases live in shared
+  // memory (one slot of kRH floats per compute warp, read with broadcast loads);
+  // below, in registers.
   static constexpr bool kBiasInSmem = NC >= 3;
-  static constexpr int kBias = kJRow + 64 * 4;                 // float[16 warps][16]
+  static constexpr int kBias = kJRow + 64 * 4;                 // float[kCW][kRH]
+  static_assert(kCW * kRH <= 256, "bias slots");
   static constexpr int kInfo = kBias + 16 * 16 * 4;            // int4[2]
   static constexpr int kBars = kInfo + 32;
   // q_full[2] q_empty[2] s_full[2] s_free[2] p_full[2] pv_done[2] o_free drain flag[2]
@@ -601,7 +604,7 @@ struct Tc {
       // base 2, so one FMA per element gives the exp2 argument a = c * S - bo.  The
       // biases are kept negated (nb = -bo), the FMA's addend.
       float bo_r[S::kBiasInSmem ? 1 : RH], lsum[RH];
-      float *const bo_s = reinterpret_cast<float *>(smem + S::kBias) + w * 16;  // this warp's slot
+      float *const bo_s = reinterpret_cast<float *>(smem + S::kBias) + w * RH;  // this warp's slot
       // nb of rows e4 .. e4 + 3 of this warp
       auto nbias4 = [&](int e4, float (&v)[4]) {
         if constexpr (S::kBiasInSmem) {
@@ -708,6 +711,66 @@ struct Tc {
                 if (d0[m] >= jrow[r0 + e]) a[m][e] = -CUDART_INF_F;
             }
         };
+        // P^T goes to shared memory MN-major: this thread's key kk holds rows
+        // [r0, r0 + RH) at bytes [r0, r0 + RH) (E4M3 hi; lo at Rp + r0) or [2 r0, 2 r0 + 2 RH)
+        // (bf16) of its row
+        auto encode = [&](bool add) {  // add: take the probabilities into l
+        const uint32_t pb = base + st * S::kStageBytes;  // over this step's K (read by Q K^T)
+#pragma unroll
+        for (int m = 0; m < MT; ++m) {
+          const int kk = kt + 128 * m;  // key within the step
+          static_assert(RH == 32 || RH == 16 || RH == 8, "rows per compute warp");
+          if (KV == HPA_KV_BF16) {
+            uint32_t pw[RH / 2];  // rows (r0 + e, r0 + e + 1) in word e / 2
+#pragma unroll
+            for (int e = 0; e < RH; e += 2) {
+              const float p0 = exp2f(a[m][e]), p1 = exp2f(a[m][e + 1]);
+              if (add) upk(add2(pk(lsum[e], lsum[e + 1]), pk(p0, p1)), lsum[e], lsum[e + 1]);
+              pw[e / 2] = pack_bf16(p0, p1);
+            }
+#pragma unroll
+            for (int c = 0; c < RH / 8; ++c)
+              sts128(pb + mnmaj(kk, 2 * r0 + 16 * c, S::kPSW), pw[4 * c], pw[4 * c + 1],
+                     pw[4 * c + 2], pw[4 * c + 3]);
+          } else {
+            uint32_t hw[RH / 4], lw[RH / 4];  // rows r0 + e4 .. r0 + e4 + 3 in word e4 / 4
+#pragma unroll
+            for (int e4 = 0; e4 < RH; e4 += 4) {
+              uint32_t hi = 0, lo = 0;
+#pragma unroll
+              for (int e = 0; e < 4; e += 2) {
+                const int a0 = e4 + e;
+                const float p0 = exp2f(a[m][a0]);
+                const float p1 = exp2f(a[m][a0 + 1]);
+                if (add) upk(add2(pk(lsum[a0], lsum[a0 + 1]), pk(p0, p1)), lsum[a0], lsum[a0 + 1]);
+                // hi = e4m3(p), lo = e4m3(p - hi), the residual taken in f16 (exact there)
+                const uint32_t pf = pack_f16(p0, p1);
+                const uint16_t h2 = f16x2_to_e4m3x2(pf);
+                const uint32_t hh = e4m3x2_to_f16x2(h2);
+                const __half2 rr2 = __hsub2(*reinterpret_cast<const __half2 *>(&pf),
+                                            *reinterpret_cast<const __half2 *>(&hh));
+                const uint16_t l2 = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t *>(&rr2));
+                hi |= static_cast<uint32_t>(h2) << (8 * e);
+                lo |= static_cast<uint32_t>(l2) << (8 * e);
+              }
+              hw[e4 / 4] = hi;
+              lw[e4 / 4] = lo;
+            }
+            if constexpr (RH >= 16) {
+#pragma unroll
+              for (int c = 0; c < RH / 16; ++c) {
+                sts128(pb + mnmaj(kk, r0 + 16 * c, S::kPSW), hw[4 * c], hw[4 * c + 1],
+                       hw[4 * c + 2], hw[4 * c + 3]);
+                sts128(pb + mnmaj(kk, kRp + r0 + 16 * c, S::kPSW), lw[4 * c], lw[4 * c + 1],
+                       lw[4 * c + 2], lw[4 * c + 3]);
+              }
+            } else {
+              sts64(pb + mnmaj(kk, r0, S::kPSW), hw[0], hw[1]);
+              sts64(pb + mnmaj(kk, kRp + r0, S::kPSW), lw[0], lw[1]);
+            }
+          }
+        }
+        };
         scores(true);
         // A reference moves only when some score exceeds it by more than the slack, i.e.
         // when a > kSlack + kPOff (always, for a row with no reference yet: a = +inf).
@@ -720,13 +783,26 @@ struct Tc {
         // The 4 warps that share this warp's rows agree through an mbarrier of their own
         // (bounded waits, never named barriers: a warp that gives up must not leave the
         // others waiting without a limit).
-        {
-          const bool any = __any_sync(kFull, flag);
-          if (lane == 0) {
-            flags[b * 16 + w] = any;  // w = 4 hf + qd
-            mbar_arrive(bars + 8 * (B_FLAG + 4 * b + hf));
-          }
+        const bool any = __any_sync(kFull, flag);
+        if (lane == 0) {
+          flags[b * 16 + w] = any;  // w = 4 hf + qd
+          mbar_arrive(bars + 8 * (B_FLAG + 4 * b + hf));
         }
+        // Wait out the P V of two steps back.  P^T lives in this step's own stage, so no
+        // buffer depends on it; the wait keeps this thread's parity waits on PV_DONE[b]
+        // in order (each of its uses waited, so a later parity wait cannot mistake an
+        // older phase for the one it expects) and bounds how far the compute warps run
+        // ahead of P V.
+        if (i >= 2 && (*abort_flag ||
+                       !mbar_wait_bounded(bars + 8 * (B_PV_DONE + b), ((i - 2) >> 1) & 1))) {
+          ok = false;
+          break;
+        }
+        // While the vote completes, a warp with no score past the slack writes its
+        // probabilities against the reference as it stands.  If the vote moves the
+        // reference, they are written again; l already holds them, and the rescale by
+        // alpha = 2^(bo - bn) turns 2^(x - bo) into 2^(x - bn).
+        if (!any) encode(true);
         if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_FLAG + 4 * b + hf), (i >> 1) & 1)) {
           ok = false;
           break;
@@ -803,73 +879,15 @@ struct Tc {
               }
             tc_wait_st();
           }
+          encode(any);  // l takes them now only if this warp did not write them above
         }
         // S[b] may be overwritten by the Q K^T two steps on
         tc_fence_before();
         __syncwarp();
         if (lane == 0) mbar_arrive(bars + 8 * (B_S_FREE + b));
-        // Wait out the P V of two steps back.  P^T now lives in this step's own stage,
-        // so no buffer depends on it; the wait keeps this thread's parity waits on
-        // PV_DONE[b] in order (each of its uses waited, so a later parity wait cannot
-        // mistake an older phase for the one it expects) and bounds how far the
-        // compute warps run ahead of P V.
-        if (i >= 2 && (*abort_flag ||
-                       !mbar_wait_bounded(bars + 8 * (B_PV_DONE + b), ((i - 2) >> 1) & 1))) {
-          ok = false;
-          break;
-        }
-        // P^T goes to shared memory MN-major: this thread's key kk holds rows
-        // [r0, r0 + RH) at bytes [r0, r0 + RH) (E4M3 hi; lo at Rp + r0) or [2 r0, 2 r0 + 2 RH)
-        // (bf16) of its row
-        const uint32_t pb = base + st * S::kStageBytes;  // over this step's K (read by Q K^T)
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
           const int kk = kt + 128 * m;  // key within the step
-          static_assert(RH == 16 || RH == 8, "rows per compute warp");
-          if (KV == HPA_KV_BF16) {
-            uint32_t pw[RH / 2];  // rows (r0 + e, r0 + e + 1) in word e / 2
-#pragma unroll
-            for (int e = 0; e < RH; e += 2) {
-              const float p0 = exp2f(a[m][e]), p1 = exp2f(a[m][e + 1]);
-              upk(add2(pk(lsum[e], lsum[e + 1]), pk(p0, p1)), lsum[e], lsum[e + 1]);
-              pw[e / 2] = pack_bf16(p0, p1);
-            }
-#pragma unroll
-            for (int c = 0; c < RH / 8; ++c)
-              sts128(pb + mnmaj(kk, 2 * r0 + 16 * c, S::kPSW), pw[4 * c], pw[4 * c + 1],
-                     pw[4 * c + 2], pw[4 * c + 3]);
-          } else {
-            uint32_t hw[RH / 4], lw[RH / 4];  // rows r0 + e4 .. r0 + e4 + 3 in word e4 / 4
-#pragma unroll
-            for (int e4 = 0; e4 < RH; e4 += 4) {
-              uint32_t hi = 0, lo = 0;
-#pragma unroll
-              for (int e = 0; e < 4; e += 2) {
-                const int a0 = e4 + e;
-                const float p0 = exp2f(a[m][a0]);
-                const float p1 = exp2f(a[m][a0 + 1]);
-                upk(add2(pk(lsum[a0], lsum[a0 + 1]), pk(p0, p1)), lsum[a0], lsum[a0 + 1]);
-                // hi = e4m3(p), lo = e4m3(p - hi), the residual taken in f16 (exact there)
-                const uint32_t pf = pack_f16(p0, p1);
-                const uint16_t h2 = f16x2_to_e4m3x2(pf);
-                const uint32_t hh = e4m3x2_to_f16x2(h2);
-                const __half2 rr2 = __hsub2(*reinterpret_cast<const __half2 *>(&pf),
-                                            *reinterpret_cast<const __half2 *>(&hh));
-                const uint16_t l2 = f16x2_to_e4m3x2(*reinterpret_cast<const uint32_t *>(&rr2));
-                hi |= static_cast<uint32_t>(h2) << (8 * e);
-                lo |= static_cast<uint32_t>(l2) << (8 * e);
-              }
-              hw[e4 / 4] = hi;
-              lw[e4 / 4] = lo;
-            }
-            if constexpr (RH == 16) {
-              sts128(pb + mnmaj(kk, r0, S::kPSW), hw[0], hw[1], hw[2], hw[3]);
-              sts128(pb + mnmaj(kk, kRp + r0, S::kPSW), lw[0], lw[1], lw[2], lw[3]);
-            } else {
-              sts64(pb + mnmaj(kk, r0, S::kPSW), hw[0], hw[1]);
-              sts64(pb + mnmaj(kk, kRp + r0, S::kPSW), lw[0], lw[1]);
-            }
-          }
           // V rows of keys past the request (or of a missing page) must be finite: zero them
           if (hf == 0 && (key0 + 128 * m >= pg1 * PAGE || key0 + 128 * m >= L)) {
             uint8_t *vr = smem + st * S::kStageBytes + S::kKStep + (kk >> 3) * 1024 + (kk & 7) * 128;
