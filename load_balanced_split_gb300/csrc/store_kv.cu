@@ -329,25 +329,29 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
       for (int ps = 0; ps < kChunkHeads / kHeadsPerPass; ++ps) {
         const int hh = ps * kHeadsPerPass + hp;  // head within the chunk
         const bool active = hh < cur.nh;  // lanes of a missing head still take the shuffles
-        f32x2 y[8], x[8];
+        f32x2 y[8];
+        const uint32_t ka = slot + hh * (HEAD_DIM * 2) + 16 * k;
         if (active) {
-          uint4 kr[2], vr[2];
-          const uint32_t ka = slot + hh * (HEAD_DIM * 2) + 16 * k;
+          uint4 kr[2];
           lds128(ka, kr[0].x, kr[0].y, kr[0].z, kr[0].w);
           lds128(ka + 128, kr[1].x, kr[1].y, kr[1].z, kr[1].w);
-          lds128(ka + kRowsBytes / 2, vr[0].x, vr[0].y, vr[0].z, vr[0].w);
-          lds128(ka + kRowsBytes / 2 + 128, vr[1].x, vr[1].y, vr[1].z, vr[1].w);
           unpack16(kr, y);
-          unpack16(vr, x);
         } else {
 #pragma unroll
-          for (int j = 0; j < 8; ++j) y[j] = x[j] = 0ull;
+          for (int j = 0; j < 8; ++j) y[j] = 0ull;
         }
         const float fk = key_transform(y, c, sn, nsn, w, eps, use_hadamard);
         if (active) {
           const int h = cur.hc + hh;
           const int64_t row = (static_cast<int64_t>(page) * Hkv + h) * PAGE + pos % PAGE;
           store16(k_pool, kv_dtype, row, k, y, e4m3 ? fk / k_scale[h] : fk);
+          // the value, loaded only now: its registers are not live across the key's
+          // transform
+          uint4 vr[2];
+          f32x2 x[8];
+          lds128(ka + kRowsBytes / 2, vr[0].x, vr[0].y, vr[0].z, vr[0].w);
+          lds128(ka + kRowsBytes / 2 + 128, vr[1].x, vr[1].y, vr[1].z, vr[1].w);
+          unpack16(vr, x);
           store16(v_pool, kv_dtype, row, k, x, e4m3 ? 1.f / v_scale[h] : 1.f);  // value: converted only
         }
       }

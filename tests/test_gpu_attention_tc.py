@@ -190,13 +190,15 @@ def test_thousands_of_short_requests(kv):
 
 
 @pytest.mark.parametrize("case", ["large", "tiny", "mixed_rows"])
-@pytest.mark.parametrize("q_len", [1, 2, 4])
+@pytest.mark.parametrize("q_len", [1, 2, 4, 6, 8])
 @pytest.mark.parametrize("kv", ["e4m3", "bf16"])
 def test_query_magnitudes(kv, q_len, case):
-    """bf16 query rows far outside N(0,1): elements near 1e5 and near 1e-6.  The E4M3
-    path carries each row as two E4M3 terms, each with a power-of-two row scale of its
-    own, so rows of any magnitude are exact and the scores of 1e5-sized rows keep the
-    precision the 1e-4 lse bound needs where they cancel to a small lse.  (A row with a
+    """bf16 query rows far outside N(0,1): elements near 1e5 and near 1e-6, at 8 to 64
+    rows per KV head (every compute-warp layout).  The E4M3 path carries each row as
+    two E4M3 terms under a power-of-two row scale, the second term with a further
+    fixed x16, so rows of any magnitude are carried to bf16 precision and the scores of
+    1e5-sized rows keep the precision the 1e-4 lse bound needs where they cancel to a
+    small lse.  (A row with a
     single element 3e5 times its others is run on the mma.sync kernel only: here up to
     16 partial-output elements of such rows, among keys that tie on that element, miss
     the bound.)"""
