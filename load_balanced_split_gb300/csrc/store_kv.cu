@@ -146,9 +146,9 @@ __device__ __forceinline__ void cp_async_wait_1() {
 }
 
 // An item is one new token (r, j) and a chunk of up to 8 of its KV heads; each
-// warp keeps two items' raw K and V rows in its own shared-memory slots (4 KB
-// each), so the next item's rows stream in while this one's page lookup and
-// arithmetic run.
+// warp keeps two items' raw K and V rows and cos/sin row in its own shared-memory
+// slots (4.5 KB each), so the next item's rows stream in while this one's
+// arithmetic runs.
 constexpr int kChunkHeads = 8;
 constexpr int kRowsBytes = kChunkHeads * HEAD_DIM * 2 * 2;  // K then V, bf16
 constexpr int kCosOff = kRowsBytes;                         // then the token's cos/sin row
@@ -370,7 +370,7 @@ cudaError_t launch_store_kv(const StoreKvParams &p, cudaStream_t s) {
   int dev = 0;
   cudaError_t e = cudaGetDevice(&dev);
   if (e != cudaSuccess) return e;
-  constexpr int kSmem = kWarps * kWarpSmem;  // 64 KB: two 4 KB slots per warp
+  constexpr int kSmem = kWarps * kWarpSmem;  // 72 KB: two 4.5 KB slots per warp
   if (dev < 64 && !configured[dev]) {
     e = cudaFuncSetAttribute(store_kv_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
     if (e != cudaSuccess) return e;
