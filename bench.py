@@ -248,8 +248,13 @@ def run_ours(args, rank, world, local_rank):
 
     def traced_tail(w, reps=3):
         """Per-CTA timestamps of the attention kernel (outside the timed region)."""
-        if tc:
-            return None  # the tcgen05 kernel has no traced variant
+        # the traced call runs the kernel hpa_decode_attn picks (tcgen05 above 16 rows);
+        # a forced choice that differs from it has no trace
+        rows = b.Hq // b.Hkv * b.q_len  # query rows per KV head
+        traced_tc = rows > 16 and not allh
+        if (tc or (rows > 16 and not mma and not allh)) != traced_tc:
+            return None
+        groups_t = 1 if traced_tc else groups
         heads_axis = 1 if allh else b.Hkv  # CTAs per partition and row group
         tr = torch.zeros(4 * w.num_ctas * heads_axis * groups, dtype=torch.int64, device=dev)
         out_t = None
@@ -263,7 +268,7 @@ def run_ours(args, rank, world, local_rank):
                 hpa.hpa_decode_attn_traced(q, k, v, indptr, indices, w.taskmap, w.num_ctas,
                                            w.partial_o, w.partial_lse, tr, ks, vs, stream=stream)
             torch.cuda.synchronize(dev)
-            out_t = hpa.trace_summary(tr, w.num_ctas, heads_axis, groups)
+            out_t = hpa.trace_summary(tr, w.num_ctas, heads_axis, groups_t)
         return {k2: round(v2, 3) if isinstance(v2, float) else v2 for k2, v2 in out_t.items()}
 
     tail = traced_tail(ws)

@@ -245,14 +245,16 @@ int hpa_decode_attn_tc(const void *q_dev, const void *k_pool_dev, const void *v_
 int32_t hpa_default_num_ctas_tc(int32_t Hq, int32_t Hkv, int32_t q_len, int32_t kv_dtype);
 
 /*
- * hpa_decode_attn_traced -- hpa_decode_attn that also records, for every CTA,
- * four uint64 words at trace_dev[4 * (h * num_ctas + c)]: the %globaltimer (ns)
- * at kernel entry, after the task map was read, after the CTA's last segment
- * was stored, and (smid | segments << 32).  Used to measure SM busy time and
- * the tail idle of the last CTA (the pages watch "attention kernel tail idle",
- * "Hy3 Preview AI Infra 推理优化精读笔记", §3.1 对我们的启发).  trace_dev: device,
- * 8-byte aligned, >= 4 * num_ctas * Hkv * row groups words, CTA (c, h, z) at
- * word 4 * ((z * Hkv + h) * num_ctas + c).
+ * hpa_decode_attn_traced -- hpa_decode_attn (the same kernel choice) that
+ * also records, for every CTA, four uint64 words at trace_dev[4 * (h * num_ctas
+ * + c)]: the %globaltimer (ns) at kernel entry, after the task map was read,
+ * after the CTA's last segment was stored, and (smid | segments << 32).  Used
+ * to measure SM busy time and the tail idle of the last CTA (the pages watch
+ * "attention kernel tail idle", "Hy3 Preview AI Infra 推理优化精读笔记", §3.1
+ * 对我们的启发).  trace_dev: device, 8-byte aligned, >= 4 * num_ctas * Hkv *
+ * row groups words; CTA (c, h, z) of the mma.sync kernel (up to 16 rows) at
+ * word 4 * ((z * Hkv + h) * num_ctas + c), CTA (c, h) of the tcgen05 kernel
+ * (above 16 rows, no row-group axis) at word 4 * (h * num_ctas + c).
  */
 int hpa_decode_attn_traced(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,
                            int32_t kv_dtype, const float *k_scale_dev, const float *v_scale_dev,

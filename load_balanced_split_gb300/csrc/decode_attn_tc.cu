@@ -980,6 +980,10 @@ __global__ void __launch_bounds__(TcSmem<KV, NC>::kThreads, 1)
   const int c = blockIdx.x, h = blockIdx.y;
   __shared__ int hdr[4];  // go, tile, s_begin, s_end
   const uint32_t base = smem_u32(smem), bars = base + S::kBars;
+  // optional per-CTA timestamps: entry, map read, last segment stored, smid | segments << 32
+  unsigned long long *trace =
+      p.trace ? p.trace + 4 * (static_cast<int64_t>(h) * p.C + c) : nullptr;
+  if (trace && threadIdx.x == 0) trace[0] = globaltimer_ns();
   pdl_wait();
   if (threadIdx.x == 0) {
     const int32_t *tm = p.tm;
@@ -1014,7 +1018,14 @@ __global__ void __launch_bounds__(TcSmem<KV, NC>::kThreads, 1)
   }
   __syncthreads();
   pdl_launch_dependents();
-  if (!hdr[0]) return;  // bad map, or a partition with no tiles
+  if (trace && threadIdx.x == 0) {
+    trace[1] = globaltimer_ns();
+    trace[3] = smid() | (static_cast<unsigned long long>(hdr[3] - hdr[2]) << 32);
+  }
+  if (!hdr[0]) {  // bad map, or a partition with no tiles
+    if (trace && threadIdx.x == 0) trace[2] = globaltimer_ns();
+    return;
+  }
   if (threadIdx.x < 32) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(
                      base + S::kTmem),
@@ -1038,6 +1049,7 @@ __global__ void __launch_bounds__(TcSmem<KV, NC>::kThreads, 1)
     Tc<KV, NC>::pv_issuer(p, smem, s_begin, s_end, tile, tmem);
   tc_fence_before();
   __syncthreads();
+  if (trace && threadIdx.x == 0) trace[2] = globaltimer_ns();  // every segment stored
   // both issuers have committed to the drain barrier: wait (bounded) for their MMAs
   mbar_wait_bounded(bars + 8 * B_DRAIN, 0, 1000000000ull);
   if (threadIdx.x < 32) {

@@ -332,7 +332,8 @@ int hpa_decode_attn_traced(const void *q_dev, const void *k_pool_dev, const void
   return decode_attn_impl(q_dev, k_pool_dev, v_pool_dev, kv_dtype, k_scale_dev, v_scale_dev,
                           num_pages, page_indptr_dev, page_indices_dev, page_size, B, q_len, Hq,
                           Hkv, d, sm_scale, taskmap_dev, num_ctas, partial_o_dev,
-                          partial_lse_dev, trace_dev, nullptr, nullptr, nullptr, stream);
+                          partial_lse_dev, trace_dev, nullptr, nullptr, nullptr, stream,
+                          routes_to_tc(Hq, Hkv, q_len));
 }
 
 int hpa_decode_attn_allheads(const void *q_dev, const void *k_pool_dev, const void *v_pool_dev,

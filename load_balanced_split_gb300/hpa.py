@@ -451,9 +451,10 @@ class Workspace:
     Sized once for (B, num_ctas, q_len, Hq, d) -- dynamic map by default, or
     the static comparator with `splits`.  Allocation is done with torch; the
     library itself never allocates.  num_ctas (partitions per KV head) is
-    normally hpa_default_num_ctas(...) for the mma.sync attention kernel, or
-    hpa_default_num_ctas_tc(...) when the step runs the tcgen05 kernel
-    (decode_step(..., tc=True)); either kernel accepts any partition count.
+    normally hpa_default_num_ctas(...), which follows hpa_decode_attn's kernel
+    choice (mma.sync up to 16 query rows per KV head, tcgen05 above);
+    hpa_default_num_ctas_mma / _tc size for a forced kernel.  Either kernel
+    accepts any partition count.
     """
 
     def __init__(self, B, q_len, Hq, d, num_ctas=None, splits=None, device="cuda", Hkv=8,

@@ -204,3 +204,38 @@ def test_query_magnitudes(kv, q_len, case):
     the bound.)"""
     b, sm = scaled_query_batch([2 * q_len, 65, 513, 1000, 3333], q_len, kv, 140 + q_len, case)
     check(b, num_ctas=5, sm_scale=sm)
+
+
+@pytest.mark.parametrize("q_len", [3, 8])
+def test_traced_call_runs_tcgen05_above_16_rows(q_len):
+    """hpa_decode_attn_traced makes hpa_decode_attn's kernel choice: above 16 rows it runs
+    this kernel (the same partials as hpa_decode_attn_tc, bit for bit) and records one
+    trace entry per (partition, KV head) CTA, with every segment counted once per head."""
+    b = W.make_batch([3000, 40, 12000, 700], q_len=q_len, kv_dtype="e4m3", seed=90 + q_len)
+    db = DeviceBatch(b)
+    C = 6
+    ws = hpa.Workspace(b.B, q_len, b.Hq, b.d, num_ctas=C)
+    ws.plan(db.lens)
+    hpa.hpa_decode_attn_tc(db.q, db.k, db.v, db.indptr, db.indices, ws.taskmap, C, ws.partial_o,
+                           ws.partial_lse, db.ks, db.vs)
+    torch.cuda.synchronize()
+    S = int(ws.taskmap[5].item())
+    n = S * q_len * b.Hq
+    ref_o, ref_l = ws.partial_o[:n * b.d].clone(), ws.partial_lse[:n].clone()
+    groups = (b.Hq // b.Hkv * q_len + 15) // 16
+    trace = torch.zeros(4 * C * b.Hkv * groups, dtype=torch.int64, device="cuda")
+    hpa.hpa_decode_attn_traced(db.q, db.k, db.v, db.indptr, db.indices, ws.taskmap, C,
+                               ws.partial_o, ws.partial_lse, trace, db.ks, db.vs)
+    torch.cuda.synchronize()
+    assert int(ws.taskmap[6].item()) == 0
+    assert torch.equal(ws.partial_o[:n * b.d], ref_o) and torch.equal(ws.partial_lse[:n], ref_l)
+    t = trace.view(-1, 4).cpu().numpy()
+    used, rest = t[:C * b.Hkv], t[C * b.Hkv:]
+    assert (used[:, 0] > 0).all() and (used[:, 0] <= used[:, 1]).all()
+    assert (used[:, 1] <= used[:, 2]).all()
+    assert (rest == 0).all()                             # no row-group axis on this kernel
+    sms = torch.cuda.get_device_properties(0).multi_processor_count
+    assert ((used[:, 3] & 0xffffffff) < sms).all()
+    assert int((used[:, 3] >> 32).sum()) == S * b.Hkv   # every segment, once per KV head
+    summ = hpa.trace_summary(trace, C, b.Hkv)
+    assert summ["span_us"] > 0 and 0 < summ["sm_busy_frac"] <= 1.0
