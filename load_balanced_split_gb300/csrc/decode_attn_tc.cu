@@ -316,52 +316,71 @@ struct Tc {
         ok = false;
         break;
       }
-      // query rows -> operand slot (K-major, 128-byte swizzle); lane l holds dims 4l..4l+3
+      // query rows -> operand slot (K-major, 128-byte swizzle); lane l holds dims 4l..4l+3.
+      // The rows' loads go out 8 at a time: with one at a time, staging 64 rows took
+      // about 28 us of load latency per segment, during which this warp issued no K/V
+      // copies and the compute warps drained the ring (measured per CTA against its
+      // segment count: 28 -> 10 us per segment at 64 rows, 15 -> 7 at 32).
       uint8_t *qs = smem + S::kQ + slot * S::kOperand;
       float *rowc = reinterpret_cast<float *>(smem + S::kRowC) + slot * 64;
-      for (int row = 0; row < kRp; ++row) {
-        float x[4] = {0.f, 0.f, 0.f, 0.f};
-        if (row < R) {
-          const int j = row / G, g = row % G;
-          const uint2 raw = reinterpret_cast<const uint2 *>(
-              p.q + ((static_cast<int64_t>(r) * p.q_len + j) * p.Hq + h * G + g) * HEAD_DIM)[lane];
-          const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
-          const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
-          x[0] = a.x, x[1] = a.y, x[2] = b.x, x[3] = b.y;
-        }
-        if (KV == HPA_KV_BF16) {
-          uint2 w;
-          w.x = pack_bf16(x[0], x[1]);
-          w.y = pack_bf16(x[2], x[3]);
-          *reinterpret_cast<uint2 *>(qs + kmaj(row, 8 * lane, kRp * 128)) = w;
-          if (lane == 0) rowc[row] = p.scale_log2;
-        } else {
-          float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
-          amax = warp_max(amax);
-          // A power-of-two row scale puts amax * sq in [128, 256) (hi = e4m3 of it).  Every
-          // residual x * sq - hi is then at most half an E4M3 step of [128, 256), i.e. 8, so
-          // lo = e4m3(16 (x * sq - hi)) never saturates, and hi + lo / 16 carries a bf16
-          // element to its 8 significant bits down to 2^-12 of the row's largest (without
-          // the 16, residuals of small elements fall under E4M3's smallest step).
-          const float sq = pow2_to_128(amax);
-          uint32_t hi = 0, lo = 0;
-          float res[4];
+      const int *jrow = reinterpret_cast<const int *>(smem + S::kJRow);
+      constexpr int kQB = 8;  // rows whose loads are in flight together
+      for (int rb = 0; rb < kRp; rb += kQB) {
+        uint2 raws[kQB];
 #pragma unroll
-          for (int e = 0; e < 4; e += 2) {
-            const float v0 = x[e] * sq, v1 = x[e + 1] * sq;
-            const uint16_t h2 = f32x2_to_e4m3x2(v0, v1);
-            const uint32_t hh = e4m3x2_to_f16x2(h2);
-            const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hh));
-            res[e] = v0 - hf.x;  // exact: both have at most 8 significant bits
-            res[e + 1] = v1 - hf.y;
-            hi |= static_cast<uint32_t>(h2) << (8 * e);
+        for (int u = 0; u < kQB; ++u) {
+          const int row = rb + u;
+          raws[u] = make_uint2(0u, 0u);
+          if (row < R) {
+            const int j = jrow[row], g = row - j * G;
+            raws[u] = reinterpret_cast<const uint2 *>(
+                p.q + ((static_cast<int64_t>(r) * p.q_len + j) * p.Hq + h * G + g) * HEAD_DIM)[lane];
           }
+        }
 #pragma unroll
-          for (int e = 0; e < 4; e += 2)
-            lo |= static_cast<uint32_t>(f32x2_to_e4m3x2(16.f * res[e], 16.f * res[e + 1])) << (8 * e);
-          *reinterpret_cast<uint32_t *>(qs + kmaj(row, 4 * lane, 0)) = hi;
-          *reinterpret_cast<uint32_t *>(qs + kRp * 128 + kmaj(row, 4 * lane, 0)) = lo;
-          if (lane == 0) rowc[row] = p.scale_log2 * ksc / sq;
+        for (int u = 0; u < kQB; ++u) {
+          const int row = rb + u;
+          float x[4];
+          {
+            const uint2 raw = raws[u];
+            const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.x));
+            const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162 *>(&raw.y));
+            x[0] = a.x, x[1] = a.y, x[2] = b.x, x[3] = b.y;
+          }
+          if (KV == HPA_KV_BF16) {
+            uint2 w;
+            w.x = pack_bf16(x[0], x[1]);
+            w.y = pack_bf16(x[2], x[3]);
+            *reinterpret_cast<uint2 *>(qs + kmaj(row, 8 * lane, kRp * 128)) = w;
+            if (lane == 0) rowc[row] = p.scale_log2;
+          } else {
+            float amax = fmaxf(fmaxf(fabsf(x[0]), fabsf(x[1])), fmaxf(fabsf(x[2]), fabsf(x[3])));
+            amax = warp_max(amax);
+            // A power-of-two row scale puts amax * sq in [128, 256) (hi = e4m3 of it).  Every
+            // residual x * sq - hi is then at most half an E4M3 step of [128, 256), i.e. 8, so
+            // lo = e4m3(16 (x * sq - hi)) never saturates, and hi + lo / 16 carries a bf16
+            // element to its 8 significant bits down to 2^-12 of the row's largest (without
+            // the 16, residuals of small elements fall under E4M3's smallest step).
+            const float sq = pow2_to_128(amax);
+            uint32_t hi = 0, lo = 0;
+            float res[4];
+#pragma unroll
+            for (int e = 0; e < 4; e += 2) {
+              const float v0 = x[e] * sq, v1 = x[e + 1] * sq;
+              const uint16_t h2 = f32x2_to_e4m3x2(v0, v1);
+              const uint32_t hh = e4m3x2_to_f16x2(h2);
+              const float2 hf = __half22float2(*reinterpret_cast<const __half2 *>(&hh));
+              res[e] = v0 - hf.x;  // exact: both have at most 8 significant bits
+              res[e + 1] = v1 - hf.y;
+              hi |= static_cast<uint32_t>(h2) << (8 * e);
+            }
+#pragma unroll
+            for (int e = 0; e < 4; e += 2)
+              lo |= static_cast<uint32_t>(f32x2_to_e4m3x2(16.f * res[e], 16.f * res[e + 1])) << (8 * e);
+            *reinterpret_cast<uint32_t *>(qs + kmaj(row, 4 * lane, 0)) = hi;
+            *reinterpret_cast<uint32_t *>(qs + kRp * 128 + kmaj(row, 4 * lane, 0)) = lo;
+            if (lane == 0) rowc[row] = p.scale_log2 * ksc / sq;
+          }
         }
       }
       if (lane == 0)
