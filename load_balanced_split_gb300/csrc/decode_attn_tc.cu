@@ -9,7 +9,7 @@
 // with several draft tokens, where the warp-level MMAs become the bound.
 //
 // Work per step = PPS pages (64 PPS keys) of one KV head, PPS = 4 for the 8-bit
-// path with up to 32 rows (TMEM allowing) and 2 otherwise; per 128-key tile:
+// path and 2 for bf16; per 128-key tile:
 //   S^T[128 keys][rows]  = K[128 keys][128 dims] . Q^T          (tcgen05.mma, TMEM)
 //   P^T = 2^(S^T - m)    by the compute threads, one key each    (registers -> smem,
 //                        MN-major: each thread stores its key's row with 16-byte stores)
@@ -35,9 +35,9 @@
 // dims -- and split the query rows, 8, 16 or 32 rows each), then one TMA
 // producer warp, one warp whose thread issues Q K^T and one issuing P V.  A
 // tcgen05.mma costs its issuing thread about 100 cycles whatever N is, so the
-// two products are issued from
-// two threads and each step issues few, wide MMAs.  S is double-buffered in
-// TMEM so Q K^T of step i+1 overlaps the softmax of step i.  Every wait is
+// two products are issued from two threads and each step issues few, wide
+// MMAs.  S is double-buffered in TMEM (single-buffered at 64 E4M3 rows) so Q K^T
+// of step i+1 overlaps the softmax of step i.  Every wait is
 // bounded in time; a role that gives up flags the task map's status word and
 // raises the CTA's abort flag, each MMA thread commits its MMAs to a drain
 // barrier that the CTA waits on, the producer waits for its copies, and the
@@ -84,11 +84,15 @@ struct TcSmem {
   // is what a step of narrow MMAs costs).
   static constexpr int kNS = KV == HPA_KV_E4M3 ? 2 * kRp : kRp;
   // Pages per step: every step pays a fixed chain of waits (S ready, the reference-max
-  // vote, P V done), so the 8-bit path takes four pages when S fits twice in TMEM:
-  // up to 48 rows (48 rows: 2 x 2 tiles x 96 columns of S + 96 of O = 480 of 512;
-  // 1790 -> 1449 us at q_len 6 against two-page steps).  bf16 stages of four pages
-  // would not fit twice in shared memory.
-  static constexpr int kPPS = KV == HPA_KV_E4M3 && NC <= 3 ? 4 : 2;
+  // vote, P V done), so the 8-bit path takes four pages (1790 -> 1449 us at q_len 6,
+  // 2093 -> 2040 at q_len 8, against two-page steps).  bf16 stages of four pages would
+  // not fit twice in shared memory.
+  static constexpr int kPPS = KV == HPA_KV_E4M3 ? 4 : 2;
+  // S buffers in TMEM: two (48 rows: 2 x 2 tiles x 96 columns of S + 96 of O = 480 of
+  // 512), except at 64 E4M3 rows, where two tiles of 128 columns plus O leave room for
+  // one.  With one, Q K^T of step i + 1 waits until step i's scores are in registers
+  // and its reference vote is done, and runs under step i's P encoding.
+  static constexpr int kSBufs = KV == HPA_KV_E4M3 && NC == 4 ? 1 : 2;
   static constexpr int kMT = kPPS / 2;                         // 128-key tiles per step
   static constexpr int kStepKeys = PAGE * kPPS;
   static constexpr int kKStep = kPPS * TcCfg<KV>::kPageBytes;  // K of one step
@@ -139,10 +143,10 @@ struct TcSmem {
   static_assert(kAlloc <= 232448, "dynamic shared memory of one CTA");
   // TMEM columns: S[0], S[1] (kMT tiles of kNS each), O (kNS), rounded up to a power
   // of two >= 32
-  static constexpr int kCols = (2 * kMT + 1) * kNS;
+  static constexpr int kCols = (kSBufs * kMT + 1) * kNS;
   static constexpr int kTmemCols =
       kCols <= 32 ? 32 : kCols <= 64 ? 64 : kCols <= 128 ? 128 : kCols <= 256 ? 256 : 512;
-  static constexpr int kOCol = 2 * kMT * kNS;  // first column of O
+  static constexpr int kOCol = kSBufs * kMT * kNS;  // first column of O
   static_assert(kCols <= 512, "TMEM");
   static_assert(kStages >= 2, "shared memory");
 };
@@ -493,7 +497,11 @@ struct Tc {
       for (int j = 0; j < nsteps; ++j) {
         const int b = i & 1;
         if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_KV_FULL + st), phase) ||
-            !mbar_wait_bounded(bars + 8 * (B_S_FREE + b), ((i >> 1) & 1) ^ 1)) {
+            !(S::kSBufs == 2
+                  ? mbar_wait_bounded(bars + 8 * (B_S_FREE + b), ((i >> 1) & 1) ^ 1)
+                  // one buffer: step i - 1 must have released it (for i = 0, the barrier
+                  // of step -1 passes at once)
+                  : mbar_wait_bounded(bars + 8 * (B_S_FREE + ((i - 1) & 1)), ((i - 1) >> 1) & 1))) {
           ok = false;
           break;
         }
@@ -501,7 +509,7 @@ struct Tc {
         const uint32_t kbase = base + st * S::kStageBytes;
 #pragma unroll
         for (int mt = 0; mt < S::kMT; ++mt) {  // keys [128 mt, 128 mt + 128) of the step
-          const uint32_t s_t = tmem + (b * S::kMT + mt) * S::kNS;
+          const uint32_t s_t = tmem + ((S::kSBufs == 2 ? b : 0) * S::kMT + mt) * S::kNS;
           if (KV == HPA_KV_BF16) {
             const uint32_t id = tc_idesc(1, kRp, 0, 0);
 #pragma unroll
@@ -536,7 +544,7 @@ struct Tc {
                                    int tile, uint32_t tmem) {
     const uint32_t base = smem_u32(smem), bars = base + S::kBars;
     volatile int *abort_flag = reinterpret_cast<volatile int *>(smem + S::kAbort);
-    const uint32_t o_t = tmem + 2 * S::kMT * S::kNS;
+    const uint32_t o_t = tmem + S::kOCol;
     int i = 0, st = 0;
     bool ok = true;
     for (int s = s_begin; s < s_end && ok; ++s) {
@@ -680,7 +688,7 @@ struct Tc {
           for (int m = 0; m < MT; ++m)
 #pragma unroll
             for (int c = 0; c < RH / 8; ++c) {
-              const uint32_t col = lane_t + (b * MT + m) * S::kNS + r0 + 8 * c;
+              const uint32_t col = lane_t + ((S::kSBufs == 2 ? b : 0) * MT + m) * S::kNS + r0 + 8 * c;
               float v[8];
               tc_ld8(col, v);
               if (KV == HPA_KV_E4M3) {  // S = S(Q hi) + S(Q lo) / 16 (the lo term's fixed scale)
