@@ -656,11 +656,16 @@ struct Tc {
           bo_r[e] = -v;
         }
       };
+      // A row with no reference yet has bias 0 (its a is the plain score x) and its bit set
+      // in `unref`; padding rows never get one and have no bit.
 #pragma unroll
       for (int e = 0; e < RH; ++e) {
-        bias_set(e, -CUDART_INF_F);
+        bias_set(e, 0.f);
         lsum[e] = 0.f;
       }
+      uint32_t unref = 0;
+#pragma unroll
+      for (int e = 0; e < RH; ++e) unref |= (r0 + e < R ? 1u : 0u) << e;
       if constexpr (S::kBiasInSmem) __syncwarp();
       const bool full = r0 + RH <= R;  // every row of this warp is a query row (warp-uniform)
 
@@ -679,11 +684,10 @@ struct Tc {
           // row r (token j = r / G) sees keys < L - q_len + 1 + j
           d0[m] = present ? key0 + 128 * m - (L - q_len + 1) : INT_MAX;
         }
-        // a[m][e] = c_e * S - bias_e for this key slot and the warp's rows: -inf for keys a
-        // row may not see and for padding rows.  bias is bo, or 0 while computing the
-        // plain scores x (the rare path where a reference moves).
+        // a[m][e] = c_e * S - bo_e for this key slot and the warp's rows: -inf for keys a
+        // row may not see and for padding rows.
         float a[MT][RH];
-        auto scores = [&](bool with_bias) {
+        auto scores = [&]() {
 #pragma unroll
           for (int m = 0; m < MT; ++m)
 #pragma unroll
@@ -713,14 +717,13 @@ struct Tc {
               c4[2] = __uint_as_float(w2), c4[3] = __uint_as_float(w3);
             }
             float nb4[4];
-            if (with_bias) nbias4(e4, nb4);
+            nbias4(e4, nb4);
 #pragma unroll
             for (int m = 0; m < MT; ++m)
 #pragma unroll
               for (int e = 0; e < 4; e += 2) {
                 const f32x2 s2 = pk(a[m][e4 + e], a[m][e4 + e + 1]), c2 = pk(c4[e], c4[e + 1]);
-                upk(with_bias ? fma2(s2, c2, pk(nb4[e], nb4[e + 1])) : mul2(s2, c2),
-                    a[m][e4 + e], a[m][e4 + e + 1]);
+                upk(fma2(s2, c2, pk(nb4[e], nb4[e + 1])), a[m][e4 + e], a[m][e4 + e + 1]);
               }
           }
           if (!full) {
@@ -798,15 +801,20 @@ struct Tc {
           }
         }
         };
-        scores(true);
+        scores();
+        // Every read of S[b] is done (a moved reference recovers x from a): Q K^T of a
+        // later step may overwrite it while this step votes and encodes.
+        tc_fence_before();
+        __syncwarp();
+        if (lane == 0) mbar_arrive(bars + 8 * (B_S_FREE + b));
         // A reference moves only when some score exceeds it by more than the slack, i.e.
-        // when a > kSlack + kPOff (always, for a row with no reference yet: a = +inf).
+        // when a > kSlack + kPOff, and always while a row has none.
         float amax = a[0][0];
 #pragma unroll
         for (int m = 0; m < MT; ++m)
 #pragma unroll
           for (int e = 0; e < RH; ++e) amax = fmaxf(amax, a[m][e]);
-        const bool flag = amax > kSlack + kPOff;
+        const bool flag = amax > kSlack + kPOff || unref != 0;
         // The 4 warps that share this warp's rows agree through an mbarrier of their own
         // (bounded waits, never named barriers: a warp that gives up must not leave the
         // others waiting without a limit).
@@ -838,8 +846,16 @@ struct Tc {
 #pragma unroll
         for (int x4 = 0; x4 < 4; ++x4) moved |= flags[b * 16 + 4 * hf + x4];
         if (moved) {
-          // S[b] is still this warp's (released below): read the plain scores x again
-          scores(false);
+          // the plain scores x = a + bo = a - nb (S[b] is already released)
+#pragma unroll
+          for (int e4 = 0; e4 < RH; e4 += 4) {
+            float nb4[4];
+            nbias4(e4, nb4);
+#pragma unroll
+            for (int m = 0; m < MT; ++m)
+#pragma unroll
+              for (int e1 = 0; e1 < 4; ++e1) a[m][e4 + e1] -= nb4[e1];
+          }
           float *sm = stepmax + (n_moved & 1) * 4 * 64;
 #pragma unroll
           for (int e = 0; e < RH; ++e) {
@@ -858,6 +874,7 @@ struct Tc {
           ++n_moved;
           float alpha[RH];
           bool rescale = false;
+          uint32_t nunref = 0;
 #pragma unroll
           for (int e4 = 0; e4 < RH; e4 += 4) {
             float b4[4], bn4[4];
@@ -865,22 +882,25 @@ struct Tc {
 #pragma unroll
             for (int e1 = 0; e1 < 4; ++e1) {
               const int e = e4 + e1, r = r0 + e;
-              // new reference: the exact max of the row so far (never below the old one)
+              const float bo = (unref >> e) & 1u ? -CUDART_INF_F : b4[e1];
+              // new reference: the max of the row so far (never below the old one)
               const float mn = fmaxf(fmaxf(fmaxf(sm[r], sm[64 + r]), fmaxf(sm[128 + r], sm[192 + r])),
-                                     b4[e1] + kPOff);
+                                     bo + kPOff);
               const float bn = mn - kPOff;
-              bn4[e1] = bn;
-              alpha[e] = bn == b4[e1] ? 1.f : exp2f(b4[e1] - bn);  // 0 from -inf
+              alpha[e] = bn == bo ? 1.f : exp2f(bo - bn);  // 0 from -inf
               rescale |= alpha[e] != 1.f;
               lsum[e] *= alpha[e];
-              const float bsafe = bn == -CUDART_INF_F ? 0.f : bn;  // a row with no visible key yet
+              const bool none = bn == -CUDART_INF_F;  // a row with no visible key yet
+              nunref |= (none && (r < R) ? 1u : 0u) << e;
+              bn4[e1] = none ? 0.f : bn;
 #pragma unroll
-              for (int m = 0; m < MT; ++m) a[m][e] -= bsafe;
+              for (int m = 0; m < MT; ++m) a[m][e] -= bn4[e1];
             }
             if constexpr (S::kBiasInSmem) __syncwarp();  // every lane has read the old values
 #pragma unroll
             for (int e1 = 0; e1 < 4; ++e1) bias_set(e4 + e1, bn4[e1]);
           }
+          unref = nunref;
           if constexpr (S::kBiasInSmem) __syncwarp();
           if (jp > 0 && __any_sync(kFull, rescale)) {
             // O holds the earlier steps of this segment: wait for the last P V, then
@@ -908,10 +928,6 @@ struct Tc {
           }
           encode(any);  // l takes them now only if this warp did not write them above
         }
-        // S[b] may be overwritten by the Q K^T two steps on
-        tc_fence_before();
-        __syncwarp();
-        if (lane == 0) mbar_arrive(bars + 8 * (B_S_FREE + b));
 #pragma unroll
         for (int m = 0; m < MT; ++m) {
           const int kk = kt + 128 * m;  // key within the step
