@@ -204,9 +204,19 @@ __device__ __forceinline__ void fetch_item(const Item &x, const __nv_bfloat16 *k
                                            int lane) {
   const int64_t src = (x.rj * Hkv + x.hc) * HEAD_DIM;
   const int chunks = x.nh * (HEAD_DIM * 2 / 16);  // 16-byte chunks per tensor
-  for (int c = lane; c < chunks; c += 32) {
-    cp_async16(slot + 16 * c, k_new + src + 8 * c);
-    cp_async16(slot + kRowsBytes / 2 + 16 * c, v_new + src + 8 * c);
+  const __nv_bfloat16 *ks = k_new + src + 8 * lane, *vs = v_new + src + 8 * lane;
+  const uint32_t dk = slot + 16 * lane;
+  if (chunks == kChunkHeads * (HEAD_DIM * 2 / 16)) {  // a full chunk: 4 copies per tensor
+#pragma unroll
+    for (int u = 0; u < 4; ++u) {
+      cp_async16(dk + 512 * u, ks + 256 * u);
+      cp_async16(dk + kRowsBytes / 2 + 512 * u, vs + 256 * u);
+    }
+  } else {
+    for (int c = lane; c < chunks; c += 32) {
+      cp_async16(slot + 16 * c, k_new + src + 8 * c);
+      cp_async16(slot + kRowsBytes / 2 + 16 * c, v_new + src + 8 * c);
+    }
   }
 }
 
@@ -272,6 +282,16 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     w[4] = pk(w2.x, w2.y), w[5] = pk(w2.z, w2.w), w[6] = pk(w3.x, w3.y), w[7] = pk(w3.z, w3.w);
   }
   const bool e4m3 = kv_dtype == HPA_KV_E4M3;
+  // With one chunk of heads (Hkv <= 8) a lane always serves heads hp and 4 + hp: their
+  // inverse cache scales are read once
+  float rk0[2] = {1.f, 1.f}, rv0[2] = {1.f, 1.f};
+  const bool one_chunk = n_chunks == 1;
+  if (e4m3 && one_chunk)
+#pragma unroll
+    for (int ps = 0; ps < 2; ++ps) {
+      const int h = ps * kHeadsPerPass + hp;
+      if (h < Hkv) rk0[ps] = 1.f / k_scale[h], rv0[ps] = 1.f / v_scale[h];
+    }
   ItemWalk walk;
   walk.n_chunks = n_chunks;
   walk.q_len = q_len;
@@ -344,7 +364,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         if (active) {
           const int h = cur.hc + hh;
           const int64_t row = (static_cast<int64_t>(page) * Hkv + h) * PAGE + pos % PAGE;
-          store16(k_pool, kv_dtype, row, k, y, e4m3 ? fk / k_scale[h] : fk);
+          const float rk = !e4m3 ? 1.f : one_chunk ? rk0[ps] : 1.f / k_scale[h];
+          store16(k_pool, kv_dtype, row, k, y, fk * rk);
           // the value, loaded only now: its registers are not live across the key's
           // transform
           uint4 vr[2];
@@ -352,7 +373,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
           lds128(ka + kRowsBytes / 2, vr[0].x, vr[0].y, vr[0].z, vr[0].w);
           lds128(ka + kRowsBytes / 2 + 128, vr[1].x, vr[1].y, vr[1].z, vr[1].w);
           unpack16(vr, x);
-          store16(v_pool, kv_dtype, row, k, x, e4m3 ? 1.f / v_scale[h] : 1.f);  // value: converted only
+          const float rv = !e4m3 ? 1.f : one_chunk ? rv0[ps] : 1.f / v_scale[h];
+          store16(v_pool, kv_dtype, row, k, x, rv);  // value: converted only
         }
       }
     }
