@@ -219,7 +219,7 @@ int hpa_decode_attn_mma(const void *q_dev, const void *k_pool_dev, const void *v
  * (up to 64) in a single pass over the keys, where hpa_decode_attn makes one
  * pass per group of 16 rows.  It pays for MTP with more than 16 rows per KV
  * head, and hpa_decode_attn runs it there (on the E4M3 MTP workload at 64/8
- * heads: 1.8x the mma.sync kernel at q_len 3-4, 2.8x at q_len 6, 2.5x at
+ * heads: 1.9x the mma.sync kernel at q_len 3-4, 2.7x at q_len 6, 2.6x at
  * q_len 8).  With up to 16 rows, or with many short segments per partition
  * (hundreds of short requests), the mma.sync kernel is as fast or faster.
  * Arguments, layouts, supported shapes, outputs and errors are exactly those

@@ -315,7 +315,7 @@ struct Tc {
       const int pg0 = klo / PAGE, pg1 = (khi + PAGE - 1) / PAGE;
       int good = 1;
       if (lane == 0)
-        good = !*abort_flag && mbar_wait_bounded(bars + 8 * (B_Q_EMPTY + slot), ((k >> 1) & 1) ^ 1);
+        good = !*abort_flag && mbar_wait_bounded_rolled(bars + 8 * (B_Q_EMPTY + slot), ((k >> 1) & 1) ^ 1);
       if (!__shfl_sync(kFull, good, 0)) {
         ok = false;
         break;
@@ -420,7 +420,7 @@ struct Tc {
           int g2 = 1;
           if (lane == 0) {
             if (*abort_flag ||
-                !mbar_wait_bounded(bars + 8 * (S::kKvEmpty + st), phase ^ 1)) {
+                !mbar_wait_bounded_rolled(bars + 8 * (S::kKvEmpty + st), phase ^ 1)) {
               g2 = 0;
             } else {
               const uint32_t fb = bars + 8 * (B_KV_FULL + st);
@@ -460,7 +460,7 @@ struct Tc {
       *abort_flag = 1;
       for (int i = 0; i < S::kStages; ++i)  // never leave copies landing in shared memory
         if (issued & (1u << i))
-          mbar_wait_bounded(bars + 8 * (B_KV_FULL + i), (parity_bits >> i) & 1u, 1000000000ull);
+          mbar_wait_bounded_rolled(bars + 8 * (B_KV_FULL + i), (parity_bits >> i) & 1u, 1000000000ull);
     }
   }
 
@@ -489,19 +489,19 @@ struct Tc {
       const SegRow sr = read_seg_row(p.tm, p.lay, p.B, s, blockIdx.x, tile, false);
       const int pg0 = sr.klo / PAGE, pg1 = (sr.khi + PAGE - 1) / PAGE;
       const int nsteps = (pg1 - pg0 + S::kPPS - 1) / S::kPPS;
-      if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_Q_FULL + slot), (k >> 1) & 1)) {
+      if (*abort_flag || !mbar_wait_bounded_rolled(bars + 8 * (B_Q_FULL + slot), (k >> 1) & 1)) {
         ok = false;
         break;
       }
       const uint32_t qbase = base + S::kQ + slot * S::kOperand;
       for (int j = 0; j < nsteps; ++j) {
         const int b = i & 1;
-        if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_KV_FULL + st), phase) ||
+        if (*abort_flag || !mbar_wait_bounded_rolled(bars + 8 * (B_KV_FULL + st), phase) ||
             !(S::kSBufs == 2
-                  ? mbar_wait_bounded(bars + 8 * (B_S_FREE + b), ((i >> 1) & 1) ^ 1)
+                  ? mbar_wait_bounded_rolled(bars + 8 * (B_S_FREE + b), ((i >> 1) & 1) ^ 1)
                   // one buffer: step i - 1 must have released it (for i = 0, the barrier
                   // of step -1 passes at once)
-                  : mbar_wait_bounded(bars + 8 * (B_S_FREE + ((i - 1) & 1)), ((i - 1) >> 1) & 1))) {
+                  : mbar_wait_bounded_rolled(bars + 8 * (B_S_FREE + ((i - 1) & 1)), ((i - 1) >> 1) & 1))) {
           ok = false;
           break;
         }
@@ -555,8 +555,8 @@ struct Tc {
       for (int j = 0; j < nsteps; ++j) {
         const int b = i & 1;
         // P of this step written; at a segment start, the previous segment's O read out
-        if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_P_FULL + b), (i >> 1) & 1) ||
-            (j == 0 && k > 0 && !mbar_wait_bounded(bars + 8 * B_O_FREE, (k - 1) & 1))) {
+        if (*abort_flag || !mbar_wait_bounded_rolled(bars + 8 * (B_P_FULL + b), (i >> 1) & 1) ||
+            (j == 0 && k > 0 && !mbar_wait_bounded_rolled(bars + 8 * B_O_FREE, (k - 1) & 1))) {
           ok = false;
           break;
         }
@@ -615,7 +615,7 @@ struct Tc {
     bool ok = true;
     for (int s = s_begin; s < s_end && ok; ++s) {
       const int k = s - s_begin, slot = k & 1;
-      if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_Q_FULL + slot), (k >> 1) & 1)) {
+      if (*abort_flag || !mbar_wait_bounded_rolled(bars + 8 * (B_Q_FULL + slot), (k >> 1) & 1)) {
         ok = false;
         break;
       }
@@ -671,7 +671,7 @@ struct Tc {
 
       for (int jp = 0; jp < nsteps; ++jp) {
         const int b = i & 1, st = i % S::kStages;
-        if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_S_FULL + b), (i >> 1) & 1)) {
+        if (*abort_flag || !mbar_wait_bounded_rolled(bars + 8 * (B_S_FULL + b), (i >> 1) & 1)) {
           ok = false;
           break;
         }
@@ -829,7 +829,7 @@ struct Tc {
         // older phase for the one it expects) and bounds how far the compute warps run
         // ahead of P V.
         if (i >= 2 && (*abort_flag ||
-                       !mbar_wait_bounded(bars + 8 * (B_PV_DONE + b), ((i - 2) >> 1) & 1))) {
+                       !mbar_wait_bounded_rolled(bars + 8 * (B_PV_DONE + b), ((i - 2) >> 1) & 1))) {
           ok = false;
           break;
         }
@@ -838,7 +838,7 @@ struct Tc {
         // reference, they are written again; l already holds them, and the rescale by
         // alpha = 2^(bo - bn) turns 2^(x - bo) into 2^(x - bn).
         if (!any) encode(true);
-        if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_FLAG + 4 * b + hf), (i >> 1) & 1)) {
+        if (*abort_flag || !mbar_wait_bounded_rolled(bars + 8 * (B_FLAG + 4 * b + hf), (i >> 1) & 1)) {
           ok = false;
           break;
         }
@@ -867,7 +867,7 @@ struct Tc {
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(bars + 8 * (B_SMAX + hf));
-          if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_SMAX + hf), n_moved & 1)) {
+          if (*abort_flag || !mbar_wait_bounded_rolled(bars + 8 * (B_SMAX + hf), n_moved & 1)) {
             ok = false;
             break;
           }
@@ -907,7 +907,7 @@ struct Tc {
             // rescale this warp's rows of it in TMEM (lane = output dim kt)
             const int pi = i - 1;
             if (*abort_flag ||
-                !mbar_wait_bounded(bars + 8 * (B_PV_DONE + (pi & 1)), (pi >> 1) & 1)) {
+                !mbar_wait_bounded_rolled(bars + 8 * (B_PV_DONE + (pi & 1)), (pi >> 1) & 1)) {
               ok = false;
               break;
             }
@@ -958,8 +958,8 @@ struct Tc {
           }
           __syncwarp();
           if (lane == 0) mbar_arrive(bars + 8 * (B_LRED + hf));
-          if (*abort_flag || !mbar_wait_bounded(bars + 8 * (B_LRED + hf), n_seg & 1) ||
-              !mbar_wait_bounded(bars + 8 * (B_PV_DONE + b), (i >> 1) & 1)) {
+          if (*abort_flag || !mbar_wait_bounded_rolled(bars + 8 * (B_LRED + hf), n_seg & 1) ||
+              !mbar_wait_bounded_rolled(bars + 8 * (B_PV_DONE + b), (i >> 1) & 1)) {
             ok = false;
             break;
           }
@@ -1094,7 +1094,7 @@ __global__ void __launch_bounds__(TcSmem<KV, NC>::kThreads, 1)
   __syncthreads();
   if (trace && threadIdx.x == 0) trace[2] = globaltimer_ns();  // every segment stored
   // both issuers have committed to the drain barrier: wait (bounded) for their MMAs
-  mbar_wait_bounded(bars + 8 * B_DRAIN, 0, 1000000000ull);
+  mbar_wait_bounded_rolled(bars + 8 * B_DRAIN, 0, 1000000000ull);
   if (threadIdx.x < 32) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem),
