@@ -207,10 +207,12 @@ def run_ours(args, rank, world, local_rank):
             import torch.distributed as dist
             dist.barrier()
 
-    def timed(fn, steps, warmup, breakdown=True):
+    def timed(fn, steps, warmup, breakdown=True, join=None):
         """ms per step over `steps` back-to-back steps (events only at the two ends, so
         consecutive kernels keep their programmatic-dependent-launch overlap), then,
-        if asked, a second pass with events around each kernel for the breakdown."""
+        if asked, a second pass with events around each kernel for the breakdown.
+        join(), if given, makes `stream` wait for work the steps left on other streams
+        before the end event."""
         for _ in range(warmup):
             fn()
         t0, t1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
@@ -220,6 +222,8 @@ def run_ours(args, rank, world, local_rank):
         t0.record(stream)
         for _ in range(steps):
             fn()
+        if join is not None:
+            join()
         t1.record(stream)
         torch.cuda.synchronize(dev)
         barrier()
@@ -324,6 +328,10 @@ def run_ours(args, rank, world, local_rank):
     # lengths, page table) sit back to back in one pinned host buffer and one device
     # buffer, and its outputs (out, lse) likewise, so a step moves them with one copy
     # each way; the device tensors the calls take are views into those buffers.
+    # Every step copies its inputs in and its result out inside the timed region, on
+    # two copy streams and two sets of device buffers, so that step i + 1's input copy
+    # and step i's result copy run while the neighbouring step computes (as a serving
+    # loop would pipeline them).
     def packed(tensors, device):
         offs, total = [], 0
         for t in tensors:
@@ -340,33 +348,65 @@ def run_ours(args, rank, world, local_rank):
     in_h, in_h_views = packed(inputs, None)
     for dst, src in zip(in_h_views, inputs):
         dst.copy_(src)
-    in_d, (q_e, lens_e, indptr_e, indices_e) = packed(inputs, dev)
-    out_d, (out_e, lse_e) = packed([out, out_lse], dev)
-    out_h, _ = packed([out, out_lse], None)
+    in_ds = [packed(inputs, dev) for _ in range(2)]            # (buffer, views) per set
+    out_ds = [packed([out, out_lse], dev) for _ in range(2)]
+    out_hs = [packed([out, out_lse], None)[0] for _ in range(2)]
     h2d = in_h.numel()
-    d2h = out_h.numel()
+    d2h = out_hs[0].numel()
+    h2d_stream = torch.cuda.Stream(device=dev)
+    d2h_stream = torch.cuda.Stream(device=dev)
+    h2d_ev = [torch.cuda.Event() for _ in range(2)]
+    comp_ev = [torch.cuda.Event() for _ in range(2)]
+    d2h_ev = [torch.cuda.Event() for _ in range(2)]
+    e2e_count = [0]
 
     def e2e_step(ev=None):
-        if ev is not None:
-            ev[0].record(stream)
+        cur = e2e_count[0] % 2
+        e2e_count[0] += 1
+        in_d, (q_e, lens_e, indptr_e, indices_e) = in_ds[cur]
+        out_d, (out_e, lse_e) = out_ds[cur]
+        # inputs: after the step two back (which read this buffer set) has computed
+        h2d_stream.wait_event(comp_ev[cur])
+        with torch.cuda.stream(h2d_stream):
+            in_d.copy_(in_h, non_blocking=True)
+        h2d_ev[cur].record(h2d_stream)
+        stream.wait_event(h2d_ev[cur])
+        stream.wait_event(d2h_ev[cur])  # the result buffer's previous copy-out is done
+        hpa.decode_step(ws, q_e, k, v, lens_e, indptr_e, indices_e, out_e, lse_e, ks, vs,
+                        tile=b.tile, stream=stream, tc=tc, allheads=allh, mma=mma)
+        comp_ev[cur].record(stream)
+        d2h_stream.wait_event(comp_ev[cur])
+        with torch.cuda.stream(d2h_stream):
+            out_hs[cur].copy_(out_d, non_blocking=True)
+        d2h_ev[cur].record(d2h_stream)
+
+    def e2e_join():
+        stream.wait_stream(h2d_stream)
+        stream.wait_stream(d2h_stream)
+
+    e2e_ms = max_over_ranks(timed(e2e_step, args.steps, args.warmup, breakdown=False,
+                                  join=e2e_join)[0], world, dev)
+
+    def e2e_serial_step(ev=None):
+        """The same step with both copies on the compute stream (nothing overlaps)."""
+        in_d, (q_e, lens_e, indptr_e, indices_e) = in_ds[0]
+        out_d, (out_e, lse_e) = out_ds[0]
         with torch.cuda.stream(stream):
             in_d.copy_(in_h, non_blocking=True)
         hpa.decode_step(ws, q_e, k, v, lens_e, indptr_e, indices_e, out_e, lse_e, ks, vs,
                         tile=b.tile, stream=stream, tc=tc, allheads=allh, mma=mma)
         with torch.cuda.stream(stream):
-            out_h.copy_(out_d, non_blocking=True)
-        if ev is not None:
-            for e in ev[1:]:
-                e.record(stream)
+            out_hs[0].copy_(out_d, non_blocking=True)
 
-    e2e_ms = max_over_ranks(timed(e2e_step, args.steps, args.warmup, breakdown=False)[0],
-                            world, dev)
+    e2e_serial_ms = max_over_ranks(
+        timed(e2e_serial_step, args.steps, args.warmup, breakdown=False)[0], world, dev)
 
     feeder = None if args.no_feeder else feeder_measure(hpa, dev, stream, args, timed)
     return dict(b=b, C=C, ms=ms, attn=attn, plan=plan_ms, comb=comb_ms, step_ms=step_ms,
                 clocks=clocks, tail=tail, floor_us=floor_us,
                 feeder=feeder,
-                fused_ms=fused_ms, comparator=comparator, e2e_ms=e2e_ms, h2d=h2d, d2h=d2h)
+                fused_ms=fused_ms, comparator=comparator, e2e_ms=e2e_ms,
+                e2e_serial_ms=e2e_serial_ms, h2d=h2d, d2h=d2h)
 
 
 def feeder_measure(hpa, dev, stream, args, timed, n_tokens=65536):
@@ -559,7 +599,11 @@ def main():
             "speedup_vs_three_calls": round(r["ms"] / r["fused_ms"], 3)},
         "cpu_baseline": cpu,
         "e2e": {"value": round(per_batch_us(r["e2e_ms"], world), 2), "unit": UNIT,
-                "h2d_bytes_per_step": int(r["h2d"]), "d2h_bytes_per_step": int(r["d2h"])},
+                "h2d_bytes_per_step": int(r["h2d"]), "d2h_bytes_per_step": int(r["d2h"]),
+                "copies": "every step's input and result copies inside the timed region, on "
+                          "two copy streams with double-buffered device buffers, overlapping "
+                          "the neighbouring steps",
+                "serial_value": round(per_batch_us(r["e2e_serial_ms"], world), 2)},
         "gpu_launches": 3 * args.steps,
         "clocks": r["clocks"],
         "comparator": r["comparator"],
