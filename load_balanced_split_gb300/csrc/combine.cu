@@ -29,6 +29,34 @@ constexpr int kUnroll = 4;         // its segments in flight per round
 constexpr int kBlockWarps = 4;     // block-per-item kernel
 constexpr int kBlockUnroll = 4;
 
+// Request r's segment range [s0, s1) from the task map, checked before any partial is
+// read through it: false for a map with a non-zero status word, built for another
+// shape, or whose range for r is out of bounds (then reported as HPA_STATUS_BAD_MAP
+// by the thread with `report` set).
+__device__ __forceinline__ bool segment_range(int32_t *tm, int B, int C, int r, bool report,
+                                              int &s0, int &s1) {
+  s0 = s1 = 0;
+  if (!(tm[TM_STATUS] == 0 && tm[TM_B] == B && tm[TM_C] == C)) return false;
+  const TaskMapLayout lay = TaskMapLayout::make(B, C);
+  s0 = tm[lay.seg_off + r];
+  s1 = tm[lay.seg_off + r + 1];
+  const int S = tm[TM_S];
+  const bool good = s0 >= 0 && s0 < s1 && s1 <= S && S <= B + C - 1;
+  if (!good && report) status_or(tm, HPA_STATUS_BAD_MAP);
+  return good;
+}
+
+// The NaN output of one (request, token, head) item: lane i writes dims [4i, 4i+4).
+__device__ __forceinline__ void write_nan(__nv_bfloat16 *out, float *out_lse, int64_t item,
+                                          int lane) {
+  const float nan = CUDART_NAN_F;
+  const __nv_bfloat162 n2 = __floats2bfloat162_rn(nan, nan);
+  uint2 pk;
+  pk.x = pk.y = *reinterpret_cast<const uint32_t *>(&n2);
+  reinterpret_cast<uint2 *>(out + item * HEAD_DIM)[lane] = pk;
+  if (out_lse != nullptr && lane == 0) out_lse[item] = nan;
+}
+
 __global__ void __launch_bounds__(kItemsPerBlock * 32)
     combine_warp_kernel(const float *__restrict__ po, const float *__restrict__ plse,
                         int32_t *__restrict__ tm, int B, int C, int q_len, int Hq,
@@ -41,24 +69,9 @@ __global__ void __launch_bounds__(kItemsPerBlock * 32)
   const int r = static_cast<int>(item / per_req);
   const int64_t jg = item - r * per_req;
 
-  const TaskMapLayout lay = TaskMapLayout::make(B, C);
-  int s0 = 0, s1 = 0;
-  bool good = tm[TM_STATUS] == 0 && tm[TM_B] == B && tm[TM_C] == C;
-  if (good) {
-    // r's segment range, checked before any partial is read through it
-    s0 = tm[lay.seg_off + r];
-    s1 = tm[lay.seg_off + r + 1];
-    const int S = tm[TM_S];
-    good = s0 >= 0 && s0 < s1 && s1 <= S && S <= B + C - 1;
-    if (!good && lane == 0) status_or(tm, HPA_STATUS_BAD_MAP);
-  }
-  if (!good) {
-    const float nan = CUDART_NAN_F;
-    const __nv_bfloat162 n2 = __floats2bfloat162_rn(nan, nan);
-    uint2 pk;
-    pk.x = pk.y = *reinterpret_cast<const uint32_t *>(&n2);
-    reinterpret_cast<uint2 *>(out + item * HEAD_DIM)[lane] = pk;
-    if (out_lse != nullptr && lane == 0) out_lse[item] = nan;
+  int s0, s1;
+  if (!segment_range(tm, B, C, r, lane == 0, s0, s1)) {
+    write_nan(out, out_lse, item, lane);
     return;
   }
 
@@ -119,26 +132,9 @@ __global__ void __launch_bounds__(kBlockWarps * 32)
   __shared__ float s_max[kBlockWarps], s_w[kBlockWarps];
   __shared__ float4 s_acc[kBlockWarps][32];
 
-  const TaskMapLayout lay = TaskMapLayout::make(B, C);
-  int s0 = 0, s1 = 0;
-  bool good = tm[TM_STATUS] == 0 && tm[TM_B] == B && tm[TM_C] == C;
-  if (good) {
-    // r's segment range, checked before any partial is read through it
-    s0 = tm[lay.seg_off + r];
-    s1 = tm[lay.seg_off + r + 1];
-    const int S = tm[TM_S];
-    good = s0 >= 0 && s0 < s1 && s1 <= S && S <= B + C - 1;
-    if (!good && threadIdx.x == 0) status_or(tm, HPA_STATUS_BAD_MAP);
-  }
-  if (!good) {
-    if (w == 0) {
-      const float nan = CUDART_NAN_F;
-      const __nv_bfloat162 n2 = __floats2bfloat162_rn(nan, nan);
-      uint2 pk;
-      pk.x = pk.y = *reinterpret_cast<const uint32_t *>(&n2);
-      reinterpret_cast<uint2 *>(out + item * HEAD_DIM)[lane] = pk;
-      if (out_lse != nullptr && lane == 0) out_lse[item] = nan;
-    }
+  int s0, s1;
+  if (!segment_range(tm, B, C, r, threadIdx.x == 0, s0, s1)) {
+    if (w == 0) write_nan(out, out_lse, item, lane);
     return;
   }
 
