@@ -688,24 +688,26 @@ struct Tc {
         // row may not see and for padding rows.
         float a[MT][RH];
         auto scores = [&]() {
+          // The loaded registers are read only after tcgen05.wait::ld: a tile's hi terms
+          // land in a, its lo terms (E4M3) in u, and S = S(Q hi) + S(Q lo) / 16 (the lo
+          // term's fixed scale) is formed after the wait.
 #pragma unroll
-          for (int m = 0; m < MT; ++m)
+          for (int m = 0; m < MT; ++m) {
+            float u[KV == HPA_KV_E4M3 ? RH : 1];
 #pragma unroll
             for (int c = 0; c < RH / 8; ++c) {
               const uint32_t col = lane_t + ((S::kSBufs == 2 ? b : 0) * MT + m) * S::kNS + r0 + 8 * c;
-              float v[8];
-              tc_ld8(col, v);
-              if (KV == HPA_KV_E4M3) {  // S = S(Q hi) + S(Q lo) / 16 (the lo term's fixed scale)
-                float u[8];
-                tc_ld8(col + kRp, u);
-                const f32x2 k16 = pk(0.0625f, 0.0625f);
-#pragma unroll
-                for (int e = 0; e < 8; e += 2)
-                  upk(fma2(pk(u[e], u[e + 1]), k16, pk(v[e], v[e + 1])), v[e], v[e + 1]);
-              }
-#pragma unroll
-              for (int e = 0; e < 8; ++e) a[m][8 * c + e] = v[e];
+              tc_ld8(col, *reinterpret_cast<float(*)[8]>(&a[m][8 * c]));
+              if (KV == HPA_KV_E4M3) tc_ld8(col + kRp, *reinterpret_cast<float(*)[8]>(&u[8 * c]));
             }
+            if (KV == HPA_KV_E4M3) {
+              tc_wait_ld();
+              const f32x2 k16 = pk(0.0625f, 0.0625f);
+#pragma unroll
+              for (int e = 0; e < RH; e += 2)
+                upk(fma2(pk(u[e], u[e + 1]), k16, pk(a[m][e], a[m][e + 1])), a[m][e], a[m][e + 1]);
+            }
+          }
           tc_wait_ld();
 #pragma unroll
           for (int e4 = 0; e4 < RH; e4 += 4) {
