@@ -137,31 +137,34 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
 }
 
 // Bounded wait on an mbarrier phase: gives up after ~limit_ns and returns false.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
-                                                  uint64_t limit_ns = 2000000000ull) {
+// kRolled keeps the 64-retry loop between clock checks rolled: a few instructions at
+// each call site instead of 64 unrolled retries, for kernels whose hot loops hold many
+// waits (the tcgen05 attention kernel: 1974 -> 1872 us at 64 rows; the mma.sync
+// kernel was 2 % slower with it, so it keeps the unrolled form).
+template <bool kRolled>
+__device__ __forceinline__ bool mbar_wait_bounded_impl(uint32_t bar, uint32_t parity,
+                                                       uint64_t limit_ns) {
   if (mbar_try_wait(bar, parity)) return true;
   const uint64_t t0 = globaltimer_ns();
   for (;;) {
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
+    if constexpr (kRolled) {
+#pragma unroll 1
+      for (int i = 0; i < 64; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    } else {
+      for (int i = 0; i < 64; ++i)
+        if (mbar_try_wait(bar, parity)) return true;
+    }
     if (globaltimer_ns() - t0 > limit_ns) return false;
   }
 }
-
-// The same wait with its retry loop kept rolled: a few instructions at each call site
-// instead of 64 unrolled retries, for kernels whose hot loops hold many waits (the
-// tcgen05 attention kernel: 1974 -> 1872 us at 64 rows; the mma.sync kernel was 2 %
-// slower with it, so it keeps the unrolled form).
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  uint64_t limit_ns = 2000000000ull) {
+  return mbar_wait_bounded_impl<false>(bar, parity, limit_ns);
+}
 __device__ __forceinline__ bool mbar_wait_bounded_rolled(uint32_t bar, uint32_t parity,
                                                          uint64_t limit_ns = 2000000000ull) {
-  if (mbar_try_wait(bar, parity)) return true;
-  const uint64_t t0 = globaltimer_ns();
-  for (;;) {
-#pragma unroll 1
-    for (int i = 0; i < 64; ++i)
-      if (mbar_try_wait(bar, parity)) return true;
-    if (globaltimer_ns() - t0 > limit_ns) return false;
-  }
+  return mbar_wait_bounded_impl<true>(bar, parity, limit_ns);
 }
 
 __device__ __forceinline__ void fence_barrier_init() {
