@@ -71,6 +71,10 @@ __global__ void __launch_bounds__(kPlanThreads) plan_kernel(const int32_t *__res
   // Let the attention kernel that follows start its prologue now; it waits for
   // this grid's completion before it reads the map.
   pdl_launch_dependents();
+  // Launched with programmatic serialisation, this grid may start while the kernel
+  // before it (the previous step's combine, which reads the map) still runs: read the
+  // lengths and write the map only after that grid has completed.
+  pdl_wait();
   const TaskMapLayout lay = TaskMapLayout::make(B, C);
   int32_t *lens = tm + lay.lens, *cu_g = tm + lay.cu_tiles, *cb_g = tm + lay.cta_begin;
   int32_t *cs = tm + lay.cta_seg, *so = tm + lay.seg_off;
@@ -256,15 +260,36 @@ cudaError_t launch_plan(const int32_t *seq_lens, int B, int tile, int C, int kin
   const int staged = stage_bytes <= kPlanStageLimit;
   const size_t smem = staged ? stage_bytes : 0;
   const int need = B > C ? B : C;
-  if (need <= 32)
-    plan_kernel<32><<<1, 32, smem, s>>>(seq_lens, B, tile, C, kind, splits, tm, s_cap, staged);
-  else if (need <= 128)
-    plan_kernel<128><<<1, 128, smem, s>>>(seq_lens, B, tile, C, kind, splits, tm, s_cap, staged);
-  else if (need <= 256)
-    plan_kernel<256><<<1, 256, smem, s>>>(seq_lens, B, tile, C, kind, splits, tm, s_cap, staged);
-  else
-    plan_kernel<1024><<<1, 1024, smem, s>>>(seq_lens, B, tile, C, kind, splits, tm, s_cap, staged);
-  return cudaGetLastError();
+  // Programmatic dependent launch: the block's launch overlaps the end of the kernel
+  // before it, and pdl_wait() in the kernel orders every read and write after it.
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(1);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = s;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  const int32_t *lens = seq_lens;
+  if (need <= 32) {
+    cfg.blockDim = dim3(32);
+    return cudaLaunchKernelEx(&cfg, plan_kernel<32>, lens, B, tile, C, kind, splits, tm,
+                              static_cast<long long>(s_cap), staged);
+  }
+  if (need <= 128) {
+    cfg.blockDim = dim3(128);
+    return cudaLaunchKernelEx(&cfg, plan_kernel<128>, lens, B, tile, C, kind, splits, tm,
+                              static_cast<long long>(s_cap), staged);
+  }
+  if (need <= 256) {
+    cfg.blockDim = dim3(256);
+    return cudaLaunchKernelEx(&cfg, plan_kernel<256>, lens, B, tile, C, kind, splits, tm,
+                              static_cast<long long>(s_cap), staged);
+  }
+  cfg.blockDim = dim3(1024);
+  return cudaLaunchKernelEx(&cfg, plan_kernel<1024>, lens, B, tile, C, kind, splits, tm,
+                            static_cast<long long>(s_cap), staged);
 }
 
 }  // namespace hpa
