@@ -136,6 +136,23 @@ def per_batch_us(ms_per_step: float, world: int) -> float:
 
 
 # ----------------------------------------------------------------------------- our arm
+def traced_groups(rows: int, attn: str):
+    """Row groups of the CTA trace the bench can take for the kernel it times, or None.
+
+    hpa_decode_attn_traced runs the kernel hpa_decode_attn picks: the tcgen05 kernel
+    above 16 query rows per KV head (no row-group axis), else mma.sync (one CTA per
+    group of 16 rows); the all-heads variant traces itself.  A forced kernel that
+    differs from that choice has no trace."""
+    groups = (rows + 15) // 16
+    if attn == "allheads":
+        return groups
+    traced_tc = rows > 16
+    timed_tc = attn == "tc" or (attn == "auto" and rows > 16)
+    if timed_tc != traced_tc:
+        return None
+    return 1 if traced_tc else groups
+
+
 def step_distribution(step_ms):
     """Median and p10 / p90 of single-step times (µs), from the breakdown pass: events
     around every kernel of every step, so each step pays its own event overhead."""
@@ -252,13 +269,9 @@ def run_ours(args, rank, world, local_rank):
 
     def traced_tail(w, reps=3):
         """Per-CTA timestamps of the attention kernel (outside the timed region)."""
-        # the traced call runs the kernel hpa_decode_attn picks (tcgen05 above 16 rows);
-        # a forced choice that differs from it has no trace
-        rows = b.Hq // b.Hkv * b.q_len  # query rows per KV head
-        traced_tc = rows > 16 and not allh
-        if (tc or (rows > 16 and not mma and not allh)) != traced_tc:
+        groups_t = traced_groups(b.Hq // b.Hkv * b.q_len, args.attn)
+        if groups_t is None:
             return None
-        groups_t = 1 if traced_tc else groups
         heads_axis = 1 if allh else b.Hkv  # CTAs per partition and row group
         tr = torch.zeros(4 * w.num_ctas * heads_axis * groups, dtype=torch.int64, device=dev)
         out_t = None

@@ -81,3 +81,14 @@ def test_reference_line_contract(monkeypatch):
     assert line["e2e"] == {"value": 250000.0, "unit": bench.UNIT, "h2d_bytes_per_step": 0,
                            "d2h_bytes_per_step": 0}
     json.dumps(line)                                           # one JSON line
+
+
+@pytest.mark.parametrize("rows,attn,expect", [
+    (8, "auto", 1), (16, "auto", 1), (16, "mma", 1), (16, "tc", None),
+    (32, "auto", 1), (32, "tc", 1), (32, "mma", None), (64, "auto", 1),
+    (48, "allheads", 3), (8, "allheads", 1)])
+def test_traced_tail_follows_the_timed_kernel(rows, attn, expect):
+    """The tail is traced only when the traced call runs the kernel the bench times: the
+    tcgen05 kernel above 16 rows per KV head (one trace row per CTA), mma.sync up to 16
+    (one per row group), the all-heads variant always."""
+    assert bench.traced_groups(rows, attn) == expect
